@@ -1,0 +1,395 @@
+"""Pins for the CPU oracle: checks against facts that do not come from the oracle.
+
+Each ``pin_*`` function takes an ``oracle.Oracle`` handle and raises
+AssertionError on a mismatch. They check the oracle against closed forms,
+invariants of the routing, brute force on tiny inputs (every expert applied to
+every token, then masked), library routines (numpy / scipy / torch CPU in fp64)
+and values printed on the pages (``tests/golden``). ``test_oracle_pins.py``
+runs them on the normal build; ``test_oracle_plants.py`` runs them on builds
+with a deliberate mistake compiled in and requires that some pin fails.
+"""
+from __future__ import annotations
+
+import json
+import math
+import os
+from types import SimpleNamespace
+
+import numpy as np
+import scipy.special
+import torch
+import torch.nn.functional as Fn
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def wl(**kw):
+    base = dict(n_tokens=8, d_model=8, d_ff=16, n_experts=4, top_k=2, capacity_factor=0.0,
+                gating="softmax_topk", act="gelu", dtype="f32", has_bias=False, n_shared=0,
+                d_ff_shared=0, aux_alpha=0.01)
+    base.update(kw)
+    return SimpleNamespace(**base)
+
+
+def rand_layer(w, seed, scale_router=1.0):
+    """fp32 numpy tensors for a layer described by ``w`` (tiny sizes only)."""
+    rs = np.random.RandomState(seed)
+    N, d, F, E, S, Fs = w.n_tokens, w.d_model, w.d_ff, w.n_experts, w.n_shared, w.d_ff_shared
+    f = lambda *s: rs.standard_normal(s).astype(np.float32)
+    t = dict(x=f(N, d), w_router=(f(E, d) * scale_router).astype(np.float32), logit_bias=None,
+             w1=f(E, F, d) / np.float32(math.sqrt(d)), w2=f(E, d, F) / np.float32(math.sqrt(F)))
+    t["w3"] = f(E, F, d) / np.float32(math.sqrt(d)) if w.act == "swiglu" else None
+    t["b1"] = f(E, F) * np.float32(0.1) if w.has_bias else None
+    t["b2"] = f(E, d) * np.float32(0.1) if w.has_bias else None
+    if S:
+        t["ws1"] = f(S, Fs, d) / np.float32(math.sqrt(d))
+        t["ws3"] = f(S, Fs, d) / np.float32(math.sqrt(d)) if w.act == "swiglu" else None
+        t["ws2"] = f(S, d, Fs) / np.float32(math.sqrt(Fs))
+        t["bs1"] = f(S, Fs) * np.float32(0.1) if w.has_bias else None
+        t["bs2"] = f(S, d) * np.float32(0.1) if w.has_bias else None
+    return {k: (None if v is None else np.ascontiguousarray(v, np.float32)) for k, v in t.items()}
+
+
+# --- library-routine restatements used by the brute-force checks -------------
+def torch_expert(t, e, x64, act, has_bias, shared=False):
+    """One expert on rows x64 [n, d] with torch CPU fp64 library ops (F.linear, F.gelu, F.silu)."""
+    pre = "ws" if shared else "w"
+    bpre = "bs" if shared else "b"
+    W1 = torch.from_numpy(t[pre + "1"][e].astype(np.float64))
+    W2 = torch.from_numpy(t[pre + "2"][e].astype(np.float64))
+    xt = torch.from_numpy(x64)
+    if act == "gelu":
+        b1 = torch.from_numpy(t[bpre + "1"][e].astype(np.float64)) if has_bias else None
+        b2 = torch.from_numpy(t[bpre + "2"][e].astype(np.float64)) if has_bias else None
+        return Fn.linear(Fn.gelu(Fn.linear(xt, W1, b1)), W2, b2).numpy()
+    W3 = torch.from_numpy(t[pre + "3"][e].astype(np.float64))
+    return Fn.linear(Fn.silu(Fn.linear(xt, W1)) * Fn.linear(xt, W3), W2).numpy()
+
+
+def brute_force_layer(w, t, logits):
+    """Every expert on every token, then masked: the layer by its defining formula.
+
+    Top-k by a stable lexicographic sort, gates by scipy softmax, dropping by the
+    pages' own "nonzero in token order, keep the first C" formulation.
+    """
+    N, E, k = w.n_tokens, w.n_experts, w.top_k
+    x64 = t["x"].astype(np.float64)
+    L = logits.astype(np.float64)
+    dense = np.stack([torch_expert(t, e, x64, w.act, w.has_bias) for e in range(E)], axis=1)  # [N,E,d]
+    p = scipy.special.softmax(L, axis=1)
+    weight = np.zeros((N, E))
+    if w.gating == "expert_choice":
+        C = min(N, math.ceil(N * k * (w.capacity_factor if w.capacity_factor > 0 else 1.0) / E))
+        keys = p.astype(np.float32)  # selection keys: the fp32 softmax-over-experts probabilities
+        for e in range(E):
+            order = np.lexsort((np.arange(N), -keys[:, e].astype(np.float64)))
+            for tok in order[:C]:
+                weight[tok, e] = p[tok, e]
+    else:
+        order = np.lexsort((np.tile(np.arange(E), (N, 1)), -L), axis=1)[:, :k]  # desc value, asc index
+        if w.gating == "topk_softmax":
+            sel = np.take_along_axis(L, order, 1)
+            gsel = scipy.special.softmax(sel, axis=1)
+        else:
+            gsel = np.take_along_axis(p, order, 1)
+            if w.gating == "softmax_topk_renorm":
+                gsel = gsel / gsel.sum(1, keepdims=True)
+        C = math.ceil(N * k * w.capacity_factor / E) if w.capacity_factor > 0 else N
+        choice = order
+        for e in range(E):
+            mask = (choice == e)
+            index = np.nonzero(mask.any(axis=1))[0][:C]
+            for tok in index:
+                weight[tok, e] = gsel[tok][mask[tok]][0]
+    out = np.einsum("ne,ned->nd", weight, dense)
+    for s in range(w.n_shared):
+        out += torch_expert(t, s, x64, w.act, w.has_bias, shared=True)
+    return out
+
+
+# --- pins -------------------------------------------------------------------
+def pin_capacity(o):
+    """C = ceil(N*k*cf/E), no limit for cf <= 0 (hand-computed values)."""
+    cases = [  # (N, k, cf, E, C)
+        (64, 2, 1.25, 8, 20), (8192, 2, 1.25, 8, 2560), (8192, 6, 1.25, 160, 384),
+        (10, 1, 1.25, 8, 2), (16384, 8, 1.0, 256, 512), (100, 3, 0.0, 7, 100), (4, 4, 1.25, 2, 4),
+    ]
+    for N, k, cf, E, C in cases:
+        cfg = o.config(wl(n_tokens=N, top_k=min(k, E), n_experts=E, capacity_factor=cf), top_k=k)
+        assert o.capacity(cfg) == C, (N, k, cf, E, o.capacity(cfg), C)
+
+
+def pin_router_logits(o):
+    """Router logits equal numpy's fp64 matmul rounded to fp32 (within 1 ulp)."""
+    w = wl(n_tokens=13, d_model=24, n_experts=5)
+    t = rand_layer(w, 1)
+    t["logit_bias"] = np.linspace(0, 2, 5).astype(np.float32)
+    cfg = o.config(w)
+    L = o.router_logits(cfg, t["x"], o.weights(t))
+    ref = (t["x"].astype(np.float64) @ t["w_router"].astype(np.float64).T + t["logit_bias"]).astype(np.float32)
+    assert np.all(np.abs(L - ref) <= np.spacing(np.abs(ref))), np.max(np.abs(L - ref))
+
+
+def pin_softmax(o):
+    """Softmax and log-sum-exp equal scipy's."""
+    rs = np.random.RandomState(2)
+    L = (rs.standard_normal((9, 11)) * 5).astype(np.float32)
+    p, lse = o.softmax(L)
+    np.testing.assert_allclose(p, scipy.special.softmax(L.astype(np.float64), axis=1), rtol=1e-13, atol=1e-15)
+    np.testing.assert_allclose(lse, scipy.special.logsumexp(L.astype(np.float64), axis=1), rtol=1e-13)
+
+
+def pin_topk(o):
+    """Top-k by value descending, equal values to the lower expert index."""
+    L = np.array([[1, 3, 3, 2], [0, 0, 0, 0], [5, -1, 5, 5], [-2, -1, -3, -1]], np.float32)
+    assert o.topk(L, 2).tolist() == [[1, 2], [0, 1], [0, 2], [1, 3]]
+    assert o.topk(L, 4).tolist() == [[1, 2, 3, 0], [0, 1, 2, 3], [0, 2, 3, 1], [1, 3, 0, 2]]
+    rs = np.random.RandomState(3)
+    L = rs.randint(-3, 3, size=(50, 7)).astype(np.float32)  # many ties
+    for k in (1, 3, 7):
+        ref = np.lexsort((np.tile(np.arange(7), (50, 1)), -L), axis=1)[:, :k]
+        assert np.array_equal(o.topk(L, k), ref)
+
+
+def pin_gates(o):
+    """Gate variants: A = p[idx]; A' and B sum to 1 and agree; a two-expert closed form."""
+    rs = np.random.RandomState(4)
+    N, E, k = 20, 6, 3
+    L = (rs.standard_normal((N, E)) * 2).astype(np.float32)
+    idx = o.topk(L, k)
+    gA = o.gates(o.config(wl(n_tokens=N, n_experts=E, top_k=k, gating="softmax_topk")), L, idx)
+    gR = o.gates(o.config(wl(n_tokens=N, n_experts=E, top_k=k, gating="softmax_topk_renorm")), L, idx)
+    gB = o.gates(o.config(wl(n_tokens=N, n_experts=E, top_k=k, gating="topk_softmax")), L, idx)
+    p = scipy.special.softmax(L.astype(np.float64), axis=1)
+    np.testing.assert_allclose(gA, np.take_along_axis(p, idx, 1), rtol=1e-13)
+    np.testing.assert_allclose(gR.sum(1), 1.0, rtol=1e-14)
+    np.testing.assert_allclose(gB.sum(1), 1.0, rtol=1e-14)
+    np.testing.assert_allclose(gR, gB, rtol=1e-12)
+    assert np.all(gA.sum(1) < 1.0)
+    # logits (0, ln 3): top-2 order (1, 0), renormalised gates (3/4, 1/4); A gives the same here (k = E)
+    L2 = np.array([[0.0, math.log(3.0)]], np.float32)
+    i2 = o.topk(L2, 2)
+    assert i2.tolist() == [[1, 0]]
+    for g in ("softmax_topk", "softmax_topk_renorm", "topk_softmax"):
+        gg = o.gates(o.config(wl(n_tokens=1, n_experts=2, top_k=2, gating=g)), L2, i2)
+        np.testing.assert_allclose(gg[0], [0.75, 0.25], rtol=1e-7)
+
+
+def _check_assign_invariants(idx, a, C, E):
+    N, k = idx.shape
+    row_of, off, counts, kept = a["row_of"], a["expert_off"], a["counts"], a["kept"]
+    assert np.array_equal(counts, np.bincount(idx.ravel(), minlength=E))
+    assert np.all(kept == np.minimum(counts, C))
+    assert off[0] == 0 and np.array_equal(np.diff(off), kept)
+    R = int(off[-1])
+    assert R == N * k - a["dropped"]
+    rows = row_of[row_of >= 0]
+    assert np.array_equal(np.sort(rows), np.arange(R))  # bijection onto kept (t, j)
+    for e in range(E):
+        ts, js = np.nonzero((idx == e) & (row_of >= 0))
+        r = row_of[ts, js]
+        assert np.all((r >= off[e]) & (r < off[e + 1]))
+        assert np.all(np.diff(r) > 0) and np.all(np.diff(ts) > 0)  # token order inside the segment
+
+
+def pin_assign(o):
+    """Dropping keeps each expert's first C tokens in token order (the pages' nonzero()[:C])."""
+    rs = np.random.RandomState(5)
+    for N, E, k, cf in [(40, 4, 2, 1.0), (64, 8, 2, 1.25), (33, 5, 3, 0.6), (16, 6, 6, 1.25), (25, 3, 1, 0.0)]:
+        L = (rs.standard_normal((N, E)) + np.linspace(0, 2, E)).astype(np.float32)
+        idx = o.topk(L, k)
+        cfg = o.config(wl(n_tokens=N, n_experts=E, top_k=k, capacity_factor=cf))
+        C = o.capacity(cfg)
+        a = o.assign(cfg, idx, C)
+        _check_assign_invariants(idx, a, C, E)
+        for e in range(E):
+            mask = idx == e
+            index = np.nonzero(mask.any(axis=1))[0]
+            kept_tokens = set(index[:C].tolist())
+            got = set(np.nonzero(((idx == e) & (a["row_of"] >= 0)).any(axis=1))[0].tolist())
+            assert got == kept_tokens
+
+
+def pin_zero_router(o):
+    """W_r = 0: all logits tie, every token picks experts 0..k-1; closed-form gates and stats."""
+    N, E, k, cf = 40, 8, 2, 1.25
+    w = wl(n_tokens=N, d_model=8, n_experts=E, top_k=k, capacity_factor=cf)
+    t = rand_layer(w, 6)
+    t["w_router"][:] = 0
+    C = math.ceil(N * k * cf / E)  # 13
+    for gating, gexp in (("softmax_topk", 1.0 / E), ("softmax_topk_renorm", 1.0 / k), ("topk_softmax", 1.0 / k)):
+        cfg = o.config(w, gating=__import__("oracle").GATING[gating])
+        r = o.route(cfg, t["x"], o.weights(t))
+        assert np.all(r["idx"] == np.arange(k))
+        np.testing.assert_allclose(r["gate"], gexp, rtol=1e-14)
+        assert r["kept"].tolist() == [min(N, C)] * k + [0] * (E - k)
+        assert np.all(r["row_of"][C:] == -1) and np.all(r["row_of"][:C] >= 0)
+        assert r["dropped"] == k * (N - C)
+        st = r["stats"]
+        np.testing.assert_allclose(st["P"], 1.0 / E, rtol=1e-14)
+        np.testing.assert_allclose(st["aux_loss"], 0.01, rtol=1e-13)  # alpha exactly, whatever f is
+        np.testing.assert_allclose(st["z_loss"], math.log(E) ** 2, rtol=1e-13)
+        np.testing.assert_allclose(st["mean_lse_sq"], math.log(E) ** 2, rtol=1e-13)
+        np.testing.assert_allclose(st["f"], [0.5, 0.5] + [0.0] * (E - 2), rtol=1e-14)
+    cfg = o.config(w, gating=3, capacity_factor=1.0)
+    r = o.route(cfg, t["x"], o.weights(t))
+    C_ec = math.ceil(N * k / E)
+    assert np.array_equal(r["sel"], np.tile(np.arange(C_ec), (E, 1)))  # ties -> lowest token ids
+
+
+def pin_uniform_usage(o):
+    """Cyclic routing makes f uniform, so aux = alpha * sum P = alpha for any P."""
+    N, E, k = 32, 8, 2
+    L = np.zeros((N, E), np.float32)
+    for t_ in range(N):
+        for j in range(k):
+            L[t_, (t_ * k + j) % E] = 5.0 - j
+    L += (np.random.RandomState(7).standard_normal((N, E)) * 0.1).astype(np.float32)
+    cfg = o.config(wl(n_tokens=N, n_experts=E, top_k=k))
+    r = o.route(cfg, None, None, logits=L)
+    np.testing.assert_allclose(r["stats"]["f"], 1.0 / E, rtol=1e-14)
+    np.testing.assert_allclose(r["stats"]["aux_loss"], 0.01, rtol=1e-12)
+    # the loss grows when usage concentrates: all tokens on one expert pair
+    L2 = np.zeros((N, E), np.float32)
+    L2[:, 0], L2[:, 1] = 3.0, 2.0
+    r2 = o.route(cfg, None, None, logits=L2)
+    assert r2["stats"]["aux_loss"] > 0.01
+
+
+def pin_stats_formula(o):
+    """f, P, aux, z against scipy on random logits (library routines)."""
+    rs = np.random.RandomState(8)
+    N, E, k = 30, 6, 2
+    L = (rs.standard_normal((N, E)) * 3).astype(np.float32)
+    cfg = o.config(wl(n_tokens=N, n_experts=E, top_k=k, aux_alpha=0.02))
+    r = o.route(cfg, None, None, logits=L)
+    L64 = L.astype(np.float64)
+    P = scipy.special.softmax(L64, axis=1).mean(0)
+    onehot = np.zeros((N, k, E))
+    np.put_along_axis(onehot, r["idx"][:, :, None].astype(np.int64), 1.0, axis=2)
+    f = onehot.mean(axis=(0, 1))
+    np.testing.assert_allclose(r["stats"]["P"], P, rtol=1e-12)
+    np.testing.assert_allclose(r["stats"]["f"], f, rtol=1e-14)
+    np.testing.assert_allclose(r["stats"]["aux_loss"], 0.02 * E * (f * P).sum(), rtol=1e-12)
+    lse = scipy.special.logsumexp(L64, axis=1)
+    np.testing.assert_allclose(r["stats"]["z_loss"], lse.mean() ** 2, rtol=1e-12)
+    np.testing.assert_allclose(r["stats"]["mean_lse_sq"], (lse ** 2).mean(), rtol=1e-12)
+
+
+def pin_single_expert_is_dense_ffn(o):
+    """E = 1, k = 1, no cap: the layer is one dense FFN with gate 1 (torch F.linear/gelu/silu, fp64)."""
+    for act, bias in (("gelu", True), ("gelu", False), ("swiglu", False)):
+        w = wl(n_tokens=7, d_model=12, d_ff=20, n_experts=1, top_k=1, act=act, has_bias=bias)
+        t = rand_layer(w, 9)
+        cfg = o.config(w)
+        ow = o.weights(t)
+        r = o.route(cfg, t["x"], ow)
+        out = o.outputs(cfg, t["x"], ow, r)
+        ref = torch_expert(t, 0, t["x"].astype(np.float64), act, bias)
+        np.testing.assert_allclose(out, ref, rtol=1e-12, atol=1e-13)
+
+
+def pin_activation_zero(o):
+    """gelu(0) = silu(0) = 0: with x = 0 a GELU expert returns b2 and a SwiGLU expert 0."""
+    w = wl(n_tokens=1, d_model=8, d_ff=16, n_experts=2, top_k=1, act="gelu", has_bias=True)
+    t = rand_layer(w, 10)
+    t["b1"][:] = 0
+    ow = o.weights(t)
+    y = o.expert_apply(o.config(w), ow, 1, np.zeros(8))
+    np.testing.assert_array_equal(y, t["b2"][1].astype(np.float64))
+    w2 = wl(n_tokens=1, d_model=8, d_ff=16, n_experts=2, top_k=1, act="swiglu")
+    t2 = rand_layer(w2, 11)
+    y2 = o.expert_apply(o.config(w2), o.weights(t2), 0, np.zeros(8))
+    np.testing.assert_array_equal(y2, 0.0)
+
+
+def pin_brute_force(o):
+    """Sparse dispatch equals dense-then-mask on tiny layers, every gating, k = 1..E, with and without drops."""
+    case = 0
+    for gating in ("softmax_topk", "softmax_topk_renorm", "topk_softmax", "expert_choice"):
+        for act, bias in (("gelu", True), ("swiglu", False)):
+            for E in (1, 3, 6):
+                for k in sorted({1, 2, E}):
+                    if k > E:
+                        continue
+                    for cf in ((0.0, 1.0) if gating != "expert_choice" else (1.0, 0.5)):
+                        case += 1
+                        N = 5 + (case * 7) % 12
+                        w = wl(n_tokens=N, d_model=8, d_ff=12, n_experts=E, top_k=k, gating=gating,
+                               act=act, has_bias=bias, capacity_factor=cf,
+                               n_shared=case % 3 == 0 and 1 or 0, d_ff_shared=8)
+                        t = rand_layer(w, 100 + case, scale_router=2.0)
+                        cfg = o.config(w)
+                        ow = o.weights(t)
+                        r = o.route(cfg, t["x"], ow)
+                        out = o.outputs(cfg, t["x"], ow, r)
+                        ref = brute_force_layer(w, t, r["logits"])
+                        np.testing.assert_allclose(out, ref, rtol=1e-11, atol=1e-12, err_msg=str(w))
+
+
+def pin_dense_softmax_mixture(o):
+    """k = E, no cap, gating A: the layer is the softmax-weighted sum of every expert."""
+    w = wl(n_tokens=9, d_model=8, d_ff=12, n_experts=5, top_k=5)
+    t = rand_layer(w, 12, scale_router=2.0)
+    cfg = o.config(w)
+    ow = o.weights(t)
+    r = o.route(cfg, t["x"], ow)
+    out = o.outputs(cfg, t["x"], ow, r)
+    x64 = t["x"].astype(np.float64)
+    p = scipy.special.softmax(r["logits"].astype(np.float64), axis=1)
+    ref = sum(p[:, e:e + 1] * torch_expert(t, e, x64, "gelu", False) for e in range(5))
+    np.testing.assert_allclose(out, ref, rtol=1e-12, atol=1e-13)
+
+
+def pin_expert_choice(o):
+    """Expert choice: exactly C tokens per expert, the top-C by key (ties to lower t), ascending."""
+    rs = np.random.RandomState(13)
+    N, E, k = 37, 5, 2
+    keys = rs.randint(0, 6, size=(N, E)).astype(np.float32)  # many ties
+    cfg = o.config(wl(n_tokens=N, n_experts=E, top_k=k, gating="expert_choice", capacity_factor=1.0))
+    C = o.capacity(cfg)
+    assert C == math.ceil(N * k / E)
+    sel = o.expert_choice(cfg, keys, C)
+    for e in range(E):
+        ref = np.sort(np.lexsort((np.arange(N), -keys[:, e]))[:C])
+        assert np.array_equal(sel[e], ref)
+    L = rs.standard_normal((N, E)).astype(np.float32)
+    r = o.route(cfg, None, None, logits=L)
+    np.testing.assert_allclose(r["stats"]["f"], 1.0 / E, rtol=1e-14)
+    np.testing.assert_allclose(r["stats"]["aux_loss"], 0.01, rtol=1e-12)  # alpha * sum P
+
+
+def pin_bf16_inputs_and_mimic(o):
+    """bf16 storage widens exactly; mimic rounding gives bf16 values close to the exact output."""
+    w = wl(n_tokens=6, d_model=16, d_ff=32, n_experts=3, top_k=2, dtype="bf16", act="swiglu")
+    t32 = rand_layer(w, 14)
+    tb = {k: (None if v is None else torch.from_numpy(v).to(torch.bfloat16)) for k, v in t32.items()}
+    as_u16 = {k: (None if v is None else v.view(torch.int16).numpy().view(np.uint16)) for k, v in tb.items()}
+    as_f32 = {k: (None if v is None else v.float().numpy()) for k, v in tb.items()}
+    cfg_b = o.config(w)
+    cfg_f = o.config(w, dtype=0)
+    rb = o.route(cfg_b, as_u16["x"], o.weights(as_u16))
+    rf = o.route(cfg_f, as_f32["x"], o.weights(as_f32))
+    assert np.array_equal(rb["logits"], rf["logits"])
+    ob = o.outputs(cfg_b, as_u16["x"], o.weights(as_u16), rb)
+    of = o.outputs(cfg_f, as_f32["x"], o.weights(as_f32), rf)
+    np.testing.assert_array_equal(ob, of)
+    cfg_m = o.config(w, mimic_bf16=1)
+    om = o.outputs(cfg_m, as_u16["x"], o.weights(as_u16), rb)
+    assert np.array_equal(om, torch.from_numpy(om).float().to(torch.bfloat16).double().numpy())
+    rms = np.sqrt((of ** 2).mean())
+    assert np.max(np.abs(om - of)) <= 2e-2 * rms
+
+
+def pin_page_entropy(o):
+    """The collapse-detector entropies the aigrafen.se page prints."""
+    g = json.load(open(os.path.join(GOLDEN, "routing_entropy.json")))
+    for case in g["cases"]:
+        assert round(o.entropy(case["distribution"]), 3) == case["entropy"], case
+    assert round(math.log(8), 3) == g["maximum"]
+
+
+ALL_PINS = [pin_capacity, pin_router_logits, pin_softmax, pin_topk, pin_gates, pin_assign, pin_zero_router,
+            pin_uniform_usage, pin_stats_formula, pin_single_expert_is_dense_ffn, pin_activation_zero,
+            pin_brute_force, pin_dense_softmax_mixture, pin_expert_choice, pin_bf16_inputs_and_mimic,
+            pin_page_entropy]
