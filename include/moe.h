@@ -1,0 +1,264 @@
+/*
+ * moe.h -- C ABI of the B300 (sm_103a) top-k Mixture-of-Experts layer forward.
+ *
+ * The layer: router logits -> softmax / top-k gates (+ balancing statistics)
+ * -> per-expert capacity with in-token-order dropping -> permute into
+ * expert-contiguous rows -> expert FFNs (GELU with bias, or SwiGLU; optional
+ * always-on shared experts) -> gate-weighted combine back into token order.
+ * Definitions follow these pages (cited by title and section):
+ *   [AIG] "Mixture of Experts" (aigrafen.se): gate formula y = sum_{top-k} g_i E_i(x),
+ *         g = softmax(W_r x); auxiliary loss; expert capacity; MoE module code.
+ *   [AIE] "Mixture of Experts (MoE)" (wiki.ai-engineering.at): router, softmax, top-k,
+ *         weighted combination; "Gather/scatter outputs from experts".
+ *   [VAN] "MoE Architecture" (vanos001.github.io): TokenChoiceRouter (top-k on logits,
+ *         softmax over k), ExpertChoiceRouter, SwiGLUExpert / StandardExpert,
+ *         CapacityManagedMoE, HybridMoE (shared experts), "Efficient Batched MoE".
+ *   [STP] "Mixture of Experts (MoE)" (learn.starphix.com): "Key Equations",
+ *         "Load Balancing (Critical)" (aux loss, z-loss), "Shared + Specialized".
+ *
+ * Conventions for every entry point:
+ *  - All tensor pointers are DEVICE pointers owned by the caller, row-major,
+ *    16-byte aligned, and stay owned by the caller. The library allocates and
+ *    frees nothing and never synchronises the stream (except
+ *    moe_get_device_status). Work is enqueued on `stream` (a cudaStream_t;
+ *    NULL = the legacy default stream) and the call returns before it runs.
+ *  - "dtype" tensors hold fp32 (MOE_DT_F32) or bf16 (MOE_DT_BF16) elements as
+ *    cfg->dtype says; index tensors are int32; gates/probabilities fp32.
+ *  - Argument errors are detected on the host before anything is launched and
+ *    returned synchronously (MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED,
+ *    MOE_ERR_WORKSPACE). A launch failure returns MOE_ERR_CUDA. Conditions
+ *    found on the device (an index out of range, a pipeline wait that ran out
+ *    of time) set a sticky error word in the workspace; read it with
+ *    moe_get_device_status. No kernel traps or spins without a bound.
+ *  - `ws` is a caller-allocated device workspace of at least
+ *    moe_workspace_size() bytes (256-byte aligned), initialised once with
+ *    moe_workspace_init(). Every stage call with the same cfg may share one
+ *    workspace; calls that run concurrently must not.
+ *  - Limits: 1 <= k <= min(E, 32); E <= 512; N*k < 2^31; bf16 layers need
+ *    d % 64 == 0, F % 64 == 0 and Fs % 64 == 0; fp32 layers need d % 4 == 0.
+ *    SwiGLU experts take no biases. Expert choice needs N <= 1<<20.
+ */
+#ifndef MOE_B300_H
+#define MOE_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_ABI_VERSION 1
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+typedef enum moe_status {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, size out of range          */
+  MOE_ERR_UNSUPPORTED = 2,  /* valid layer this build does not run (see Limits)     */
+  MOE_ERR_WORKSPACE = 3,    /* ws smaller than moe_workspace_size()                 */
+  MOE_ERR_CUDA = 4,         /* a CUDA runtime/driver call or launch failed          */
+  MOE_ERR_DEVICE_CHECK = 5, /* a kernel found an out-of-range index (sticky word)   */
+  MOE_ERR_TIMEOUT = 6       /* a kernel's bounded pipeline wait ran out (sticky)    */
+} moe_status;
+
+/* Gate rule. [AIG] formula / [AIE]: g = top-k of softmax(L) (A, no renormalisation);
+ * [AIG] MoE code: the chosen weights divided by their sum (A');
+ * [VAN] TokenChoiceRouter / [STP] TopKRouter / [AIE] MoELayer: top-k on the logits,
+ * then a softmax over those k (B); [VAN] ExpertChoiceRouter: every expert takes its
+ * top-C tokens by softmax probability (EC). Top-k ranks logits descending, equal
+ * logits to the lower expert index. */
+typedef enum moe_gating {
+  MOE_GATE_SOFTMAX_TOPK = 0,
+  MOE_GATE_SOFTMAX_TOPK_RENORM = 1,
+  MOE_GATE_TOPK_SOFTMAX = 2,
+  MOE_GATE_EXPERT_CHOICE = 3
+} moe_gating;
+
+/* Expert FFN. [AIG] MoE experts / [VAN] StandardExpert: W2 gelu(W1 x + b1) + b2 (exact
+ * erf GELU; biases optional). [VAN] SwiGLUExpert / [STP] Expert: W2 (silu(W1 x) * W3 x). */
+typedef enum moe_act { MOE_ACT_GELU = 0, MOE_ACT_SWIGLU = 1 } moe_act;
+
+typedef enum moe_dtype { MOE_DT_F32 = 0, MOE_DT_BF16 = 1 } moe_dtype;
+
+/* Layer description (plain data, 80 bytes). */
+typedef struct moe_config {
+  int64_t n_tokens;      /* N: tokens (B*T flattened)                                 */
+  int64_t d_model;       /* d                                                         */
+  int64_t d_ff;          /* F: routed expert hidden size                              */
+  int64_t n_experts;     /* E: routed experts                                         */
+  int64_t n_shared;      /* S: always-on shared experts (0 = none)                    */
+  int64_t d_ff_shared;   /* Fs: shared expert hidden size                             */
+  int64_t top_k;         /* k (expert choice: average experts per token, sets C)      */
+  float capacity_factor; /* cf. Token choice: C = ceil(N*k*cf/E), cf <= 0 = no limit.
+                            Expert choice: C = min(N, ceil(N*k*cf/E)), cf <= 0 = 1.
+                            [AIG] "Expert capacity"; [VAN] CapacityManagedMoE.        */
+  int32_t gating;        /* moe_gating                                                */
+  int32_t act;           /* moe_act                                                   */
+  int32_t dtype;         /* moe_dtype of x, weights, biases, outputs                  */
+  int32_t has_bias;      /* GELU experts: b1/b2 (and bs1/bs2) present                 */
+  float aux_alpha;       /* alpha of the auxiliary loss ([AIG]: ~0.01)                */
+} moe_config;
+
+/* Weights, nn.Linear [out, in] layout, all device pointers of cfg->dtype except
+ * logit_bias (fp32). Unused entries may be NULL. */
+typedef struct moe_weights {
+  const void* w_router;    /* [E, d]   router, no bias ([AIG], [VAN], [STP])          */
+  const float* logit_bias; /* [E] fp32 constant added to every token's logits, or NULL */
+  const void* w1;          /* [E, F, d]                                               */
+  const void* w3;          /* [E, F, d] SwiGLU only                                   */
+  const void* b1;          /* [E, F]   GELU with bias only                            */
+  const void* w2;          /* [E, d, F]                                               */
+  const void* b2;          /* [E, d]   GELU with bias only                            */
+  const void* ws1;         /* [S, Fs, d] shared experts                               */
+  const void* ws3;         /* [S, Fs, d] shared, SwiGLU only                          */
+  const void* bs1;         /* [S, Fs]  shared, GELU with bias only                    */
+  const void* ws2;         /* [S, d, Fs] shared                                       */
+  const void* bs2;         /* [S, d]   shared, GELU with bias only                    */
+} moe_weights;
+
+/* Router statistics, written to a caller-owned DEVICE buffer of
+ * moe_stats_bytes(E) bytes: this 32-byte header, then float f[E], float P[E],
+ * int32 counts[E], int32 kept[E].
+ *   f_e   = share of the N*k assignments routed to e before dropping
+ *   P_e   = mean over tokens of softmax(L)[t, e]
+ *   aux   = alpha * E * sum_e f_e P_e        ([AIG] L_aux; [STP] load_balancing_loss)
+ *   z     = (mean_t logsumexp_e L[t, e])^2   ([STP] z_loss)
+ *   mean_lse_sq = mean_t logsumexp^2
+ *   dropped = assignments over capacity ([AIG] "dropped_share" = dropped/(N*k))
+ * moe_route writes aux, z, mean_lse_sq, f, P, counts; moe_permute writes
+ * dropped, dropped_share, capacity, rows, kept. */
+typedef struct moe_stats_header {
+  float aux_loss;
+  float z_loss;
+  float mean_lse_sq;
+  float dropped_share;
+  int32_t dropped;
+  int32_t capacity;
+  int32_t rows; /* R: kept (token, expert) rows */
+  int32_t n_experts;
+} moe_stats_header;
+
+/* Byte offsets of the intermediate buffers inside a workspace (for callers and
+ * tests that want to read them after moe_forward). */
+typedef struct moe_workspace_layout {
+  size_t total_bytes;
+  size_t status;      /* int32[4] sticky device error word                     */
+  size_t logits;      /* fp32 [N, E] router logits                              */
+  size_t probs;       /* fp32 [N, E] softmax probabilities (expert choice)      */
+  size_t idx;         /* int32 token choice [N, k]; expert choice [E, C]        */
+  size_t gate;        /* fp32, same shape as idx                                */
+  size_t tok_rows;    /* int32 token choice [N, k] (-1 dropped); EC [E*C]       */
+  size_t tok_off;     /* int32 [N+1] (expert choice)                            */
+  size_t expert_off;  /* int32 [E+1]                                            */
+  size_t row_token;   /* int32 [max_rows]                                       */
+  size_t row_gate;    /* fp32 [max_rows]                                        */
+  size_t xp;          /* dtype [max_rows, d] permuted tokens                    */
+  size_t h;           /* dtype [max_rows, F] routed hidden activations          */
+  size_t hs;          /* dtype [N, S*Fs] shared hidden activations              */
+  size_t yp;          /* dtype [max_rows, d] gate-scaled expert outputs         */
+  size_t ys;          /* dtype [N, d] sum of shared expert outputs              */
+  size_t stats;       /* moe_stats_bytes(E) used when the caller passes none    */
+  size_t scratch;     /* per-kernel partial sums and tile counts                */
+  int64_t max_rows;   /* token choice N*k; expert choice E*C                    */
+  int64_t capacity;   /* C (token choice without a limit: N)                    */
+} moe_workspace_layout;
+
+/* ABI version of the loaded library (MOE_ABI_VERSION at build time). */
+MOE_API int32_t moe_abi_version(void);
+
+/* Human-readable name of a status code (static string). */
+MOE_API const char* moe_status_string(moe_status s);
+
+/* Bytes of the device statistics buffer for E routed experts. */
+MOE_API size_t moe_stats_bytes(int64_t n_experts);
+
+/* Validates cfg (no CUDA call) and returns the workspace size in *bytes. */
+MOE_API moe_status moe_workspace_size(const moe_config* cfg, size_t* bytes);
+
+/* Validates cfg (no CUDA call) and fills *layout. */
+MOE_API moe_status moe_workspace_layout_of(const moe_config* cfg, moe_workspace_layout* layout);
+
+/* Zeroes the workspace's device error word (enqueued on stream). Call once on a
+ * freshly allocated workspace. */
+MOE_API moe_status moe_workspace_init(const moe_config* cfg, void* ws, size_t ws_bytes, void* stream);
+
+/* Router, gates and balancing statistics (hot-path steps: router GEMM, softmax,
+ * log-sum-exp, top-k, gates, statistics). [STP] "Key Equations"; [AIG] formula and
+ * MoE code; [VAN] TokenChoiceRouter / ExpertChoiceRouter.
+ *  x      [N, d] dtype
+ *  idx    token choice: [N, k] int32 expert ids, rank order (largest logit first).
+ *         expert choice: [E, C] int32 token ids, ascending within each expert.
+ *  gate   fp32, same shape as idx: the gate of each choice (expert choice: p[t, e]).
+ *  logits [N, E] fp32 or NULL; probs [N, E] fp32 softmax or NULL.
+ *  stats  moe_stats buffer or NULL. */
+MOE_API moe_status moe_route(const moe_config* cfg, const void* x, const moe_weights* w, int32_t* idx,
+                     float* gate, float* logits, float* probs, void* stats, void* ws, size_t ws_bytes,
+                     void* stream);
+
+/* Capacity, dropping and permutation ([AIG] "Expert capacity" and MoE code's
+ * nonzero()[:capacity]; [AIE] "Gather/scatter"). Kept (token, choice) pairs are
+ * numbered expert by expert, in token order inside each expert; row r of xp is
+ * x[row_token[r]].
+ *  x          [N, d] dtype;  idx / gate as written by moe_route.
+ *  xp         [max_rows, d] dtype: rows [0, R) written.
+ *  tok_rows   token choice: [N, k] row of each choice or -1 if dropped.
+ *             expert choice: [E*C] rows listed token by token (ascending expert id).
+ *  tok_off    expert choice: [N+1] start of each token's list in tok_rows
+ *             (token choice: may be NULL, unused).
+ *  expert_off [E+1] int32 first row of each expert (exclusive prefix of kept counts).
+ *  row_token  [max_rows] int32; row_gate [max_rows] fp32 (the row's gate).
+ *  stats      moe_stats buffer or NULL (kept/dropped/rows/capacity). */
+MOE_API moe_status moe_permute(const moe_config* cfg, const void* x, const int32_t* idx, const float* gate, void* xp,
+                       int32_t* tok_rows, int32_t* tok_off, int32_t* expert_off, int32_t* row_token,
+                       float* row_gate, void* stats, void* ws, size_t ws_bytes, void* stream);
+
+/* Grouped expert FFNs over the expert-contiguous rows, and the shared experts
+ * over all tokens ([VAN] SwiGLUExpert / StandardExpert / HybridMoE;
+ * [VAN] "Efficient Batched MoE": one grouped computation instead of a loop).
+ *  xp         [max_rows, d]; expert_off [E+1] (device; read on the device only).
+ *  row_gate   [max_rows] fp32: yp row r = row_gate[r] * E_e(xp[r]).
+ *  x          [N, d] (needed when S > 0).
+ *  yp         [max_rows, d] dtype: rows [0, R) written.
+ *  ys         [N, d] dtype: sum of the shared experts (written when S > 0). */
+MOE_API moe_status moe_expert_ffn(const moe_config* cfg, const void* xp, const int32_t* expert_off,
+                          const float* row_gate, const void* x, const moe_weights* w, void* yp, void* ys,
+                          void* ws, size_t ws_bytes, void* stream);
+
+/* Combine into token order ([AIG] out[index] += w * expert(x); [VAN] HybridMoE):
+ * out[t] = ys[t] + sum of yp over the token's rows, in fixed order (token choice:
+ * j = 0..k-1 skipping dropped; expert choice: ascending expert id), fp32
+ * accumulation and one rounding. Tokens with no kept row get ys[t] (or 0).
+ *  tok_rows / tok_off as written by moe_permute; ys may be NULL. out [N, d] dtype. */
+MOE_API moe_status moe_combine(const moe_config* cfg, const void* yp, const int32_t* tok_rows, const int32_t* tok_off,
+                       const void* ys, void* out, void* stream);
+
+/* The whole layer: moe_route -> moe_permute -> moe_expert_ffn -> moe_combine with
+ * every intermediate in ws (see moe_workspace_layout_of). out [N, d] dtype.
+ * stats: moe_stats buffer or NULL (then written inside ws). No host sync. */
+MOE_API moe_status moe_forward(const moe_config* cfg, const void* x, const moe_weights* w, void* out, void* stats,
+                       void* ws, size_t ws_bytes, void* stream);
+
+/* moe_forward that also records caller-created CUDA events (cudaEvent_t) on
+ * `stream`: events[0] before the first kernel and events[i] after the i-th
+ * stage (route, permute, expert up-projection, expert down-projection,
+ * combine); n_events <= 6 are used, extra ones ignored. For timing stages. */
+MOE_API moe_status moe_forward_traced(const moe_config* cfg, const void* x, const moe_weights* w, void* out,
+                              void* stats, void* ws, size_t ws_bytes, void* stream, void* const* events,
+                              int32_t n_events);
+
+/* Synchronises `stream`, reads and clears the workspace's device error word.
+ * *device_error receives the raw word (0 = none). Returns MOE_OK, or
+ * MOE_ERR_DEVICE_CHECK / MOE_ERR_TIMEOUT when a kernel recorded one. */
+MOE_API moe_status moe_get_device_status(const moe_config* cfg, void* ws, size_t ws_bytes, void* stream,
+                                 int32_t* device_error);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_B300_H */

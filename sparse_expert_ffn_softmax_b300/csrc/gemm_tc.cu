@@ -1,0 +1,700 @@
+// Grouped expert GEMMs for bf16 layers on the 5th-generation tensor cores
+// (tcgen05.mma, accumulators in tensor memory, operands staged by TMA).
+//
+// Pages: "MoE Architecture" (vanos001.github.io) "Efficient Batched MoE" (one
+// grouped computation over the experts instead of a per-expert loop),
+// SwiGLUExpert / StandardExpert, HybridMoE (shared expert on every token);
+// "Mixture of Experts" (aigrafen.se) MoE code (out[index] += w * expert(x));
+// "Mixture of Experts (MoE)" (learn.starphix.com) "Shared + Specialized".
+//
+// One launch computes every tile of two families of groups:
+//   up-projection   family 0: expert e's rows of xp  x  W1[e] (+W3[e])  -> H
+//                   family 1: all tokens of x  x  Ws1[s] (+Ws3[s])      -> Hs[:, s*Fs...]
+//   down-projection family 0: expert e's rows of H   x  W2[e]           -> Yp (x row gate)
+//                   family 1: all tokens of Hs x [Ws2[0] | Ws2[1] | ...] -> Ys (the shared
+//                             experts concatenated along K, so their sum comes out of one
+//                             accumulator)
+// A group's rows come from the device-side expert offsets, so no host sync is
+// needed; every CTA builds the same tile prefix over the groups and walks tiles
+// blockIdx.x, blockIdx.x + gridDim.x, ... (persistent, one CTA per SM).
+//
+// Tile 128 x BN x 64, K-major operands in 128-byte-swizzled shared memory.
+// Warp roles: warp 0 issues TMA loads into a STAGES-deep ring, warp 1 issues
+// tcgen05.mma (M=128, N=BN, K=16) into one of two TMEM accumulators, warps 2-9
+// drain the other accumulator with tcgen05.ld (warp w reads TMEM lanes
+// 32*(w%4)...), apply the epilogue (GELU + bias, SiLU x gate, or bias x row gate),
+// convert to bf16 and store. SwiGLU tiles load BN/2 rows of W1 and BN/2 rows of
+// W3 into one BN-row B tile, so one MMA fills both halves of the accumulator.
+//
+// Every mbarrier wait is bounded by the global timer; on expiry the CTA records
+// MOE_ERR_TIMEOUT in the workspace error word, waits (bounded) for its own TMA
+// copies and MMAs in flight, frees its TMEM and exits.
+#include <cuda.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+namespace tc {
+
+constexpr int BM = 128;
+constexpr int BK = 64;  // one 128-byte swizzle atom of bf16
+constexpr int UMMA_K = 16;
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 64 + kEpiWarps * 32;
+constexpr int kMaxGroups = 512 + 64;  // E <= 512 routed + S <= 64 shared groups
+constexpr unsigned long long kTimeoutNs = 2000000000ull;
+
+enum Epi { kGelu = 0, kSwiglu = 1, kLinear = 2 };
+
+struct Family {
+  int32_t groups;       // groups in the family (0 = unused)
+  int32_t m_from_off;   // 1: group g has rows [off[g], off[g+1]); 0: rows [0, m_fixed)
+  int32_t m_fixed;
+  int32_t n_tiles;      // output column tiles per group
+  int32_t k_blocks;     // K / BK
+  int32_t kseg_blocks;  // B is cut along K into segments of this many blocks
+  int32_t b_rows_group; // B-map row offset of group g: g * b_rows_group
+  int32_t b_rows_kseg;  // B-map row offset of K segment s: s * b_rows_kseg
+  int32_t a_map, b_map, b3_map;
+  int32_t pad0;
+  void* out;
+  int64_t ld_out;         // elements between output rows
+  int64_t out_col_group;  // output column offset of group g: g * out_col_group
+  const __nv_bfloat16* bias;
+  int64_t bias_group;       // bias offset of group g
+  int64_t bias_sum_stride;  // stride between summed bias vectors
+  int32_t bias_nsum;        // bias vectors summed per column (0 = no bias)
+  int32_t pad1;
+  const float* row_gate;  // per output row scale, or null
+};
+
+struct Params {
+  Family fam[2];
+  const int32_t* expert_off;
+  int32_t* status;
+};
+
+// ---- PTX wrappers -----------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ unsigned long long globaltimer() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n"
+      ".reg .pred p;\n"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      "selp.u32 %0, 1, 0, p;\n"
+      "}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait: false after kTimeoutNs or once another role has aborted.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int32_t* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer() - t0 > kTimeoutNs) return false;
+  }
+}
+__device__ __forceinline__ void tma_load_2d(const CUtensorMap* map, uint64_t* bar, void* dst, int32_t x,
+                                            int32_t y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y)
+      : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+// D[tmem] (+)= A[smem desc] * B[smem desc]^T, bf16 inputs, fp32 accumulate.
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n"
+      ".reg .pred p;\n"
+      "setp.ne.b32 p, %4, 0;\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n"
+      "}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrive on bar once every tcgen05.mma issued so far by this thread has completed.
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+// 32 lanes x 32 consecutive fp32 columns: thread i of the warp gets lane (base lane + i).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+// Waits for this thread's tcgen05.ld results; the registers are in/out operands so
+// no use of them can be scheduled before the wait.
+__device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                 "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]),
+                 "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]),
+                 "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+               :
+               : "memory");
+}
+// Orders the registers r after an earlier wait without waiting again.
+__device__ __forceinline__ void reg_fence(uint32_t (&r)[32]) {
+  asm volatile(""
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                 "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]),
+                 "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]),
+                 "+r"(r[29]), "+r"(r[30]), "+r"(r[31]));
+}
+
+// Shared-memory matrix descriptor for a K-major operand tile written by TMA with
+// 128-byte swizzle: rows of 128 bytes, 8-row core groups 1024 bytes apart (SBO),
+// LBO unused for swizzled K-major (set to 1), descriptor version 1, layout 2 =
+// SWIZZLE_128B. Advancing K by 16 bf16 inside the atom adds 32 bytes to the start.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  uint64_t desc = 0;
+  desc |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  desc |= (uint64_t)1 << 16;
+  desc |= (uint64_t)(1024 >> 4) << 32;
+  desc |= (uint64_t)1 << 46;
+  desc |= (uint64_t)2 << 61;
+  return desc;
+}
+// Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major, M x N.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ float gelu_erf(float u) { return 0.5f * u * (1.f + erff(u * 0.70710678118654752f)); }
+
+template <int BN>
+struct Cfg {
+  static constexpr int kABytes = BM * BK * 2;
+  static constexpr int kBBytes = BN * BK * 2;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kStages = (196 * 1024) / kStageBytes > 8 ? 8 : (196 * 1024) / kStageBytes;
+  static constexpr int kTmemCols = 2 * BN;
+  static constexpr size_t kSmem = (size_t)kStages * kStageBytes + 1024;
+};
+
+struct TileInfo {
+  int fam, g, mt, nt, m, a_row0;
+};
+
+__device__ __forceinline__ TileInfo decode_tile(int tile, const int32_t* s_start, int G, int G0,
+                                                const Family* fams, const int32_t* off) {
+  int lo = 0, hi = G;  // last group whose start <= tile
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (s_start[mid] <= tile) lo = mid; else hi = mid;
+  }
+  TileInfo ti;
+  ti.fam = lo < G0 ? 0 : 1;
+  ti.g = lo < G0 ? lo : lo - G0;
+  const Family& F = fams[ti.fam];
+  int row0;
+  if (F.m_from_off) {
+    row0 = off[ti.g];
+    ti.m = off[ti.g + 1] - row0;
+  } else {
+    row0 = 0;
+    ti.m = F.m_fixed;
+  }
+  const int m_tiles = (ti.m + BM - 1) / BM;
+  const int local = tile - s_start[lo];
+  ti.nt = local / m_tiles;
+  ti.mt = local - ti.nt * m_tiles;
+  ti.a_row0 = row0 + ti.mt * BM;
+  return ti;
+}
+
+__device__ __forceinline__ const CUtensorMap* pick_map(int i, const CUtensorMap& m0, const CUtensorMap& m1,
+                                                       const CUtensorMap& m2, const CUtensorMap& m3,
+                                                       const CUtensorMap& m4, const CUtensorMap& m5) {
+  switch (i) {
+    case 0: return &m0;
+    case 1: return &m1;
+    case 2: return &m2;
+    case 3: return &m3;
+    case 4: return &m4;
+    default: return &m5;
+  }
+}
+
+template <int BN, int EPI>
+__global__ void __launch_bounds__(kThreads, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap m0, const __grid_constant__ CUtensorMap m1,
+                        const __grid_constant__ CUtensorMap m2, const __grid_constant__ CUtensorMap m3,
+                        const __grid_constant__ CUtensorMap m4, const __grid_constant__ CUtensorMap m5,
+                        const __grid_constant__ Params P) {
+  using C = Cfg<BN>;
+  constexpr int kStages = C::kStages;
+  constexpr int kOutCols = EPI == kSwiglu ? BN / 2 : BN;
+  constexpr uint32_t kIdesc = idesc_bf16(BM, BN);
+
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t full_bar[kStages], empty_bar[kStages], tfull_bar[2], tempty_bar[2], done_bar;
+  __shared__ uint32_t s_tmem_base;
+  __shared__ int32_t s_start[kMaxGroups + 1];
+  __shared__ Family s_fam[2];
+  __shared__ int32_t s_abort;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + kStages * C::kABytes;
+  const int32_t* off = P.expert_off;
+
+  if (threadIdx.x == 0) {
+    s_fam[0] = P.fam[0];
+    s_fam[1] = P.fam[1];
+    s_abort = 0;
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull_bar[a], 1);
+      mbar_init(&tempty_bar[a], kEpiWarps);
+    }
+    mbar_init(&done_bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  // tile prefix over all groups of both families (same in every CTA)
+  const int G0 = P.fam[0].groups, G = G0 + P.fam[1].groups;
+  if (warp == 0) {
+    int carry = 0;
+    for (int base = 0; base < G; base += 32) {
+      const int g = base + lane;
+      int tiles = 0;
+      if (g < G) {
+        const Family& F = g < G0 ? P.fam[0] : P.fam[1];
+        const int gl = g < G0 ? g : g - G0;
+        const int m = F.m_from_off ? off[gl + 1] - off[gl] : F.m_fixed;
+        tiles = ((m + BM - 1) / BM) * F.n_tiles;
+      }
+      const int inc = warp_inclusive_scan(tiles);
+      if (g < G) s_start[g] = carry + inc - tiles;
+      carry += __shfl_sync(kFull, inc, 31);
+    }
+    if (lane == 0) s_start[G] = carry;
+  }
+  __syncthreads();
+  const int total = s_start[G];
+  if ((int)blockIdx.x >= total) return;  // uniform across the CTA, before any TMEM is taken
+
+  if (warp == 1) tmem_alloc(&s_tmem_base, C::kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = s_tmem_base;
+  volatile int32_t* abort_flag = &s_abort;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer ----------------
+      int stage = 0;
+      uint32_t phase = 0;
+      int32_t last_parity[kStages];
+#pragma unroll
+      for (int s = 0; s < kStages; ++s) last_parity[s] = -1;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        const TileInfo ti = decode_tile(tile, s_start, G, G0, s_fam, off);
+        const Family& F = s_fam[ti.fam];
+        const CUtensorMap* ma = pick_map(F.a_map, m0, m1, m2, m3, m4, m5);
+        const CUtensorMap* mb = pick_map(F.b_map, m0, m1, m2, m3, m4, m5);
+        const CUtensorMap* mb3 = pick_map(F.b3_map, m0, m1, m2, m3, m4, m5);
+        for (int kb = 0; kb < F.k_blocks; ++kb) {
+          if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full_bar[stage], C::kStageBytes);
+          last_parity[stage] = (int32_t)phase;
+          tma_load_2d(ma, &full_bar[stage], sA + stage * C::kABytes, kb * BK, ti.a_row0);
+          const int kseg = kb / F.kseg_blocks;
+          const int kin = kb - kseg * F.kseg_blocks;
+          if (EPI == kSwiglu) {
+            const int by = ti.g * F.b_rows_group + kseg * F.b_rows_kseg + ti.nt * (BN / 2);
+            tma_load_2d(mb, &full_bar[stage], sB + stage * C::kBBytes, kin * BK, by);
+            tma_load_2d(mb3, &full_bar[stage], sB + stage * C::kBBytes + (BN / 2) * BK * 2, kin * BK, by);
+          } else {
+            const int by = ti.g * F.b_rows_group + kseg * F.b_rows_kseg + ti.nt * BN;
+            tma_load_2d(mb, &full_bar[stage], sB + stage * C::kBBytes, kin * BK, by);
+          }
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        record_error(P.status, kErrTimeout, 201, (int32_t)blockIdx.x, 0);
+        s_abort = 1;
+        // let our own copies land before the CTA's shared memory goes away
+        for (int s = 0; s < kStages; ++s)
+          if (last_parity[s] >= 0) {
+            const unsigned long long t0 = globaltimer();
+            while (!mbar_try_wait(&full_bar[s], (uint32_t)last_parity[s]) && globaltimer() - t0 < kTimeoutNs) {
+            }
+          }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer ----------------
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        const TileInfo ti = decode_tile(tile, s_start, G, G0, s_fam, off);
+        const int kblocks = s_fam[ti.fam].k_blocks;
+        if (!mbar_wait(&tempty_bar[acc], acc_phase ^ 1u, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait(&full_bar[stage], phase, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(sA + stage * C::kABytes);
+          const uint32_t b_addr = smem_u32(sB + stage * C::kBBytes);
+#pragma unroll
+          for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+            umma_bf16(d_tmem, sw128_desc(a_addr + kk * UMMA_K * 2), sw128_desc(b_addr + kk * UMMA_K * 2), kIdesc,
+                      (kb | kk) != 0 ? 1u : 0u);
+          }
+          umma_commit(&empty_bar[stage]);
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit(&tfull_bar[acc]);
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      if (!ok) {
+        record_error(P.status, kErrTimeout, 202, (int32_t)blockIdx.x, 0);
+        s_abort = 1;
+      }
+      // every MMA this thread issued has finished before TMEM is released
+      umma_commit(&done_bar);
+      const unsigned long long t0 = globaltimer();
+      while (!mbar_try_wait(&done_bar, 0u) && globaltimer() - t0 < kTimeoutNs) {
+      }
+    }
+  } else {
+    // ---------------- epilogue warps ----------------
+    const int ew = warp - 2;
+    const int q = warp & 3;       // TMEM lane quadrant this warp may read
+    const int half = ew >> 2;     // which interleaved half of the column chunks
+    const int r = q * 32 + lane;  // row inside the tile
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+      const TileInfo ti = decode_tile(tile, s_start, G, G0, s_fam, off);
+      const Family& F = s_fam[ti.fam];
+      const bool got = __all_sync(kFull, mbar_wait(&tfull_bar[acc], acc_phase, abort_flag) ? 1 : 0) != 0;
+      if (!got) {
+        if (lane == 0) {
+          record_error(P.status, kErrTimeout, 203, (int32_t)blockIdx.x, tile);
+          s_abort = 1;
+        }
+        break;
+      }
+      tc_fence_after();
+      const bool valid = ti.mt * BM + r < ti.m;
+      const int64_t grow = (int64_t)ti.a_row0 + r;
+      const uint32_t tbase = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(q * 32) << 16);
+      __nv_bfloat16* out = static_cast<__nv_bfloat16*>(F.out) + grow * F.ld_out + (int64_t)ti.g * F.out_col_group +
+                           (int64_t)ti.nt * kOutCols;
+      const int64_t bcol0 = (int64_t)ti.nt * kOutCols;
+      const __nv_bfloat16* bias = F.bias ? F.bias + (int64_t)ti.g * F.bias_group : nullptr;
+      float gate = 1.f;
+      if (EPI == kLinear && F.row_gate && valid) gate = F.row_gate[grow];
+      for (int c = half * 32; c < kOutCols; c += 64) {
+        uint32_t v[32];
+        tmem_ld32(tbase + (uint32_t)c, v);
+        float o[32];
+        if (EPI == kSwiglu) {
+          uint32_t u[32];
+          tmem_ld32(tbase + (uint32_t)(BN / 2 + c), u);
+          tmem_ld_wait(u);
+          reg_fence(v);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float a = __uint_as_float(v[i]);
+            o[i] = a / (1.f + __expf(-a)) * __uint_as_float(u[i]);
+          }
+        } else {
+          tmem_ld_wait(v);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            float a = __uint_as_float(v[i]);
+            if (bias) {
+              for (int s = 0; s < F.bias_nsum; ++s)
+                a += __bfloat162float(bias[s * F.bias_sum_stride + bcol0 + c + i]);
+            }
+            o[i] = EPI == kGelu ? gelu_erf(a) : a * gate;
+          }
+        }
+        if (valid) {
+          uint4* dst = reinterpret_cast<uint4*>(out + c);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) dst[i] = Vec16<__nv_bfloat16>::pack(o + 8 * i);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty_bar[acc]);
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::kTmemCols);
+  }
+}
+
+// ---- host side ---------------------------------------------------------------
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = []() -> EncodeTiledFn {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<EncodeTiledFn>(p);
+  }();
+  return fn;
+}
+
+// 2-D bf16 matrix [rows, cols] row-major, box = 64 columns x box_rows rows, 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc || !ptr || rows < 1 || cols < 64) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int num_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 148;
+  return n;
+}
+
+template <int BN, int EPI>
+cudaError_t launch_t(const CUtensorMap (&maps)[6], const Params& P, int64_t max_tiles, cudaStream_t st) {
+  using C = Cfg<BN>;
+  auto kern = grouped_gemm_kernel<BN, EPI>;
+  static cudaError_t attr = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
+  if (attr != cudaSuccess) return attr;
+  const int64_t grid = max_tiles < num_sms() ? max_tiles : num_sms();
+  if (grid <= 0) return cudaSuccess;
+  kern<<<(unsigned)grid, kThreads, C::kSmem, st>>>(maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], P);
+  return cudaGetLastError();
+}
+
+template <int EPI>
+cudaError_t launch_bn(int bn, const CUtensorMap (&maps)[6], const Params& P, int64_t max_tiles, cudaStream_t st) {
+  switch (bn) {
+    case 256: return launch_t<256, EPI>(maps, P, max_tiles, st);
+    case 128: return launch_t<128, EPI>(maps, P, max_tiles, st);
+    default: return launch_t<64, EPI>(maps, P, max_tiles, st);
+  }
+}
+
+// Largest tile width BN in {256, 128, 64} whose output width (BN, or BN/2 for
+// SwiGLU) divides every listed column count.
+int pick_bn(bool swiglu, int64_t c0, int64_t c1) {
+  for (int bn : {256, 128, 64}) {
+    const int oc = swiglu ? bn / 2 : bn;
+    if (c0 % oc == 0 && (c1 <= 0 || c1 % oc == 0)) return bn;
+  }
+  return 0;
+}
+
+}  // namespace tc
+
+bool tc_gemm_available() { return tc::encode_fn() != nullptr; }
+
+// part: bit 0 = up-projections (routed + shared), bit 1 = down-projections.
+cudaError_t launch_ffn_bf16(const Plan& p, const void* xp, const int32_t* expert_off, const float* row_gate,
+                            const void* x, const moe_weights* w, void* h, void* hs, void* yp, void* ys,
+                            int32_t* status, cudaStream_t st, int part) {
+  using namespace tc;
+  const int64_t R = p.max_rows > 0 ? p.max_rows : 1;
+  if (part & 1) {
+    const int bn = pick_bn(p.swiglu, p.F, p.S > 0 ? p.Fs : 0);
+    if (!bn) return cudaErrorInvalidValue;
+    const int oc = p.swiglu ? bn / 2 : bn;
+    const int brows = p.swiglu ? bn / 2 : bn;
+    CUtensorMap maps[6];
+    if (!make_map(&maps[0], xp, R, p.d, BM)) return cudaErrorInvalidValue;
+    for (int i = 1; i < 6; ++i) maps[i] = maps[0];  // unused slots hold a valid map
+    bool ok = make_map(&maps[2], w->w1, p.E * p.F, p.d, brows);
+    if (p.swiglu) ok = ok && make_map(&maps[3], w->w3, p.E * p.F, p.d, brows);
+    if (p.S > 0) {
+      ok = ok && make_map(&maps[1], x, p.N, p.d, BM) && make_map(&maps[4], w->ws1, p.S * p.Fs, p.d, brows);
+      if (p.swiglu) ok = ok && make_map(&maps[5], w->ws3, p.S * p.Fs, p.d, brows);
+    }
+    if (!ok) return cudaErrorInvalidValue;
+    Params P{};
+    Family& f0 = P.fam[0];
+    f0.groups = (int32_t)p.E;
+    f0.m_from_off = 1;
+    f0.n_tiles = (int32_t)(p.F / oc);
+    f0.k_blocks = f0.kseg_blocks = (int32_t)(p.d / BK);
+    f0.b_rows_group = (int32_t)p.F;
+    f0.a_map = 0;
+    f0.b_map = 2;
+    f0.b3_map = 3;
+    f0.out = h;
+    f0.ld_out = p.F;
+    f0.bias = static_cast<const __nv_bfloat16*>(p.bias ? w->b1 : nullptr);
+    f0.bias_group = p.F;
+    f0.bias_nsum = p.bias ? 1 : 0;
+    if (p.S > 0) {
+      Family& f1 = P.fam[1];
+      f1.groups = (int32_t)p.S;
+      f1.m_fixed = (int32_t)p.N;
+      f1.n_tiles = (int32_t)(p.Fs / oc);
+      f1.k_blocks = f1.kseg_blocks = (int32_t)(p.d / BK);
+      f1.b_rows_group = (int32_t)p.Fs;
+      f1.a_map = 1;
+      f1.b_map = 4;
+      f1.b3_map = 5;
+      f1.out = hs;
+      f1.ld_out = p.S * p.Fs;
+      f1.out_col_group = p.Fs;
+      f1.bias = static_cast<const __nv_bfloat16*>(p.bias ? w->bs1 : nullptr);
+      f1.bias_group = p.Fs;
+      f1.bias_nsum = p.bias ? 1 : 0;
+    }
+    P.expert_off = expert_off;
+    P.status = status;
+    const int64_t max_tiles = (R / BM + p.E) * f0.n_tiles + (p.S > 0 ? p.S * ceil_div(p.N, BM) * P.fam[1].n_tiles : 0);
+    cudaError_t err = p.swiglu ? launch_bn<kSwiglu>(bn, maps, P, max_tiles, st)
+                               : launch_bn<kGelu>(bn, maps, P, max_tiles, st);
+    if (err != cudaSuccess) return err;
+  }
+  if (part & 2) {
+    const int bn = pick_bn(false, p.d, 0);
+    if (!bn) return cudaErrorInvalidValue;
+    CUtensorMap maps[6];
+    if (!make_map(&maps[0], h, R, p.F, BM)) return cudaErrorInvalidValue;
+    for (int i = 1; i < 6; ++i) maps[i] = maps[0];
+    bool ok = make_map(&maps[2], w->w2, p.E * p.d, p.F, bn);
+    if (p.S > 0) ok = ok && make_map(&maps[1], hs, p.N, p.S * p.Fs, BM) && make_map(&maps[3], w->ws2, p.S * p.d, p.Fs, bn);
+    if (!ok) return cudaErrorInvalidValue;
+    Params P{};
+    Family& f0 = P.fam[0];
+    f0.groups = (int32_t)p.E;
+    f0.m_from_off = 1;
+    f0.n_tiles = (int32_t)(p.d / bn);
+    f0.k_blocks = f0.kseg_blocks = (int32_t)(p.F / BK);
+    f0.b_rows_group = (int32_t)p.d;
+    f0.a_map = 0;
+    f0.b_map = 2;
+    f0.b3_map = 2;
+    f0.out = yp;
+    f0.ld_out = p.d;
+    f0.bias = static_cast<const __nv_bfloat16*>(p.bias ? w->b2 : nullptr);
+    f0.bias_group = p.d;
+    f0.bias_nsum = p.bias ? 1 : 0;
+    f0.row_gate = row_gate;
+    if (p.S > 0) {
+      Family& f1 = P.fam[1];
+      f1.groups = 1;
+      f1.m_fixed = (int32_t)p.N;
+      f1.n_tiles = (int32_t)(p.d / bn);
+      f1.k_blocks = (int32_t)(p.S * p.Fs / BK);
+      f1.kseg_blocks = (int32_t)(p.Fs / BK);
+      f1.b_rows_kseg = (int32_t)p.d;
+      f1.a_map = 1;
+      f1.b_map = 3;
+      f1.b3_map = 3;
+      f1.out = ys;
+      f1.ld_out = p.d;
+      f1.bias = static_cast<const __nv_bfloat16*>(p.bias ? w->bs2 : nullptr);
+      f1.bias_sum_stride = p.d;
+      f1.bias_nsum = p.bias ? (int32_t)p.S : 0;
+    }
+    P.expert_off = expert_off;
+    P.status = status;
+    const int64_t max_tiles = (R / BM + p.E) * f0.n_tiles + (p.S > 0 ? ceil_div(p.N, BM) * P.fam[1].n_tiles : 0);
+    cudaError_t err = launch_bn<kLinear>(bn, maps, P, max_tiles, st);
+    if (err != cudaSuccess) return err;
+  }
+  return cudaSuccess;
+}
+
+}  // namespace moe

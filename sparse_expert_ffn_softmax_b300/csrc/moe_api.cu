@@ -1,0 +1,359 @@
+// C ABI of the library: argument validation, workspace layout and the stage
+// entry points declared in include/moe.h. Every step of the layer runs in the
+// kernels of router.cu, permute.cu, ffn_simt.cu and gemm_tc.cu; this file only
+// checks arguments, carves the caller's workspace and enqueues launches.
+#include <cmath>
+#include <cstring>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+constexpr size_t kAlign = 256;
+inline size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool ok_ptr(const void* p) { return p != nullptr && aligned16(p); }
+inline bool ok_opt(const void* p) { return p == nullptr || aligned16(p); }
+
+moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+}  // namespace
+
+moe_status make_plan(const moe_config* c, Plan* p) {
+  if (!c || !p) return MOE_ERR_INVALID_ARG;
+  std::memset(p, 0, sizeof(*p));
+  p->cfg = *c;
+  p->N = c->n_tokens;
+  p->d = c->d_model;
+  p->F = c->d_ff;
+  p->E = c->n_experts;
+  p->S = c->n_shared;
+  p->Fs = c->d_ff_shared;
+  p->k = c->top_k;
+  if (p->N < 0 || p->d < 1 || p->F < 1 || p->E < 1 || p->k < 1 || p->S < 0) return MOE_ERR_INVALID_ARG;
+  if (p->S > 0 && p->Fs < 1) return MOE_ERR_INVALID_ARG;
+  if (c->gating < 0 || c->gating > 3 || c->act < 0 || c->act > 1 || c->dtype < 0 || c->dtype > 1)
+    return MOE_ERR_INVALID_ARG;
+  if (!std::isfinite(c->capacity_factor) || !std::isfinite(c->aux_alpha)) return MOE_ERR_INVALID_ARG;
+  if (p->k > p->E || p->k > 32 || p->E > 512 || p->S > 64) return MOE_ERR_UNSUPPORTED;
+  p->bf16 = c->dtype == MOE_DT_BF16;
+  p->swiglu = c->act == MOE_ACT_SWIGLU;
+  p->ec = c->gating == MOE_GATE_EXPERT_CHOICE;
+  p->bias = c->has_bias != 0;
+  if (p->swiglu && p->bias) return MOE_ERR_UNSUPPORTED;
+  if (p->bf16) {
+    if (p->d % 64 || p->F % 64 || (p->S > 0 && p->Fs % 64)) return MOE_ERR_UNSUPPORTED;
+  } else {
+    if (p->d % 4) return MOE_ERR_UNSUPPORTED;
+  }
+  if (p->N * p->k >= (int64_t)1 << 31) return MOE_ERR_UNSUPPORTED;
+  if (p->ec && p->N > ((int64_t)1 << 20)) return MOE_ERR_UNSUPPORTED;
+  // capacity: token choice C = ceil(N*k*cf/E) (cf <= 0: no limit); expert choice
+  // C = min(N, ceil(N*k*cf/E)) with cf <= 0 read as 1.
+  const double cf = (double)c->capacity_factor;
+  if (p->ec) {
+    const double cfe = cf > 0 ? cf : 1.0;
+    int64_t cap = (int64_t)std::ceil((double)p->N * (double)p->k * cfe / (double)p->E);
+    p->cap = cap < p->N ? cap : p->N;
+  } else if (cf <= 0) {
+    p->cap = p->N;
+  } else {
+    int64_t cap = (int64_t)std::ceil((double)p->N * (double)p->k * cf / (double)p->E);
+    p->cap = cap < p->N ? cap : p->N;
+  }
+  if (p->cap < 0) p->cap = 0;
+  p->max_rows = p->ec ? p->E * p->cap : p->N * p->k;
+  if (p->max_rows >= (int64_t)1 << 31) return MOE_ERR_UNSUPPORTED;
+  p->tiles = ceil_div(p->N, kTileTokens);
+  p->words = ceil_div(p->E, 32);
+  int64_t tpw = ceil_div(p->N, (int64_t)kRouterWarps * 2 * 148);
+  p->router_tpw = (int)(tpw < 1 ? 1 : (tpw > 64 ? 64 : tpw));
+  p->router_blocks = ceil_div(p->N, (int64_t)kRouterWarps * p->router_tpw);
+  if (p->router_blocks < 1) p->router_blocks = 1;
+
+  const size_t b = p->bf16 ? 2 : 4;
+  const int64_t nsel = p->ec ? p->E * p->cap : p->N * p->k;
+  moe_workspace_layout& L = p->L;
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o += align_up(bytes > 0 ? bytes : 1);
+    return at;
+  };
+  L.status = take(16);
+  L.logits = take((size_t)(p->N * p->E) * 4);
+  L.probs = take((size_t)(p->N * p->E) * 4);
+  L.idx = take((size_t)nsel * 4);
+  L.gate = take((size_t)nsel * 4);
+  L.tok_rows = take((size_t)nsel * 4);
+  L.tok_off = take((size_t)(p->N + 1) * 4);
+  L.expert_off = take((size_t)(p->E + 1) * 4);
+  L.row_token = take((size_t)p->max_rows * 4);
+  L.row_gate = take((size_t)p->max_rows * 4);
+  L.xp = take((size_t)p->max_rows * (size_t)p->d * b);
+  L.h = take((size_t)p->max_rows * (size_t)p->F * b);
+  L.hs = take((size_t)p->N * (size_t)(p->S * p->Fs) * b);
+  L.yp = take((size_t)p->max_rows * (size_t)p->d * b);
+  L.ys = take(p->S > 0 ? (size_t)p->N * (size_t)p->d * b : 0);
+  L.stats = take(moe_stats_bytes(p->E));
+  L.scratch = o;
+  p->part_p = take((size_t)(p->E * p->router_blocks) * 4);
+  p->part_cnt = take((size_t)(p->E * p->router_blocks) * 4);
+  p->part_lse = take((size_t)(2 * p->router_blocks) * 4);
+  p->tile_counts = take((size_t)(p->E * p->tiles) * 4);
+  p->tile_base = take((size_t)(p->E * (p->tiles + 1)) * 4);
+  p->ec_bits = take((size_t)(p->N * p->words) * 4);
+  L.total_bytes = o;
+  L.max_rows = p->max_rows;
+  L.capacity = p->cap;
+  return MOE_OK;
+}
+
+namespace {
+
+moe_status check_ws(const Plan& p, const void* ws, size_t ws_bytes) {
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1))) return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < p.L.total_bytes) return MOE_ERR_WORKSPACE;
+  return MOE_OK;
+}
+
+moe_status check_weights(const Plan& p, const moe_weights* w, bool router, bool experts) {
+  if (!w) return MOE_ERR_INVALID_ARG;
+  if (router) {
+    if (!ok_ptr(w->w_router) || !ok_opt(w->logit_bias)) return MOE_ERR_INVALID_ARG;
+  }
+  if (experts) {
+    if (!ok_ptr(w->w1) || !ok_ptr(w->w2)) return MOE_ERR_INVALID_ARG;
+    if (p.swiglu && !ok_ptr(w->w3)) return MOE_ERR_INVALID_ARG;
+    if (p.bias && (!ok_ptr(w->b1) || !ok_ptr(w->b2))) return MOE_ERR_INVALID_ARG;
+    if (p.S > 0) {
+      if (!ok_ptr(w->ws1) || !ok_ptr(w->ws2)) return MOE_ERR_INVALID_ARG;
+      if (p.swiglu && !ok_ptr(w->ws3)) return MOE_ERR_INVALID_ARG;
+      if (p.bias && (!ok_ptr(w->bs1) || !ok_ptr(w->bs2))) return MOE_ERR_INVALID_ARG;
+    }
+  }
+  return MOE_OK;
+}
+
+void* stats_or_ws(const Plan& p, void* stats, void* ws) { return stats ? stats : ws_at<uint8_t>(ws, p.L.stats); }
+
+moe_status do_route(const Plan& p, const void* x, const moe_weights* w, int32_t* idx, float* gate, float* logits,
+                    float* probs, void* stats, void* ws, cudaStream_t st) {
+  float* pr = probs;
+  if (p.ec && !pr) pr = ws_at<float>(ws, p.L.probs);
+  cudaError_t e = launch_router(p, x, w, idx, gate, logits, pr, stats_or_ws(p, stats, ws), ws, st);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  if (p.ec) {
+    e = launch_ec_select(p, pr, idx, gate, ws, st);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
+}
+
+moe_status do_ffn(const Plan& p, const void* xp, const int32_t* expert_off, const float* row_gate, const void* x,
+                  const moe_weights* w, void* yp, void* ys, void* ws, cudaStream_t st, int part) {
+  void* h = ws_at<uint8_t>(ws, p.L.h);
+  void* hs = ws_at<uint8_t>(ws, p.L.hs);
+  cudaError_t e = p.bf16 ? launch_ffn_bf16(p, xp, expert_off, row_gate, x, w, h, hs, yp, ys, status_ptr(p, ws), st,
+                                           part)
+                         : launch_ffn_f32(p, xp, expert_off, row_gate, x, w, h, hs, yp, ys, status_ptr(p, ws), st,
+                                          part);
+  return cuda_status(e);
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+int32_t moe_abi_version(void) { return MOE_ABI_VERSION; }
+
+const char* moe_status_string(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported layer shape";
+    case MOE_ERR_WORKSPACE: return "workspace too small";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_DEVICE_CHECK: return "device-side index check failed";
+    case MOE_ERR_TIMEOUT: return "device-side pipeline wait timed out";
+  }
+  return "unknown status";
+}
+
+size_t moe_stats_bytes(int64_t n_experts) {
+  if (n_experts < 0) n_experts = 0;
+  return sizeof(moe_stats_header) + (size_t)n_experts * 16;
+}
+
+moe_status moe_workspace_size(const moe_config* cfg, size_t* bytes) {
+  if (!bytes) return MOE_ERR_INVALID_ARG;
+  Plan p;
+  moe_status s = make_plan(cfg, &p);
+  if (s != MOE_OK) return s;
+  *bytes = p.L.total_bytes;
+  return MOE_OK;
+}
+
+moe_status moe_workspace_layout_of(const moe_config* cfg, moe_workspace_layout* layout) {
+  if (!layout) return MOE_ERR_INVALID_ARG;
+  Plan p;
+  moe_status s = make_plan(cfg, &p);
+  if (s != MOE_OK) return s;
+  *layout = p.L;
+  return MOE_OK;
+}
+
+moe_status moe_workspace_init(const moe_config* cfg, void* ws, size_t ws_bytes, void* stream) {
+  Plan p;
+  moe_status s = make_plan(cfg, &p);
+  if (s != MOE_OK) return s;
+  if ((s = check_ws(p, ws, ws_bytes)) != MOE_OK) return s;
+  cudaGetLastError();
+  return cuda_status(cudaMemsetAsync(ws_at<uint8_t>(ws, p.L.status), 0, 16, (cudaStream_t)stream));
+}
+
+moe_status moe_route(const moe_config* cfg, const void* x, const moe_weights* w, int32_t* idx, float* gate,
+                     float* logits, float* probs, void* stats, void* ws, size_t ws_bytes, void* stream) {
+  Plan p;
+  moe_status s = make_plan(cfg, &p);
+  if (s != MOE_OK) return s;
+  if ((s = check_ws(p, ws, ws_bytes)) != MOE_OK) return s;
+  if ((s = check_weights(p, w, true, false)) != MOE_OK) return s;
+  if (!ok_opt(logits) || !ok_opt(probs) || !ok_opt(stats)) return MOE_ERR_INVALID_ARG;
+  if (p.N == 0) return MOE_OK;
+  if (!ok_ptr(x) || !ok_ptr(idx) || !ok_ptr(gate)) return MOE_ERR_INVALID_ARG;
+  cudaGetLastError();
+  return do_route(p, x, w, idx, gate, logits, probs, stats, ws, (cudaStream_t)stream);
+}
+
+moe_status moe_permute(const moe_config* cfg, const void* x, const int32_t* idx, const float* gate, void* xp,
+                       int32_t* tok_rows, int32_t* tok_off, int32_t* expert_off, int32_t* row_token,
+                       float* row_gate, void* stats, void* ws, size_t ws_bytes, void* stream) {
+  Plan p;
+  moe_status s = make_plan(cfg, &p);
+  if (s != MOE_OK) return s;
+  if ((s = check_ws(p, ws, ws_bytes)) != MOE_OK) return s;
+  if (!ok_opt(stats) || !ok_ptr(expert_off)) return MOE_ERR_INVALID_ARG;
+  if (p.ec && !ok_ptr(tok_off)) return MOE_ERR_INVALID_ARG;
+  if (p.N == 0) {
+    cudaGetLastError();
+    return cuda_status(cudaMemsetAsync(expert_off, 0, (size_t)(p.E + 1) * 4, (cudaStream_t)stream));
+  }
+  if (!ok_ptr(x) || !ok_ptr(idx) || !ok_ptr(gate) || !ok_ptr(xp) || !ok_ptr(tok_rows) || !ok_ptr(row_token) ||
+      !ok_ptr(row_gate))
+    return MOE_ERR_INVALID_ARG;
+  cudaGetLastError();
+  return cuda_status(launch_permute(p, x, idx, gate, xp, tok_rows, tok_off, expert_off, row_token, row_gate, stats,
+                                    ws, (cudaStream_t)stream));
+}
+
+moe_status moe_expert_ffn(const moe_config* cfg, const void* xp, const int32_t* expert_off, const float* row_gate,
+                          const void* x, const moe_weights* w, void* yp, void* ys, void* ws, size_t ws_bytes,
+                          void* stream) {
+  Plan p;
+  moe_status s = make_plan(cfg, &p);
+  if (s != MOE_OK) return s;
+  if ((s = check_ws(p, ws, ws_bytes)) != MOE_OK) return s;
+  if ((s = check_weights(p, w, false, true)) != MOE_OK) return s;
+  if (p.N == 0) return MOE_OK;
+  if (!ok_ptr(xp) || !ok_ptr(expert_off) || !ok_ptr(row_gate) || !ok_ptr(yp)) return MOE_ERR_INVALID_ARG;
+  if (p.S > 0 && (!ok_ptr(x) || !ok_ptr(ys))) return MOE_ERR_INVALID_ARG;
+  if (p.bf16 && !tc_gemm_available()) return MOE_ERR_CUDA;
+  cudaGetLastError();
+  return do_ffn(p, xp, expert_off, row_gate, x, w, yp, ys, ws, (cudaStream_t)stream, 3);
+}
+
+moe_status moe_combine(const moe_config* cfg, const void* yp, const int32_t* tok_rows, const int32_t* tok_off,
+                       const void* ys, void* out, void* stream) {
+  Plan p;
+  moe_status s = make_plan(cfg, &p);
+  if (s != MOE_OK) return s;
+  if (p.N == 0) return MOE_OK;
+  if (!ok_ptr(yp) || !ok_ptr(tok_rows) || !ok_ptr(out) || !ok_opt(ys)) return MOE_ERR_INVALID_ARG;
+  if (p.ec && !ok_ptr(tok_off)) return MOE_ERR_INVALID_ARG;
+  cudaGetLastError();
+  return cuda_status(launch_combine(p, yp, tok_rows, tok_off, ys, out, (cudaStream_t)stream));
+}
+
+moe_status moe_forward_traced(const moe_config* cfg, const void* x, const moe_weights* w, void* out, void* stats,
+                              void* ws, size_t ws_bytes, void* stream, void* const* events, int32_t n_events) {
+  Plan p;
+  moe_status s = make_plan(cfg, &p);
+  if (s != MOE_OK) return s;
+  if ((s = check_ws(p, ws, ws_bytes)) != MOE_OK) return s;
+  if ((s = check_weights(p, w, true, true)) != MOE_OK) return s;
+  if (!ok_opt(stats) || (n_events > 0 && !events)) return MOE_ERR_INVALID_ARG;
+  if (p.N == 0) return MOE_OK;
+  if (!ok_ptr(x) || !ok_ptr(out)) return MOE_ERR_INVALID_ARG;
+  if (p.bf16 && !tc_gemm_available()) return MOE_ERR_CUDA;
+  cudaStream_t st = (cudaStream_t)stream;
+  cudaGetLastError();
+  int ev = 0;
+  auto mark = [&]() -> bool {
+    if (ev < n_events && ev < 6) {
+      if (cudaEventRecord((cudaEvent_t)events[ev], st) != cudaSuccess) return false;
+    }
+    ++ev;
+    return true;
+  };
+  const moe_workspace_layout& L = p.L;
+  int32_t* idx = ws_at<int32_t>(ws, L.idx);
+  float* gate = ws_at<float>(ws, L.gate);
+  int32_t* tok_rows = ws_at<int32_t>(ws, L.tok_rows);
+  int32_t* tok_off = ws_at<int32_t>(ws, L.tok_off);
+  int32_t* expert_off = ws_at<int32_t>(ws, L.expert_off);
+  int32_t* row_token = ws_at<int32_t>(ws, L.row_token);
+  float* row_gate = ws_at<float>(ws, L.row_gate);
+  void* xp = ws_at<uint8_t>(ws, L.xp);
+  void* yp = ws_at<uint8_t>(ws, L.yp);
+  void* ys = p.S > 0 ? ws_at<uint8_t>(ws, L.ys) : nullptr;
+  void* st_buf = stats_or_ws(p, stats, ws);
+  if (!mark()) return MOE_ERR_CUDA;
+  if ((s = do_route(p, x, w, idx, gate, ws_at<float>(ws, L.logits), p.ec ? ws_at<float>(ws, L.probs) : nullptr,
+                    st_buf, ws, st)) != MOE_OK)
+    return s;
+  if (!mark()) return MOE_ERR_CUDA;
+  if (launch_permute(p, x, idx, gate, xp, tok_rows, tok_off, expert_off, row_token, row_gate, st_buf, ws, st) !=
+      cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (!mark()) return MOE_ERR_CUDA;
+  if ((s = do_ffn(p, xp, expert_off, row_gate, x, w, yp, ys, ws, st, 1)) != MOE_OK) return s;
+  if (!mark()) return MOE_ERR_CUDA;
+  if ((s = do_ffn(p, xp, expert_off, row_gate, x, w, yp, ys, ws, st, 2)) != MOE_OK) return s;
+  if (!mark()) return MOE_ERR_CUDA;
+  if (launch_combine(p, yp, tok_rows, tok_off, ys, out, st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (!mark()) return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+moe_status moe_forward(const moe_config* cfg, const void* x, const moe_weights* w, void* out, void* stats, void* ws,
+                       size_t ws_bytes, void* stream) {
+  return moe_forward_traced(cfg, x, w, out, stats, ws, ws_bytes, stream, nullptr, 0);
+}
+
+moe_status moe_get_device_status(const moe_config* cfg, void* ws, size_t ws_bytes, void* stream,
+                                 int32_t* device_error) {
+  Plan p;
+  moe_status s = make_plan(cfg, &p);
+  if (s != MOE_OK) return s;
+  if ((s = check_ws(p, ws, ws_bytes)) != MOE_OK) return s;
+  cudaStream_t st = (cudaStream_t)stream;
+  int32_t word[4] = {0, 0, 0, 0};
+  cudaGetLastError();
+  if (cudaMemcpyAsync(word, ws_at<uint8_t>(ws, p.L.status), sizeof word, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemsetAsync(ws_at<uint8_t>(ws, p.L.status), 0, sizeof word, st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (device_error) *device_error = word[0];
+  if (word[0] & kErrTimeout) return MOE_ERR_TIMEOUT;
+  if (word[0] & kErrIndex) return MOE_ERR_DEVICE_CHECK;
+  return MOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,458 @@
+// Capacity, in-token-order dropping, permutation into expert-contiguous rows,
+// expert-choice selection, and the combine back into token order.
+//
+// Pages: "Mixture of Experts" (aigrafen.se) "Expert capacity" (C = tokens /
+// experts x capacity factor; tokens above the limit are dropped) and its MoE
+// code (each expert's tokens listed in index order and cut to the first C);
+// "MoE Architecture" (vanos001.github.io) CapacityManagedMoE and
+// ExpertChoiceRouter; "Mixture of Experts (MoE)" (wiki.ai-engineering.at)
+// "Gather/scatter outputs from experts".
+//
+// Token choice runs four kernels, none of which waits on another block:
+//  1. count:   one warp per tile of 32 consecutive tokens counts the tile's
+//              assignments per expert            -> tile_counts[E][T]
+//  2. scan:    one warp per expert, exclusive prefix over tiles
+//                                                -> tile_base[E][T+1] (last = total)
+//  3. offsets: one block; kept_e = min(count_e, C), expert_off = exclusive
+//              prefix of kept, dropped / rows statistics
+//  4. scatter: one warp per tile; the in-tile rank of (t, j) among the tile's
+//              tokens that chose the same expert comes from a per-warp bitmask
+//              of lanes per expert (atomicOr, then popc of the lower lanes), so
+//              rank = tile_base + in-tile rank is the token-order rank exactly.
+//              Kept pairs get row = expert_off[e] + rank; the warp then copies
+//              each of its tokens' rows of x into xp with 16-byte vectors (x is
+//              read once, written once per kept choice).
+// Expert choice: one block per expert radix-selects the C-th largest
+// probability (4 passes of 8 bits over the column), takes every larger one and
+// the first ties in token order, and lists them in ascending token order; a
+// bitmap of (token, expert) then gives each token its rows in ascending expert
+// order (a CSR: tok_off / tok_rows) for the copy and the combine.
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int kWarps = 8;
+
+__global__ void __launch_bounds__(kWarps * 32) count_kernel(const int32_t* __restrict__ idx, int64_t N, int64_t k,
+                                                            int64_t E, int64_t T, int32_t* __restrict__ tile_counts,
+                                                            int32_t* status) {
+  extern __shared__ int32_t s_hist[];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t tile = (int64_t)blockIdx.x * kWarps + warp;
+  if (tile >= T) return;
+  int32_t* h = s_hist + warp * E;
+  for (int64_t e = lane; e < E; e += 32) h[e] = 0;
+  __syncwarp();
+  const int64_t t = tile * kTileTokens + lane;
+  if (t < N) {
+    for (int64_t j = 0; j < k; ++j) {
+      const int32_t e = idx[t * k + j];
+      if (e < 0 || e >= E) {
+        record_error(status, kErrIndex, 101, (int32_t)t, e);
+        continue;
+      }
+      atomicAdd(&h[e], 1);
+    }
+  }
+  __syncwarp();
+  for (int64_t e = lane; e < E; e += 32) tile_counts[e * T + tile] = h[e];
+}
+
+__global__ void __launch_bounds__(kWarps * 32) scan_kernel(const int32_t* __restrict__ tile_counts, int64_t E,
+                                                           int64_t T, int32_t* __restrict__ tile_base) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t e = (int64_t)blockIdx.x * kWarps + warp;
+  if (e >= E) return;
+  const int32_t* src = tile_counts + e * T;
+  int32_t* dst = tile_base + e * (T + 1);
+  int carry = 0;
+  for (int64_t b = 0; b < T; b += 32) {
+    const int v = (b + lane < T) ? src[b + lane] : 0;
+    const int inc = warp_inclusive_scan(v);
+    if (b + lane < T) dst[b + lane] = carry + inc - v;
+    carry += __shfl_sync(kFull, inc, 31);
+  }
+  if (lane == 0) dst[T] = carry;
+}
+
+// Block-wide exclusive scan for blockDim.x <= 1024 (multiple of 32); returns the
+// exclusive prefix of v and writes the block total to *total.
+__device__ int block_exclusive_scan(int v, int* s_warp, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const int inc = warp_inclusive_scan(v);
+  if (lane == 31) s_warp[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    const int w = lane < nw ? s_warp[lane] : 0;
+    const int winc = warp_inclusive_scan(w);
+    if (lane < nw) s_warp[lane] = winc - w;
+    if (lane == 31) s_warp[32] = winc;
+  }
+  __syncthreads();
+  const int r = s_warp[warp] + inc - v;
+  *total = s_warp[32];
+  __syncthreads();
+  return r;
+}
+
+__global__ void __launch_bounds__(512) offsets_kernel(const int32_t* __restrict__ tile_base, int64_t E, int64_t T,
+                                                      int64_t cap, int64_t N, int64_t k,
+                                                      int32_t* __restrict__ expert_off, void* stats) {
+  __shared__ int s_warp[33];
+  const int e = threadIdx.x;
+  const int cnt = e < E ? tile_base[(int64_t)e * (T + 1) + T] : 0;
+  const int kept = (int)(cnt < cap ? cnt : cap);
+  int rows = 0, dropped_total = 0;
+  const int off = block_exclusive_scan(kept, s_warp, &rows);
+  block_exclusive_scan(cnt - kept, s_warp, &dropped_total);
+  if (e < E) expert_off[e] = off;
+  if (e == 0) expert_off[E] = rows;
+  if (stats) {
+    moe_stats_header* hdr = static_cast<moe_stats_header*>(stats);
+    int32_t* kept_out = reinterpret_cast<int32_t*>(reinterpret_cast<float*>(hdr + 1) + 2 * E) + E;
+    if (e < E) kept_out[e] = kept;
+    if (e == 0) {
+      hdr->dropped = dropped_total;
+      hdr->dropped_share = (float)((double)dropped_total / (double)(N * k));
+      hdr->capacity = (int32_t)cap;
+      hdr->rows = rows;
+      hdr->n_experts = (int32_t)E;
+    }
+  }
+}
+
+template <typename DT>
+__global__ void __launch_bounds__(kWarps * 32) scatter_kernel(
+    const DT* __restrict__ x, const int32_t* __restrict__ idx, const float* __restrict__ gate,
+    const int32_t* __restrict__ tile_base, const int32_t* __restrict__ expert_off, int64_t N, int64_t d, int64_t k,
+    int64_t E, int64_t T, int64_t cap, DT* __restrict__ xp, int32_t* __restrict__ tok_rows,
+    int32_t* __restrict__ row_token, float* __restrict__ row_gate, int32_t* status) {
+  extern __shared__ uint32_t s_mask[];
+  using VT = Vec16<DT>;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t tile = (int64_t)blockIdx.x * kWarps + warp;
+  if (tile >= T) return;
+  uint32_t* msk = s_mask + warp * E;
+  const int64_t t = tile * kTileTokens + lane;
+  const bool valid = t < N;
+  const uint32_t lt = (1u << lane) - 1u;
+  if (valid)
+    for (int64_t j = 0; j < k; ++j) {
+      const int32_t e = idx[t * k + j];
+      if (e >= 0 && e < E) msk[e] = 0u;
+    }
+  __syncwarp();
+  if (valid)
+    for (int64_t j = 0; j < k; ++j) {
+      const int32_t e = idx[t * k + j];
+      if (e >= 0 && e < E) {
+        const uint32_t old = atomicOr(&msk[e], 1u << lane);
+        if (old & (1u << lane)) record_error(status, kErrIndex, 104, (int32_t)t, e);  // expert listed twice
+      }
+    }
+  __syncwarp();
+  if (valid)
+    for (int64_t j = 0; j < k; ++j) {
+      const int32_t e = idx[t * k + j];
+      int32_t row = -1;
+      if (e >= 0 && e < E) {
+        const int64_t r = (int64_t)tile_base[(int64_t)e * (T + 1) + tile] + __popc(msk[e] & lt);
+        if (r < cap) {
+          row = expert_off[e] + (int32_t)r;
+          row_token[row] = (int32_t)t;
+          row_gate[row] = gate[t * k + j];
+        }
+      } else {
+        record_error(status, kErrIndex, 102, (int32_t)t, e);
+      }
+      tok_rows[t * k + j] = row;
+    }
+  __syncwarp();
+  // copy the tile's tokens into their rows: x read once, written per kept choice.
+  // Every lane runs every chunk iteration so the row shuffles see the full warp.
+  const int64_t nchunk = d / VT::n;
+  for (int tt = 0; tt < kTileTokens; ++tt) {
+    const int64_t tok = tile * kTileTokens + tt;
+    if (tok >= N) break;
+    const int32_t my_row = lane < k ? tok_rows[tok * k + lane] : -1;
+    const uint4* src = reinterpret_cast<const uint4*>(x) + tok * nchunk;
+    for (int64_t c0 = 0; c0 < nchunk; c0 += 32) {
+      const int64_t c = c0 + lane;
+      const bool act = c < nchunk;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (act) v = __ldg(src + c);
+      for (int j = 0; j < k; ++j) {
+        const int32_t row = __shfl_sync(kFull, my_row, j);
+        if (act && row >= 0) reinterpret_cast<uint4*>(xp)[(int64_t)row * nchunk + c] = v;
+      }
+    }
+  }
+}
+
+// ---- expert choice -----------------------------------------------------------
+
+__global__ void __launch_bounds__(1024) ec_select_kernel(const float* __restrict__ probs, int64_t N, int64_t E,
+                                                         int64_t cap, int32_t* __restrict__ idx,
+                                                         float* __restrict__ gate) {
+  __shared__ int hist[256];
+  __shared__ int s_warp[33];
+  __shared__ uint32_t s_prefix;
+  __shared__ int s_remaining;
+  const int64_t e = blockIdx.x;
+  uint32_t prefix = 0, pmask = 0;
+  if (threadIdx.x == 0) s_remaining = (int)cap;
+  for (int pass = 0; pass < 4; ++pass) {
+    const int shift = 24 - 8 * pass;
+    for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0;
+    __syncthreads();
+    for (int64_t t = threadIdx.x; t < N; t += blockDim.x) {
+      const uint32_t u = __float_as_uint(probs[t * E + e]);  // p >= 0: bit order = value order
+      if ((u & pmask) == prefix) atomicAdd(&hist[(u >> shift) & 255u], 1);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      int acc = 0, rem = s_remaining, b = 255;
+      for (; b > 0; --b) {
+        if (acc + hist[b] >= rem) break;
+        acc += hist[b];
+      }
+      s_remaining = rem - acc;
+      s_prefix = prefix | ((uint32_t)b << shift);
+    }
+    __syncthreads();
+    prefix = s_prefix;
+    pmask |= 255u << shift;
+  }
+  const uint32_t thr = prefix;
+  const int need = s_remaining;  // ties equal to thr to take, first in token order
+  int carry_eq = 0, carry_sel = 0;
+  for (int64_t base = 0; base < N; base += blockDim.x) {
+    const int64_t t = base + threadIdx.x;
+    const uint32_t u = t < N ? __float_as_uint(probs[t * E + e]) : 0u;
+    const int gt = (t < N && u > thr) ? 1 : 0;
+    const int eq = (t < N && u == thr) ? 1 : 0;
+    int tot_eq = 0, tot_sel = 0;
+    const int eq_rank = block_exclusive_scan(eq, s_warp, &tot_eq) + carry_eq;
+    const int sel = gt | (eq & (eq_rank < need ? 1 : 0));
+    const int pos = block_exclusive_scan(sel, s_warp, &tot_sel) + carry_sel;
+    if (sel && pos < cap) {
+      idx[e * cap + pos] = (int32_t)t;
+      gate[e * cap + pos] = __uint_as_float(u);
+    }
+    carry_eq += tot_eq;
+    carry_sel += tot_sel;
+  }
+}
+
+__global__ void ec_mark_kernel(const int32_t* __restrict__ idx, const float* __restrict__ gate, int64_t N,
+                               int64_t E, int64_t cap, int64_t words, uint32_t* __restrict__ bits,
+                               int32_t* __restrict__ row_token, float* __restrict__ row_gate,
+                               int32_t* __restrict__ expert_off, int32_t* status) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i <= E) expert_off[i] = (int32_t)(i * cap);
+  if (i >= E * cap) return;
+  const int64_t e = i / cap;
+  const int32_t t = idx[i];
+  row_gate[i] = gate[i];
+  row_token[i] = t;
+  if (t < 0 || t >= N) {
+    record_error(status, kErrIndex, 103, (int32_t)i, t);
+    return;
+  }
+  atomicOr(&bits[(int64_t)t * words + (e >> 5)], 1u << (e & 31));
+}
+
+__global__ void __launch_bounds__(1024) ec_tok_scan_kernel(const uint32_t* __restrict__ bits, int64_t N,
+                                                           int64_t E, int64_t words, int64_t cap,
+                                                           int32_t* __restrict__ tok_off, void* stats) {
+  __shared__ int s_warp[33];
+  const int64_t per = ceil_div(N, (int64_t)blockDim.x);
+  const int64_t t0 = (int64_t)threadIdx.x * per;
+  const int64_t t1 = t0 + per < N ? t0 + per : N;
+  int local = 0;
+  for (int64_t t = t0; t < t1; ++t)
+    for (int64_t w = 0; w < words; ++w) local += __popc(bits[t * words + w]);
+  int total = 0;
+  int run = block_exclusive_scan(local, s_warp, &total);
+  for (int64_t t = t0; t < t1; ++t) {
+    tok_off[t] = run;
+    for (int64_t w = 0; w < words; ++w) run += __popc(bits[t * words + w]);
+  }
+  if (threadIdx.x == 0) tok_off[N] = total;
+  if (stats && threadIdx.x == 0) {
+    moe_stats_header* hdr = static_cast<moe_stats_header*>(stats);
+    hdr->dropped = 0;
+    hdr->dropped_share = 0.f;
+    hdr->capacity = (int32_t)cap;
+    hdr->rows = (int32_t)(E * cap);
+    hdr->n_experts = (int32_t)E;
+  }
+  if (stats) {
+    moe_stats_header* hdr = static_cast<moe_stats_header*>(stats);
+    int32_t* kept_out = reinterpret_cast<int32_t*>(reinterpret_cast<float*>(hdr + 1) + 2 * E) + E;
+    for (int64_t e = threadIdx.x; e < E; e += blockDim.x) kept_out[e] = (int32_t)cap;
+  }
+}
+
+// One warp per token: its experts in ascending id, each located in that
+// expert's ascending token list by binary search -> rows e*C + c.
+__global__ void __launch_bounds__(kWarps * 32) ec_fill_kernel(const uint32_t* __restrict__ bits,
+                                                              const int32_t* __restrict__ idx,
+                                                              const int32_t* __restrict__ tok_off, int64_t N,
+                                                              int64_t words, int64_t cap,
+                                                              int32_t* __restrict__ tok_rows) {
+  const int lane = threadIdx.x & 31;
+  const int64_t t = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
+  if (t >= N) return;
+  const uint32_t word = lane < words ? bits[t * words + lane] : 0u;
+  const int c = __popc(word);
+  const int excl = warp_inclusive_scan(c) - c;
+  int pos = tok_off[t] + excl;
+  uint32_t wleft = word;
+  while (wleft) {
+    const int b = __ffs(wleft) - 1;
+    wleft &= wleft - 1;
+    const int64_t e = (int64_t)lane * 32 + b;
+    const int32_t* list = idx + e * cap;
+    int64_t lo = 0, hi = cap;  // first position with list[pos] >= t
+    while (lo < hi) {
+      const int64_t mid = (lo + hi) >> 1;
+      if (list[mid] < t) lo = mid + 1; else hi = mid;
+    }
+    tok_rows[pos++] = (int32_t)(e * cap + lo);
+  }
+}
+
+// Copy x rows into xp by a token's row list (expert choice CSR).
+template <typename T>
+__global__ void __launch_bounds__(kWarps * 32) copy_rows_csr_kernel(const T* __restrict__ x,
+                                                                    const int32_t* __restrict__ tok_rows,
+                                                                    const int32_t* __restrict__ tok_off, int64_t N,
+                                                                    int64_t d, T* __restrict__ xp) {
+  using VT = Vec16<T>;
+  const int lane = threadIdx.x & 31;
+  const int64_t nchunk = d / VT::n;
+  for (int64_t t = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5); t < N; t += (int64_t)gridDim.x * kWarps) {
+    const int32_t beg = tok_off[t], n = tok_off[t + 1] - beg;
+    const uint4* src = reinterpret_cast<const uint4*>(x) + t * nchunk;
+    for (int64_t c = lane; c < nchunk; c += 32) {
+      const uint4 v = __ldg(src + c);
+      for (int i = 0; i < n; ++i) reinterpret_cast<uint4*>(xp)[(int64_t)tok_rows[beg + i] * nchunk + c] = v;
+    }
+  }
+}
+
+// out[t] = ys[t] + sum of yp over t's rows in list order (fp32 accumulation, one rounding).
+template <typename T>
+__global__ void __launch_bounds__(kWarps * 32) combine_kernel(const T* __restrict__ yp,
+                                                              const int32_t* __restrict__ tok_rows,
+                                                              const int32_t* __restrict__ tok_off,
+                                                              const T* __restrict__ ys, int64_t N, int64_t d,
+                                                              int64_t k, T* __restrict__ out) {
+  using VT = Vec16<T>;
+  constexpr int VN = VT::n;
+  const int lane = threadIdx.x & 31;
+  const int64_t nchunk = d / VN;
+  for (int64_t t = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5); t < N; t += (int64_t)gridDim.x * kWarps) {
+    int64_t beg, n;
+    if (tok_off) {
+      beg = tok_off[t];
+      n = tok_off[t + 1] - beg;
+    } else {
+      beg = t * k;
+      n = k;
+    }
+    const int32_t my_row = lane < n ? tok_rows[beg + lane] : -1;
+    for (int64_t c0 = 0; c0 < nchunk; c0 += 32) {
+      const int64_t c = c0 + lane;
+      const bool act = c < nchunk;
+      float acc[VN];
+#pragma unroll
+      for (int i = 0; i < VN; ++i) acc[i] = 0.f;
+      if (ys && act) VT::unpack(__ldg(reinterpret_cast<const uint4*>(ys) + t * nchunk + c), acc);
+      for (int64_t j = 0; j < n; ++j) {
+        const int32_t row = j < 32 ? __shfl_sync(kFull, my_row, (int)j) : tok_rows[beg + j];
+        if (act && row >= 0) {
+          float v[VN];
+          VT::unpack(__ldg(reinterpret_cast<const uint4*>(yp) + (int64_t)row * nchunk + c), v);
+#pragma unroll
+          for (int i = 0; i < VN; ++i) acc[i] += v[i];
+        }
+      }
+      if (act) reinterpret_cast<uint4*>(out)[t * nchunk + c] = VT::pack(acc);
+    }
+  }
+}
+
+template <typename T>
+cudaError_t launch_permute_t(const Plan& p, const void* x, const int32_t* idx, const float* gate, void* xp,
+                             int32_t* tok_rows, int32_t* tok_off, int32_t* expert_off, int32_t* row_token,
+                             float* row_gate, void* stats, void* ws, cudaStream_t st) {
+  int32_t* status = status_ptr(p, ws);
+  if (p.ec) {
+    uint32_t* bits = ws_at<uint32_t>(ws, p.ec_bits);
+    cudaError_t err = cudaMemsetAsync(bits, 0, (size_t)(p.N * p.words) * 4, st);
+    if (err != cudaSuccess) return err;
+    const int64_t n = p.E * p.cap;
+    const int64_t nb = ceil_div(n > p.E + 1 ? n : p.E + 1, 256);
+    ec_mark_kernel<<<(unsigned)nb, 256, 0, st>>>(idx, gate, p.N, p.E, p.cap, p.words, bits, row_token, row_gate,
+                                                 expert_off, status);
+    ec_tok_scan_kernel<<<1, 1024, 0, st>>>(bits, p.N, p.E, p.words, p.cap, tok_off, stats);
+    ec_fill_kernel<<<(unsigned)ceil_div(p.N, kWarps), kWarps * 32, 0, st>>>(bits, idx, tok_off, p.N, p.words, p.cap,
+                                                                            tok_rows);
+    const int64_t blocks = ceil_div(p.N, kWarps) < 148 * 16 ? ceil_div(p.N, kWarps) : 148 * 16;
+    copy_rows_csr_kernel<T><<<(unsigned)blocks, kWarps * 32, 0, st>>>(static_cast<const T*>(x), tok_rows, tok_off,
+                                                                      p.N, p.d, static_cast<T*>(xp));
+    return cudaGetLastError();
+  }
+  int32_t* tile_counts = ws_at<int32_t>(ws, p.tile_counts);
+  int32_t* tile_base = ws_at<int32_t>(ws, p.tile_base);
+  const unsigned tb = (unsigned)ceil_div(p.tiles, kWarps);
+  const size_t hist_smem = (size_t)kWarps * p.E * 4;
+  count_kernel<<<tb, kWarps * 32, hist_smem, st>>>(idx, p.N, p.k, p.E, p.tiles, tile_counts, status);
+  scan_kernel<<<(unsigned)ceil_div(p.E, kWarps), kWarps * 32, 0, st>>>(tile_counts, p.E, p.tiles, tile_base);
+  offsets_kernel<<<1, 512, 0, st>>>(tile_base, p.E, p.tiles, p.cap, p.N, p.k, expert_off, stats);
+  scatter_kernel<T><<<tb, kWarps * 32, hist_smem, st>>>(static_cast<const T*>(x), idx, gate, tile_base, expert_off,
+                                                        p.N, p.d, p.k, p.E, p.tiles, p.cap, static_cast<T*>(xp),
+                                                        tok_rows, row_token, row_gate, status);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_ec_select(const Plan& p, const float* probs, int32_t* idx, float* gate, void* ws,
+                             cudaStream_t st) {
+  (void)ws;
+  ec_select_kernel<<<(unsigned)p.E, 1024, 0, st>>>(probs, p.N, p.E, p.cap, idx, gate);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_permute(const Plan& p, const void* x, const int32_t* idx, const float* gate, void* xp,
+                           int32_t* tok_rows, int32_t* tok_off, int32_t* expert_off, int32_t* row_token,
+                           float* row_gate, void* stats, void* ws, cudaStream_t st) {
+  if (p.bf16)
+    return launch_permute_t<__nv_bfloat16>(p, x, idx, gate, xp, tok_rows, tok_off, expert_off, row_token, row_gate,
+                                           stats, ws, st);
+  return launch_permute_t<float>(p, x, idx, gate, xp, tok_rows, tok_off, expert_off, row_token, row_gate, stats, ws,
+                                 st);
+}
+
+cudaError_t launch_combine(const Plan& p, const void* yp, const int32_t* tok_rows, const int32_t* tok_off,
+                           const void* ys, void* out, cudaStream_t st) {
+  const int64_t blocks = ceil_div(p.N, kWarps) < 148 * 16 ? ceil_div(p.N, kWarps) : 148 * 16;
+  if (p.bf16) {
+    combine_kernel<__nv_bfloat16><<<(unsigned)blocks, kWarps * 32, 0, st>>>(
+        static_cast<const __nv_bfloat16*>(yp), tok_rows, p.ec ? tok_off : nullptr,
+        static_cast<const __nv_bfloat16*>(ys), p.N, p.d, p.k, static_cast<__nv_bfloat16*>(out));
+  } else {
+    combine_kernel<float><<<(unsigned)blocks, kWarps * 32, 0, st>>>(static_cast<const float*>(yp), tok_rows,
+                                                                    p.ec ? tok_off : nullptr,
+                                                                    static_cast<const float*>(ys), p.N, p.d, p.k,
+                                                                    static_cast<float*>(out));
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,159 @@
+"""Parity of the sm_103a library (through its C ABI) with the CPU oracle.
+
+Small layers are compared in full; they span several 128-row GEMM tiles, a
+ragged last tile, every gate rule, drops, shared experts, GELU and SwiGLU, fp32
+and bf16, and the tile widths 64/128/256. The workload shapes themselves run at
+full size with routing compared on every token and outputs on sampled tokens.
+"""
+import numpy as np
+import pytest
+import torch
+
+import sparse_expert_ffn_softmax_b300 as moe
+from sparse_expert_ffn_softmax_b300 import WORKLOADS, Workload
+from gpu_check import check, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+def wl(name, **kw):
+    base = dict(name=name, n_tokens=64, d_model=64, d_ff=128, n_experts=8, top_k=2, capacity_factor=1.25,
+                gating="softmax_topk", act="gelu", dtype="bf16", has_bias=False)
+    base.update(kw)
+    return Workload(**base)
+
+
+SMALL = [
+    WORKLOADS["tiny_f32"],
+    wl("f32_swiglu_shared_ec", dtype="f32", act="swiglu", n_shared=2, d_ff_shared=64, gating="expert_choice",
+       capacity_factor=1.0, n_tokens=50),
+    wl("f32_renorm_drops", dtype="f32", gating="softmax_topk_renorm", capacity_factor=0.5, n_tokens=70,
+       has_bias=True),
+    wl("bf16_gelu_bias_B", n_tokens=300, d_model=128, d_ff=256, n_experts=4, top_k=2, capacity_factor=1.0,
+       gating="topk_softmax", has_bias=True),
+    wl("bf16_swiglu_shared", n_tokens=333, d_model=192, d_ff=192, n_experts=6, top_k=3, capacity_factor=1.25,
+       act="swiglu", n_shared=2, d_ff_shared=128, logit_bias_max=2.0),
+    wl("bf16_gelu_shared_bias", n_tokens=257, d_model=256, d_ff=512, n_experts=5, top_k=2, capacity_factor=0.0,
+       gating="softmax_topk_renorm", has_bias=True, n_shared=1, d_ff_shared=256),
+    wl("bf16_ec_swiglu", n_tokens=256, d_model=128, d_ff=128, n_experts=8, top_k=2, capacity_factor=1.0,
+       gating="expert_choice", act="swiglu", n_shared=1, d_ff_shared=128),
+    wl("bf16_k_eq_E", n_tokens=130, d_model=64, d_ff=64, n_experts=3, top_k=3, capacity_factor=0.0),
+    wl("bf16_one_expert", n_tokens=129, d_model=128, d_ff=128, n_experts=1, top_k=1, capacity_factor=0.0,
+       act="swiglu"),
+    wl("bf16_one_token", n_tokens=1, d_model=128, d_ff=256, n_experts=8, top_k=2, capacity_factor=1.25),
+    wl("bf16_ragged_tile", n_tokens=33, d_model=64, d_ff=192, n_experts=40, top_k=4, capacity_factor=1.0),
+    wl("bf16_many_experts", n_tokens=520, d_model=128, d_ff=128, n_experts=160, top_k=6, capacity_factor=1.25,
+       act="swiglu", n_shared=2, d_ff_shared=128, logit_bias_max=2.0),
+    wl("bf16_heavy_drops", n_tokens=1000, d_model=64, d_ff=128, n_experts=8, top_k=2, capacity_factor=0.3,
+       logit_bias_max=4.0),
+]
+
+
+@pytest.mark.parametrize("w", SMALL, ids=lambda w: w.name)
+def test_small_layers(w):
+    layer, t, res = run_gpu(w)
+    check(w, t, res)
+
+
+def test_zero_router_ties():
+    """All logits equal: every token takes experts 0..k-1, later tokens dropped."""
+    w = wl("bf16_zero_router", n_tokens=100, d_model=64, d_ff=128, n_experts=8, top_k=2, capacity_factor=1.0)
+    t = moe.make_inputs(w, "cuda")
+    t["w_router"].zero_()
+    layer, t, res = run_gpu(w, tensors=t)
+    assert np.all(res["idx"] == np.arange(2))
+    C = res["capacity"]
+    assert np.all(res["tok_rows"][C:] == -1)
+    check(w, t, res)
+
+
+def test_empty_batch_is_noop():
+    w = wl("bf16_empty", n_tokens=0)
+    cfg = moe.config(w)
+    t = moe.make_inputs(w.replace(n_tokens=1), "cuda")
+    ws = moe.alloc_workspace(cfg)
+    x = torch.empty(0, 64, dtype=torch.bfloat16, device="cuda")
+    out = torch.empty_like(x)
+    moe.forward(cfg, x, moe.weights(t), out, None, ws)
+    torch.cuda.synchronize()
+
+
+def test_deterministic():
+    w = WORKLOADS["small_bf16"].replace(n_tokens=2048)
+    t = moe.make_inputs(w, "cuda")
+    layer = moe.Layer(w, t)
+    a = layer.forward(t["x"]).clone()
+    st_a = layer.read_stats()
+    b = layer.forward(t["x"]).clone()
+    st_b = layer.read_stats()
+    assert torch.equal(a, b)
+    assert st_a["aux_loss"] == st_b["aux_loss"] and torch.equal(st_a["P"], st_b["P"])
+
+
+def test_stage_calls_match_forward():
+    """route -> permute -> expert_ffn -> combine through the separate entry points equals forward."""
+    w = wl("bf16_stages", n_tokens=300, d_model=128, d_ff=256, n_experts=6, top_k=2, capacity_factor=1.0,
+           act="swiglu", n_shared=1, d_ff_shared=128)
+    t = moe.make_inputs(w, "cuda")
+    layer = moe.Layer(w, t)
+    ref = layer.forward(t["x"]).clone()
+    cfg, ws = layer.cfg, layer.ws
+    N, k, E, d = w.n_tokens, w.top_k, w.n_experts, w.d_model
+    R = layer.layout.max_rows
+    dev = "cuda"
+    idx = torch.empty(N, k, dtype=torch.int32, device=dev)
+    gate = torch.empty(N, k, dtype=torch.float32, device=dev)
+    logits = torch.empty(N, E, dtype=torch.float32, device=dev)
+    stats = moe.alloc_stats(E)
+    moe.route(cfg, t["x"], layer.w, idx, gate, logits, None, stats, ws)
+    xp = torch.empty(R, d, dtype=torch.bfloat16, device=dev)
+    tok_rows = torch.empty(N, k, dtype=torch.int32, device=dev)
+    expert_off = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    row_token = torch.empty(R, dtype=torch.int32, device=dev)
+    row_gate = torch.empty(R, dtype=torch.float32, device=dev)
+    moe.permute(cfg, t["x"], idx, gate, xp, tok_rows, None, expert_off, row_token, row_gate, stats, ws)
+    yp = torch.empty(R, d, dtype=torch.bfloat16, device=dev)
+    ys = torch.empty(N, d, dtype=torch.bfloat16, device=dev)
+    moe.expert_ffn(cfg, xp, expert_off, row_gate, t["x"], layer.w, yp, ys, ws)
+    out = torch.empty_like(t["x"])
+    moe.combine(cfg, yp, tok_rows, None, ys, out)
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref)
+    assert moe.get_device_status(cfg, ws) == (0, 0)
+
+
+def test_device_index_check_reports():
+    """An out-of-range expert id given to moe_permute is caught by the kernels' bounds checks."""
+    w = wl("bf16_bad_idx", n_tokens=64, d_model=64, d_ff=128, n_experts=8, top_k=2, capacity_factor=0.0)
+    t = moe.make_inputs(w, "cuda")
+    cfg = moe.config(w)
+    ws = moe.alloc_workspace(cfg)
+    N, k, E, d = 64, 2, 8, 64
+    R = N * k
+    idx = torch.stack([torch.arange(N) % E, (torch.arange(N) + 1) % E], 1).to(torch.int32).cuda()
+    idx[5, 1] = 99
+    gate = torch.full((N, k), 0.5, device="cuda")
+    xp = torch.empty(R, d, dtype=torch.bfloat16, device="cuda")
+    tok_rows = torch.empty(N, k, dtype=torch.int32, device="cuda")
+    expert_off = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    row_token = torch.empty(R, dtype=torch.int32, device="cuda")
+    row_gate = torch.empty(R, dtype=torch.float32, device="cuda")
+    moe.permute(cfg, t["x"], idx, gate, xp, tok_rows, None, expert_off, row_token, row_gate, None, ws)
+    code, word = moe.get_device_status(cfg, ws)
+    assert code == 5 and (word & 1)
+    assert tok_rows[5, 1].item() == -1
+    assert moe.get_device_status(cfg, ws) == (0, 0)  # cleared by the read
+
+
+FULL = [("small_bf16", 256), ("mixtral_decode", 6), ("mixtral_prefill", 6), ("fine_skewed", 8),
+        ("large_fine", 4), ("large_fine_ec", 4), ("large_fine_decode", 4)]
+
+
+@pytest.mark.parametrize("name,n_sample", FULL, ids=[f[0] for f in FULL])
+def test_full_size_workloads(name, n_sample):
+    w = WORKLOADS[name]
+    layer, t, res = run_gpu(w)
+    rep = check(w, t, res, n_sample=n_sample)
+    print(name, rep)
+    del layer, t, res
+    torch.cuda.empty_cache()
