@@ -160,8 +160,8 @@ typedef struct moe_workspace_layout {
   size_t xp;          /* dtype [max_rows, d] permuted tokens                    */
   size_t h;           /* dtype [max_rows, F] routed hidden activations          */
   size_t hs;          /* dtype [N, S*Fs] shared hidden activations              */
-  size_t yp;          /* dtype [max_rows, d] gate-scaled expert outputs         */
-  size_t ys;          /* dtype [N, d] sum of shared expert outputs              */
+  size_t yp;          /* fp32 [max_rows, d] gate-scaled expert outputs          */
+  size_t ys;          /* fp32 [N, d] sum of shared expert outputs               */
   size_t stats;       /* moe_stats_bytes(E) used when the caller passes none    */
   size_t scratch;     /* per-kernel partial sums and tile counts                */
   int64_t max_rows;   /* token choice N*k; expert choice E*C                    */
@@ -223,8 +223,9 @@ MOE_API moe_status moe_permute(const moe_config* cfg, const void* x, const int32
  *  xp         [max_rows, d]; expert_off [E+1] (device; read on the device only).
  *  row_gate   [max_rows] fp32: yp row r = row_gate[r] * E_e(xp[r]).
  *  x          [N, d] (needed when S > 0).
- *  yp         [max_rows, d] dtype: rows [0, R) written.
- *  ys         [N, d] dtype: sum of the shared experts (written when S > 0). */
+ *  yp         [max_rows, d] fp32: rows [0, R) written (fp32 for every layer dtype,
+ *             so the combine rounds the output once).
+ *  ys         [N, d] fp32: sum of the shared experts (written when S > 0). */
 MOE_API moe_status moe_expert_ffn(const moe_config* cfg, const void* xp, const int32_t* expert_off,
                           const float* row_gate, const void* x, const moe_weights* w, void* yp, void* ys,
                           void* ws, size_t ws_bytes, void* stream);
@@ -233,7 +234,8 @@ MOE_API moe_status moe_expert_ffn(const moe_config* cfg, const void* xp, const i
  * out[t] = ys[t] + sum of yp over the token's rows, in fixed order (token choice:
  * j = 0..k-1 skipping dropped; expert choice: ascending expert id), fp32
  * accumulation and one rounding. Tokens with no kept row get ys[t] (or 0).
- *  tok_rows / tok_off as written by moe_permute; ys may be NULL. out [N, d] dtype. */
+ *  yp [max_rows, d] fp32 and ys [N, d] fp32 (may be NULL) as written by moe_expert_ffn;
+ *  tok_rows / tok_off as written by moe_permute. out [N, d] dtype. */
 MOE_API moe_status moe_combine(const moe_config* cfg, const void* yp, const int32_t* tok_rows, const int32_t* tok_off,
                        const void* ys, void* out, void* stream);
 

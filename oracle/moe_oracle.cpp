@@ -57,8 +57,8 @@ struct OracleConfig {
   int32_t has_bias;        // biases present (GELU experts only)
   int32_t dtype;           // storage of x and all weights: 0 fp32, 1 bf16 bit patterns
   double aux_alpha;
-  int32_t mimic_bf16;      // round the hidden activations and the per-expert
-                           // weighted outputs to bf16 the way a bf16 pipeline stores them
+  int32_t mimic_bf16;      // round the hidden activations and the final output to
+                           // bf16, the two places a bf16 pipeline must store bf16
   int32_t pad_;
 };
 
@@ -404,10 +404,10 @@ void oracle_combine_tokens(const OracleConfig* c, const void* x, const OracleWei
       oracle_expert_apply(c, w, 1, s, xr.data(), y.data());
       for (int64_t i = 0; i < d; ++i) sh[i] += y[i];
     }
-    for (int64_t i = 0; i < d; ++i) acc[i] = store_round(sh[i], c);
+    for (int64_t i = 0; i < d; ++i) acc[i] = sh[i];
     auto add_term = [&](int64_t e, double g) {
       oracle_expert_apply(c, w, 0, e, xr.data(), y.data());
-      for (int64_t i = 0; i < d; ++i) acc[i] += store_round(g * y[i], c);
+      for (int64_t i = 0; i < d; ++i) acc[i] += g * y[i];
     };
     if (c->gating == 3) {
       for (int64_t e = 0; e < E; ++e)

@@ -11,7 +11,7 @@
 //   up-projection   family 0: expert e's rows of xp  x  W1[e] (+W3[e])  -> H
 //                   family 1: all tokens of x  x  Ws1[s] (+Ws3[s])      -> Hs[:, s*Fs...]
 //   down-projection family 0: expert e's rows of H   x  W2[e]           -> Yp (x row gate)
-//                   family 1: all tokens of Hs x [Ws2[0] | Ws2[1] | ...] -> Ys (the shared
+//                   family 1: all tokens of Hs x [Ws2[0] | Ws2[1] | ...] -> Ys fp32 (the shared
 //                             experts concatenated along K, so their sum comes out of one
 //                             accumulator)
 // A group's rows come from the device-side expert offsets, so no host sync is
@@ -456,8 +456,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool valid = ti.mt * BM + r < ti.m;
       const int64_t grow = (int64_t)ti.a_row0 + r;
       const uint32_t tbase = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(q * 32) << 16);
-      __nv_bfloat16* out = static_cast<__nv_bfloat16*>(F.out) + grow * F.ld_out + (int64_t)ti.g * F.out_col_group +
-                           (int64_t)ti.nt * kOutCols;
+      // H tiles (GELU / SwiGLU) are stored as bf16 for the next GEMM; gate-scaled
+      // expert outputs (linear epilogue) stay fp32 until the combine's single rounding.
+      const int64_t out_off = grow * F.ld_out + (int64_t)ti.g * F.out_col_group + (int64_t)ti.nt * kOutCols;
       const int64_t bcol0 = (int64_t)ti.nt * kOutCols;
       const __nv_bfloat16* bias = F.bias ? F.bias + (int64_t)ti.g * F.bias_group : nullptr;
       float gate = 1.f;
@@ -489,9 +490,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (valid) {
-          uint4* dst = reinterpret_cast<uint4*>(out + c);
+          if (EPI == kLinear) {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<float*>(F.out) + out_off + c);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) dst[i] = Vec16<__nv_bfloat16>::pack(o + 8 * i);
+            for (int i = 0; i < 8; ++i) dst[i] = Vec16<float>::pack(o + 4 * i);
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(F.out) + out_off + c);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) dst[i] = Vec16<__nv_bfloat16>::pack(o + 8 * i);
+          }
         }
       }
       tc_fence_before();

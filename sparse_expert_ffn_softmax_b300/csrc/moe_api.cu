@@ -96,8 +96,8 @@ moe_status make_plan(const moe_config* c, Plan* p) {
   L.xp = take((size_t)p->max_rows * (size_t)p->d * b);
   L.h = take((size_t)p->max_rows * (size_t)p->F * b);
   L.hs = take((size_t)p->N * (size_t)(p->S * p->Fs) * b);
-  L.yp = take((size_t)p->max_rows * (size_t)p->d * b);
-  L.ys = take(p->S > 0 ? (size_t)p->N * (size_t)p->d * b : 0);
+  L.yp = take((size_t)p->max_rows * (size_t)p->d * 4);  // fp32 for every layer dtype
+  L.ys = take(p->S > 0 ? (size_t)p->N * (size_t)p->d * 4 : 0);
   L.stats = take(moe_stats_bytes(p->E));
   L.scratch = o;
   p->part_p = take((size_t)(p->E * p->router_blocks) * 4);

@@ -344,15 +344,17 @@ __global__ void __launch_bounds__(kWarps * 32) copy_rows_csr_kernel(const T* __r
   }
 }
 
-// out[t] = ys[t] + sum of yp over t's rows in list order (fp32 accumulation, one rounding).
-template <typename T>
-__global__ void __launch_bounds__(kWarps * 32) combine_kernel(const T* __restrict__ yp,
+// out[t] = ys[t] + sum of yp over t's rows in list order: fp32 inputs, fp32
+// accumulation, one rounding to the output type. A lane owns 16 output bytes.
+template <typename TO>
+__global__ void __launch_bounds__(kWarps * 32) combine_kernel(const float* __restrict__ yp,
                                                               const int32_t* __restrict__ tok_rows,
                                                               const int32_t* __restrict__ tok_off,
-                                                              const T* __restrict__ ys, int64_t N, int64_t d,
-                                                              int64_t k, T* __restrict__ out) {
-  using VT = Vec16<T>;
-  constexpr int VN = VT::n;
+                                                              const float* __restrict__ ys, int64_t N, int64_t d,
+                                                              int64_t k, TO* __restrict__ out) {
+  using VO = Vec16<TO>;
+  constexpr int VN = VO::n;  // outputs per lane chunk: 8 (bf16) or 4 (fp32)
+  constexpr int NV = VN / 4; // float4 loads per row and chunk
   const int lane = threadIdx.x & 31;
   const int64_t nchunk = d / VN;
   for (int64_t t = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5); t < N; t += (int64_t)gridDim.x * kWarps) {
@@ -371,17 +373,25 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(const T* __restric
       float acc[VN];
 #pragma unroll
       for (int i = 0; i < VN; ++i) acc[i] = 0.f;
-      if (ys && act) VT::unpack(__ldg(reinterpret_cast<const uint4*>(ys) + t * nchunk + c), acc);
+      if (ys && act) {
+        const uint4* src = reinterpret_cast<const uint4*>(ys + t * d + c * VN);
+#pragma unroll
+        for (int q = 0; q < NV; ++q) Vec16<float>::unpack(__ldg(src + q), acc + 4 * q);
+      }
       for (int64_t j = 0; j < n; ++j) {
         const int32_t row = j < 32 ? __shfl_sync(kFull, my_row, (int)j) : tok_rows[beg + j];
         if (act && row >= 0) {
-          float v[VN];
-          VT::unpack(__ldg(reinterpret_cast<const uint4*>(yp) + (int64_t)row * nchunk + c), v);
+          const uint4* src = reinterpret_cast<const uint4*>(yp + (int64_t)row * d + c * VN);
 #pragma unroll
-          for (int i = 0; i < VN; ++i) acc[i] += v[i];
+          for (int q = 0; q < NV; ++q) {
+            float v[4];
+            Vec16<float>::unpack(__ldg(src + q), v);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) acc[4 * q + i] += v[i];
+          }
         }
       }
-      if (act) reinterpret_cast<uint4*>(out)[t * nchunk + c] = VT::pack(acc);
+      if (act) reinterpret_cast<uint4*>(out)[t * nchunk + c] = VO::pack(acc);
     }
   }
 }
@@ -444,8 +454,8 @@ cudaError_t launch_combine(const Plan& p, const void* yp, const int32_t* tok_row
   const int64_t blocks = ceil_div(p.N, kWarps) < 148 * 16 ? ceil_div(p.N, kWarps) : 148 * 16;
   if (p.bf16) {
     combine_kernel<__nv_bfloat16><<<(unsigned)blocks, kWarps * 32, 0, st>>>(
-        static_cast<const __nv_bfloat16*>(yp), tok_rows, p.ec ? tok_off : nullptr,
-        static_cast<const __nv_bfloat16*>(ys), p.N, p.d, p.k, static_cast<__nv_bfloat16*>(out));
+        static_cast<const float*>(yp), tok_rows, p.ec ? tok_off : nullptr, static_cast<const float*>(ys), p.N, p.d,
+        p.k, static_cast<__nv_bfloat16*>(out));
   } else {
     combine_kernel<float><<<(unsigned)blocks, kWarps * 32, 0, st>>>(static_cast<const float*>(yp), tok_rows,
                                                                     p.ec ? tok_off : nullptr,

@@ -188,6 +188,13 @@ def check(w, t, res, n_sample=None, check_self_routed=True):
     else:
         assert np.max(err) <= 2e-2 * rms, f"bf16 output: max err {np.max(err)} vs 2e-2*rms {2e-2 * rms}"
     report["out_max_err_over_rms"] = float(np.max(err) / rms) if rms > 0 else 0.0
+    if w.dtype == "bf16":
+        # the same reference with bf16 stores where the pipeline has them (hidden, output):
+        # what is left is fp32-vs-fp64 accumulation, reported in output ulps
+        cfg_m = o.config(w, mimic_bf16=1, n_experts=cfg_out.n_experts)
+        ref_m = o.outputs(cfg_m, torch_to_numpy(t["x"]), ow, r_out, tokens)
+        ulp = np.maximum(np.abs(ref_m), 1e-30) * 2.0 ** -7
+        report["mimic_max_ulps"] = float(np.max(np.abs(got - ref_m) / ulp))
 
     # ---- router logits and the oracle's self-routed choice --------------------
     if check_self_routed:

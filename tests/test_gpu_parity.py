@@ -112,8 +112,8 @@ def test_stage_calls_match_forward():
     row_token = torch.empty(R, dtype=torch.int32, device=dev)
     row_gate = torch.empty(R, dtype=torch.float32, device=dev)
     moe.permute(cfg, t["x"], idx, gate, xp, tok_rows, None, expert_off, row_token, row_gate, stats, ws)
-    yp = torch.empty(R, d, dtype=torch.bfloat16, device=dev)
-    ys = torch.empty(N, d, dtype=torch.bfloat16, device=dev)
+    yp = torch.empty(R, d, dtype=torch.float32, device=dev)
+    ys = torch.empty(N, d, dtype=torch.float32, device=dev)
     moe.expert_ffn(cfg, xp, expert_off, row_gate, t["x"], layer.w, yp, ys, ws)
     out = torch.empty_like(t["x"])
     moe.combine(cfg, yp, tok_rows, None, ys, out)
