@@ -222,8 +222,12 @@ def forward(cfg, x, w: moe_weights, out, stats=None, ws=None, stream=None):
 def forward_traced(cfg, x, w: moe_weights, out, events: Sequence[torch.cuda.Event], stats=None, ws=None,
                    stream=None):
     """forward that records ``events`` (torch.cuda.Event, up to 6) between its stages."""
+    if stream is None:
+        stream = torch.cuda.current_stream()
     arr = (ctypes.c_void_p * max(1, len(events)))()
     for i, e in enumerate(events):
+        if not e.cuda_event:
+            e.record(stream)  # torch creates the CUDA event on its first record
         arr[i] = ctypes.c_void_p(e.cuda_event)
     _check(_lib.moe_forward_traced(ctypes.byref(cfg), _ptr(x), ctypes.byref(w), _ptr(out), _ptr(stats), _ptr(ws),
                                    ws.numel(), _stream(stream), arr, len(events)), "moe_forward_traced")

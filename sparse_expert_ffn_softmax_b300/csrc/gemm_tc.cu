@@ -94,16 +94,19 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
+// Test for completion of the phase with the given parity. A waiting thread is
+// suspended in hardware (up to ~1 ms) until the phase completes, so waiting does
+// not consume issue slots or shared-memory bandwidth.
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n"
       ".reg .pred p;\n"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
       "selp.u32 %0, 1, 0, p;\n"
       "}\n"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(1000000u)
       : "memory");
   return ok != 0;
 }
@@ -112,9 +115,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer();
   while (true) {
-#pragma unroll 1
-    for (int i = 0; i < 32; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
     if (globaltimer() - t0 > kTimeoutNs) return false;
   }
@@ -206,7 +207,23 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-__device__ __forceinline__ float gelu_erf(float u) { return 0.5f * u * (1.f + erff(u * 0.70710678118654752f)); }
+// GELU(u) = u * Phi(u) = 0.5 u (1 + erf(u / sqrt 2)), with erf from Abramowitz &
+// Stegun, Handbook of Mathematical Functions, formula 7.1.26 (after Hastings):
+// erf(z) = 1 - q(z), q(z) = (a1 t + ... + a5 t^5) exp(-z^2), t = 1 / (1 + p z),
+// z >= 0, |error| <= 1.5e-7 -- far below the bf16 rounding of the stored result.
+// Branch-free: u >= 0 gives u (1 - q/2), u < 0 gives u q / 2.
+__device__ __forceinline__ float gelu_as7126(float u) {
+  const float z = fabsf(u) * 0.70710678118654752f;
+  const float t = __fdividef(1.f, fmaf(0.3275911f, z, 1.f));
+  float poly = fmaf(1.061405429f, t, -1.453152027f);
+  poly = fmaf(poly, t, 1.421413741f);
+  poly = fmaf(poly, t, -0.284496736f);
+  poly = fmaf(poly, t, 0.254829592f);
+  poly *= t;
+  const float q = poly * __expf(-z * z);
+  const float h = 0.5f * q;
+  return u * (u >= 0.f ? 1.f - h : h);
+}
 
 template <int BN>
 struct Cfg {
@@ -444,7 +461,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
       const TileInfo ti = decode_tile(tile, s_start, G, G0, s_fam, off);
       const Family& F = s_fam[ti.fam];
-      const bool got = __all_sync(kFull, mbar_wait(&tfull_bar[acc], acc_phase, abort_flag) ? 1 : 0) != 0;
+      int got = 0;
+      if (lane == 0) got = mbar_wait(&tfull_bar[acc], acc_phase, abort_flag) ? 1 : 0;
+      got = __shfl_sync(kFull, got, 0);
       if (!got) {
         if (lane == 0) {
           record_error(P.status, kErrTimeout, 203, (int32_t)blockIdx.x, tile);
@@ -479,14 +498,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         } else {
           tmem_ld_wait(v);
+          float bsum[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) bsum[i] = 0.f;
+          if (bias) {
+            for (int s = 0; s < F.bias_nsum; ++s) {
+              const uint4* bp = reinterpret_cast<const uint4*>(bias + s * F.bias_sum_stride + bcol0 + c);
+#pragma unroll
+              for (int q4 = 0; q4 < 4; ++q4) {
+                float bv[8];
+                Vec16<__nv_bfloat16>::unpack(__ldg(bp + q4), bv);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) bsum[8 * q4 + i] += bv[i];
+              }
+            }
+          }
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
-            float a = __uint_as_float(v[i]);
-            if (bias) {
-              for (int s = 0; s < F.bias_nsum; ++s)
-                a += __bfloat162float(bias[s * F.bias_sum_stride + bcol0 + c + i]);
-            }
-            o[i] = EPI == kGelu ? gelu_erf(a) : a * gate;
+            const float a = __uint_as_float(v[i]) + bsum[i];
+            o[i] = EPI == kGelu ? gelu_as7126(a) : a * gate;
           }
         }
         if (valid) {

@@ -8,7 +8,7 @@ routing, the GPU's own fp32 logits / probabilities) and compares:
 * gates, probabilities and statistics: relative 1e-5
 * permuted rows: bit-exact copies of the token rows
 * outputs: fp32 layers |y - y_ref| <= 1e-4 (|y_ref| + rms(y_ref)) per element;
-  bf16 layers max |y - y_ref| <= 2e-2 rms(y_ref)
+  bf16 layers max (|y - y_ref| - half a bf16 ulp of y_ref) <= 2e-2 rms(y_ref)
 * the router logits themselves against the oracle's fp64-accumulated logits,
   and the oracle's self-routed choice, which may differ only at near-ties
 """
@@ -87,6 +87,13 @@ def host_weights(t, experts=None):
     return h
 
 
+def half_ulp_bf16(v):
+    """Half the spacing of bf16 values at |v| (8 significant bits)."""
+    a = np.abs(np.asarray(v, np.float64))
+    e = np.floor(np.log2(np.maximum(a, 2.0 ** -126)))
+    return 0.5 * 2.0 ** (e - 7)
+
+
 def rel_err(a, b, floor=1e-30):
     a = np.asarray(a, np.float64)
     b = np.asarray(b, np.float64)
@@ -97,7 +104,8 @@ def check(w, t, res, n_sample=None, check_self_routed=True):
     o = oracle()
     N, E, k, d = w.n_tokens, w.n_experts, w.top_k, w.d_model
     ec = w.gating == "expert_choice"
-    cfg = o.config(w)
+    # the library reads the capacity factor as an fp32; give the oracle the same value
+    cfg = o.config(w, capacity_factor=float(np.float32(w.capacity_factor)))
     report = {}
 
     # ---- routing from the GPU's own logits: bit-exact -----------------------
@@ -166,7 +174,7 @@ def check(w, t, res, n_sample=None, check_self_routed=True):
         hw = host_weights(t, experts)
         remap = np.full(E, -1, np.int32)
         remap[experts] = np.arange(len(experts), dtype=np.int32)
-        cfg_out = o.config(w, n_experts=len(experts))
+        cfg_out = o.config(w, n_experts=len(experts), capacity_factor=cfg.capacity_factor)
         r_out = dict(r)
         if ec:
             r_out["sel"] = np.ascontiguousarray(r["sel"][experts])
@@ -186,15 +194,21 @@ def check(w, t, res, n_sample=None, check_self_routed=True):
         bound = 1e-4 * (np.abs(ref) + rms)
         assert np.all(err <= bound), f"fp32 output: worst excess {np.max(err - bound)}"
     else:
-        assert np.max(err) <= 2e-2 * rms, f"bf16 output: max err {np.max(err)} vs 2e-2*rms {2e-2 * rms}"
+        # A bf16 output cannot be nearer the exact value than half its own ulp; the
+        # 2e-2 x rms bar applies to the error beyond that quantisation.
+        half_ulp = half_ulp_bf16(ref)
+        excess = np.maximum(err - half_ulp, 0.0)
+        assert np.max(excess) <= 2e-2 * rms, \
+            f"bf16 output: max err beyond half an ulp {np.max(excess)} vs 2e-2*rms {2e-2 * rms}"
     report["out_max_err_over_rms"] = float(np.max(err) / rms) if rms > 0 else 0.0
     if w.dtype == "bf16":
-        # the same reference with bf16 stores where the pipeline has them (hidden, output):
-        # what is left is fp32-vs-fp64 accumulation, reported in output ulps
-        cfg_m = o.config(w, mimic_bf16=1, n_experts=cfg_out.n_experts)
+        # the same reference with bf16 stores where the pipeline has them (hidden
+        # activations, output): what is left is fp32-vs-fp64 accumulation and
+        # rounding flips
+        cfg_m = o.config(w, mimic_bf16=1, n_experts=cfg_out.n_experts, capacity_factor=cfg.capacity_factor)
         ref_m = o.outputs(cfg_m, torch_to_numpy(t["x"]), ow, r_out, tokens)
-        ulp = np.maximum(np.abs(ref_m), 1e-30) * 2.0 ** -7
-        report["mimic_max_ulps"] = float(np.max(np.abs(got - ref_m) / ulp))
+        report["mimic_max_err_over_rms"] = float(np.max(np.abs(got - ref_m)) / rms) if rms > 0 else 0.0
+        report["out_max_excess_over_rms"] = float(np.max(excess) / rms) if rms > 0 else 0.0
 
     # ---- router logits and the oracle's self-routed choice --------------------
     if check_self_routed:
