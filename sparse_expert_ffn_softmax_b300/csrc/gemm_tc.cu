@@ -45,7 +45,7 @@ constexpr int kThreads = 64 + kEpiWarps * 32;
 constexpr int kMaxGroups = 512 + 64;  // E <= 512 routed + S <= 64 shared groups
 constexpr unsigned long long kTimeoutNs = 2000000000ull;
 
-enum Epi { kGelu = 0, kSwiglu = 1, kLinear = 2 };
+enum Epi { kGelu = 0, kSwiglu = 1, kLinear = 2, kLogits = 3 };
 
 struct Family {
   int32_t groups;       // groups in the family (0 = unused)
@@ -67,6 +67,10 @@ struct Family {
   int32_t bias_nsum;        // bias vectors summed per column (0 = no bias)
   int32_t pad1;
   const float* row_gate;  // per output row scale, or null
+  const float* bias_f32;  // kLogits: fp32 per-column bias, or null
+  int64_t n_valid;        // kLogits: columns < n_valid are stored
+  int32_t tma_out;        // bf16 outputs: store full 32-row blocks through the family's output tensor map
+  int32_t pad2;
 };
 
 struct Params {
@@ -94,28 +98,46 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
-// Test for completion of the phase with the given parity. A waiting thread is
-// suspended in hardware (up to ~1 ms) until the phase completes, so waiting does
-// not consume issue slots or shared-memory bandwidth.
+// Test for completion of the phase with the given parity. kSleep: a waiting
+// thread is suspended in hardware (up to ~1 ms) until the phase completes, so a
+// long wait costs no issue slots (epilogue warps waiting for a whole mainloop);
+// otherwise the test returns at once (the single producer and MMA threads, whose
+// short waits are on the critical path, poll).
+template <bool kSleep>
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
-  asm volatile(
-      "{\n"
-      ".reg .pred p;\n"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
-      "selp.u32 %0, 1, 0, p;\n"
-      "}\n"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity), "r"(1000000u)
-      : "memory");
+  if (kSleep) {
+    asm volatile(
+        "{\n"
+        ".reg .pred p;\n"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+        "selp.u32 %0, 1, 0, p;\n"
+        "}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(1000000u)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n"
+        ".reg .pred p;\n"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        "selp.u32 %0, 1, 0, p;\n"
+        "}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+  }
   return ok != 0;
 }
 // Bounded wait: false after kTimeoutNs or once another role has aborted.
+template <bool kSleep>
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int32_t* abort_flag) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_try_wait<kSleep>(bar, parity)) return true;
   const unsigned long long t0 = globaltimer();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+#pragma unroll 1
+    for (int i = 0; i < (kSleep ? 1 : 64); ++i)
+      if (mbar_try_wait<kSleep>(bar, parity)) return true;
     if (*abort_flag) return false;
     if (globaltimer() - t0 > kTimeoutNs) return false;
   }
@@ -127,6 +149,22 @@ __device__ __forceinline__ void tma_load_2d(const CUtensorMap* map, uint64_t* ba
           smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y)
       : "memory");
+}
+// Bulk tensor store smem -> global (bulk-group completion).
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int32_t x, int32_t y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(smem_u32(src)), "r"(x), "r"(y)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until no committed bulk store is still reading shared memory.
+__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// Wait until every committed bulk store has completed.
+__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Make this thread's generic-proxy shared-memory writes visible to the async proxy (TMA).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
@@ -207,22 +245,38 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
+__device__ __forceinline__ float ex2_ftz(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float rcp_ftz(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // GELU(u) = u * Phi(u) = 0.5 u (1 + erf(u / sqrt 2)), with erf from Abramowitz &
 // Stegun, Handbook of Mathematical Functions, formula 7.1.26 (after Hastings):
 // erf(z) = 1 - q(z), q(z) = (a1 t + ... + a5 t^5) exp(-z^2), t = 1 / (1 + p z),
 // z >= 0, |error| <= 1.5e-7 -- far below the bf16 rounding of the stored result.
-// Branch-free: u >= 0 gives u (1 - q/2), u < 0 gives u q / 2.
+// Substituting z = s / sqrt(log2 e) with s = |u| sqrt(log2(e) / 2) gives
+// exp(-z^2) = 2^(-s^2) and t = 1 / (1 + p' s), p' = p / sqrt(log2 e); the
+// polynomial coefficients carry the factor 1/2 of Phi. Branch-free:
+// u >= 0 gives u - u q/2, u < 0 gives u q/2.
 __device__ __forceinline__ float gelu_as7126(float u) {
-  const float z = fabsf(u) * 0.70710678118654752f;
-  const float t = __fdividef(1.f, fmaf(0.3275911f, z, 1.f));
-  float poly = fmaf(1.061405429f, t, -1.453152027f);
-  poly = fmaf(poly, t, 1.421413741f);
-  poly = fmaf(poly, t, -0.284496736f);
-  poly = fmaf(poly, t, 0.254829592f);
-  poly *= t;
-  const float q = poly * __expf(-z * z);
-  const float h = 0.5f * q;
-  return u * (u >= 0.f ? 1.f - h : h);
+  constexpr float kS = 0.8493218002880191f;  // sqrt(log2(e) / 2)
+  constexpr float kP = 0.2727374808792225f;  // 0.3275911 / sqrt(log2 e)
+  constexpr float kA1 = 0.5f * 0.254829592f, kA2 = 0.5f * -0.284496736f, kA3 = 0.5f * 1.421413741f,
+                  kA4 = 0.5f * -1.453152027f, kA5 = 0.5f * 1.061405429f;
+  const float s = fabsf(u) * kS;
+  const float t = rcp_ftz(fmaf(kP, s, 1.f));
+  float poly = fmaf(kA5, t, kA4);
+  poly = fmaf(poly, t, kA3);
+  poly = fmaf(poly, t, kA2);
+  poly = fmaf(poly, t, kA1);
+  const float hq = u * (poly * t) * ex2_ftz(-s * s);  // u q / 2
+  return u >= 0.f ? u - hq : hq;
 }
 
 template <int BN>
@@ -230,9 +284,10 @@ struct Cfg {
   static constexpr int kABytes = BM * BK * 2;
   static constexpr int kBBytes = BN * BK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
-  static constexpr int kStages = (196 * 1024) / kStageBytes > 8 ? 8 : (196 * 1024) / kStageBytes;
+  static constexpr int kStages = (192 * 1024) / kStageBytes > 8 ? 8 : (192 * 1024) / kStageBytes;
   static constexpr int kTmemCols = 2 * BN;
-  static constexpr size_t kSmem = (size_t)kStages * kStageBytes + 1024;
+  static constexpr int kStagingBytes = 2048;  // per epilogue warp: 32 rows x 64 B (bf16 block of 32 x 32)
+  static constexpr size_t kSmem = (size_t)kStages * kStageBytes + (size_t)kEpiWarps * kStagingBytes + 1024;
 };
 
 struct TileInfo {
@@ -284,6 +339,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap m0, const __grid_constant__ CUtensorMap m1,
                         const __grid_constant__ CUtensorMap m2, const __grid_constant__ CUtensorMap m3,
                         const __grid_constant__ CUtensorMap m4, const __grid_constant__ CUtensorMap m5,
+                        const __grid_constant__ CUtensorMap o0, const __grid_constant__ CUtensorMap o1,
                         const __grid_constant__ Params P) {
   using C = Cfg<BN>;
   constexpr int kStages = C::kStages;
@@ -364,7 +420,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const CUtensorMap* mb = pick_map(F.b_map, m0, m1, m2, m3, m4, m5);
         const CUtensorMap* mb3 = pick_map(F.b3_map, m0, m1, m2, m3, m4, m5);
         for (int kb = 0; kb < F.k_blocks; ++kb) {
-          if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag)) {
+          if (!mbar_wait<false>(&empty_bar[stage], phase ^ 1u, abort_flag)) {
             ok = false;
             break;
           }
@@ -394,7 +450,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < kStages; ++s)
           if (last_parity[s] >= 0) {
             const unsigned long long t0 = globaltimer();
-            while (!mbar_try_wait(&full_bar[s], (uint32_t)last_parity[s]) && globaltimer() - t0 < kTimeoutNs) {
+            while (!mbar_try_wait<true>(&full_bar[s], (uint32_t)last_parity[s]) && globaltimer() - t0 < kTimeoutNs) {
             }
           }
       }
@@ -408,14 +464,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
         const TileInfo ti = decode_tile(tile, s_start, G, G0, s_fam, off);
         const int kblocks = s_fam[ti.fam].k_blocks;
-        if (!mbar_wait(&tempty_bar[acc], acc_phase ^ 1u, abort_flag)) {
+        if (!mbar_wait<false>(&tempty_bar[acc], acc_phase ^ 1u, abort_flag)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
         for (int kb = 0; kb < kblocks; ++kb) {
-          if (!mbar_wait(&full_bar[stage], phase, abort_flag)) {
+          if (!mbar_wait<false>(&full_bar[stage], phase, abort_flag)) {
             ok = false;
             break;
           }
@@ -447,22 +503,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       // every MMA this thread issued has finished before TMEM is released
       umma_commit(&done_bar);
       const unsigned long long t0 = globaltimer();
-      while (!mbar_try_wait(&done_bar, 0u) && globaltimer() - t0 < kTimeoutNs) {
+      while (!mbar_try_wait<true>(&done_bar, 0u) && globaltimer() - t0 < kTimeoutNs) {
       }
     }
   } else {
     // ---------------- epilogue warps ----------------
     const int ew = warp - 2;
     const int q = warp & 3;       // TMEM lane quadrant this warp may read
-    const int half = ew >> 2;     // which interleaved half of the column chunks
+    const int half = ew >> 2;     // which interleaved half of the 32-column chunks
     const int r = q * 32 + lane;  // row inside the tile
+    uint8_t* staging = smem + kStages * C::kStageBytes + ew * C::kStagingBytes;
+    bool store_pending = false;
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
       const TileInfo ti = decode_tile(tile, s_start, G, G0, s_fam, off);
       const Family& F = s_fam[ti.fam];
       int got = 0;
-      if (lane == 0) got = mbar_wait(&tfull_bar[acc], acc_phase, abort_flag) ? 1 : 0;
+      if (lane == 0) got = mbar_wait<true>(&tfull_bar[acc], acc_phase, abort_flag) ? 1 : 0;
       got = __shfl_sync(kFull, got, 0);
       if (!got) {
         if (lane == 0) {
@@ -473,31 +531,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       const bool valid = ti.mt * BM + r < ti.m;
+      // bf16 outputs of a warp whose 32 rows all belong to the group go out as one
+      // TMA block store; a group's ragged last rows are stored row by row.
+      const bool use_tma = (EPI == kGelu || EPI == kSwiglu) && F.tma_out && ti.mt * BM + q * 32 + 32 <= ti.m;
       const int64_t grow = (int64_t)ti.a_row0 + r;
       const uint32_t tbase = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(q * 32) << 16);
       // H tiles (GELU / SwiGLU) are stored as bf16 for the next GEMM; gate-scaled
       // expert outputs (linear epilogue) stay fp32 until the combine's single rounding.
       const int64_t out_off = grow * F.ld_out + (int64_t)ti.g * F.out_col_group + (int64_t)ti.nt * kOutCols;
+      const int32_t ox0 = (int32_t)((int64_t)ti.g * F.out_col_group + (int64_t)ti.nt * kOutCols);
+      const int32_t oy = ti.a_row0 + q * 32;
+      const CUtensorMap* omap = ti.fam == 0 ? &o0 : &o1;
       const int64_t bcol0 = (int64_t)ti.nt * kOutCols;
       const __nv_bfloat16* bias = F.bias ? F.bias + (int64_t)ti.g * F.bias_group : nullptr;
       float gate = 1.f;
       if (EPI == kLinear && F.row_gate && valid) gate = F.row_gate[grow];
-      for (int c = half * 32; c < kOutCols; c += 64) {
-        uint32_t v[32];
-        tmem_ld32(tbase + (uint32_t)c, v);
+
+      // one 32-column chunk: registers v (and u, the W3 half for SwiGLU) -> outputs
+      auto finish_chunk = [&](uint32_t(&v)[32], uint32_t(&u)[32], int c) {
         float o[32];
         if (EPI == kSwiglu) {
-          uint32_t u[32];
-          tmem_ld32(tbase + (uint32_t)(BN / 2 + c), u);
-          tmem_ld_wait(u);
-          reg_fence(v);
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
             const float a = __uint_as_float(v[i]);
             o[i] = a / (1.f + __expf(-a)) * __uint_as_float(u[i]);
           }
         } else {
-          tmem_ld_wait(v);
           float bsum[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) bsum[i] = 0.f;
@@ -513,13 +572,46 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
             }
           }
+          if (EPI == kLogits && F.bias_f32) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const int64_t col = bcol0 + c + i;
+              bsum[i] += col < F.n_valid ? __ldg(F.bias_f32 + col) : 0.f;
+            }
+          }
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
             const float a = __uint_as_float(v[i]) + bsum[i];
-            o[i] = EPI == kGelu ? gelu_as7126(a) : a * gate;
+            o[i] = EPI == kGelu ? gelu_as7126(a) : (EPI == kLogits ? a : a * gate);
           }
         }
-        if (valid) {
+        if (use_tma) {
+          // staging: row `lane`, 16-byte chunk j at chunk j ^ ((row >> 1) & 3) (64-byte swizzle)
+          if (lane == 0 && store_pending) bulk_wait_read0();
+          __syncwarp();
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            *reinterpret_cast<uint4*>(staging + lane * 64 + 16 * (j ^ ((lane >> 1) & 3))) =
+                Vec16<__nv_bfloat16>::pack(o + 8 * j);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(omap, staging, ox0 + c, oy);
+            bulk_commit();
+          }
+          store_pending = true;
+        } else if (valid && EPI == kLogits) {
+          float* dst = static_cast<float*>(F.out) + out_off + c;
+          const int64_t col0 = bcol0 + c;
+          if (col0 + 32 <= F.n_valid && (F.ld_out & 3) == 0) {  // rows 16-byte aligned
+#pragma unroll
+            for (int i = 0; i < 8; ++i) reinterpret_cast<uint4*>(dst)[i] = Vec16<float>::pack(o + 4 * i);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (col0 + i < F.n_valid) dst[i] = o[i];
+          }
+        } else if (valid) {
           if (EPI == kLinear) {
             uint4* dst = reinterpret_cast<uint4*>(static_cast<float*>(F.out) + out_off + c);
 #pragma unroll
@@ -530,6 +622,37 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < 4; ++i) dst[i] = Vec16<__nv_bfloat16>::pack(o + 8 * i);
           }
         }
+      };
+      auto load_chunk = [&](uint32_t(&v)[32], uint32_t(&u)[32], int c) {
+        tmem_ld32(tbase + (uint32_t)c, v);
+        if (EPI == kSwiglu) tmem_ld32(tbase + (uint32_t)(BN / 2 + c), u);
+      };
+      auto wait_chunk = [&](uint32_t(&v)[32], uint32_t(&u)[32]) {
+        tmem_ld_wait(v);
+        if (EPI == kSwiglu) reg_fence(u);
+      };
+
+      // chunks c = half*32, half*32 + 64, ...: the next chunk's TMEM load is in
+      // flight while the current one is converted and stored
+      uint32_t va[32], ua[32], vb[32], ub[32];
+      int c = half * 32;
+      if (EPI == kSwiglu) {  // two TMEM halves per chunk: no room to double-buffer
+        for (; c < kOutCols; c += 64) {
+          load_chunk(va, ua, c);
+          wait_chunk(va, ua);
+          finish_chunk(va, ua, c);
+        }
+      }
+      if (c < kOutCols) load_chunk(va, ua, c);
+      for (; c < kOutCols; c += 128) {
+        wait_chunk(va, ua);
+        if (c + 64 < kOutCols) load_chunk(vb, ub, c + 64);
+        finish_chunk(va, ua, c);
+        if (c + 64 < kOutCols) {
+          wait_chunk(vb, ub);
+          if (c + 128 < kOutCols) load_chunk(va, ua, c + 128);
+          finish_chunk(vb, ub, c + 64);
+        }
       }
       tc_fence_before();
       __syncwarp();
@@ -539,6 +662,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         acc_phase ^= 1u;
       }
     }
+    if (lane == 0 && store_pending) bulk_wait0();
   }
   __syncwarp();
   tc_fence_before();
@@ -568,17 +692,28 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 2-D bf16 matrix [rows, cols] row-major, box = 64 columns x box_rows rows, 128-byte swizzle.
-bool make_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int box_rows) {
+// 2-D matrix [rows, cols] row-major, box = box_cols x box_rows.
+bool make_map_ex(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int box_cols, int box_rows,
+                 CUtensorMapDataType dt, int elem_bytes, CUtensorMapSwizzle swz) {
   EncodeTiledFn enc = encode_fn();
-  if (!enc || !ptr || rows < 1 || cols < 64) return false;
+  if (!enc || !ptr || rows < 1 || cols < box_cols) return false;
   cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-  cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * elem_bytes};
+  cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
   cuuint32_t es[2] = {1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return enc(m, dt, 2, const_cast<void*>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Operand tiles: bf16, 64 columns (one 128-byte swizzle atom) x box_rows rows.
+bool make_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int box_rows) {
+  return make_map_ex(m, ptr, rows, cols, BK, box_rows, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                     CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// Output blocks: bf16, 32 x 32, 64-byte swizzle (matches the epilogue staging layout).
+bool make_out_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols) {
+  return make_map_ex(m, ptr, rows, cols, 32, 32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
 int num_sms() {
@@ -589,19 +724,20 @@ int num_sms() {
 }
 
 template <int BN, int EPI>
-cudaError_t launch_t(const CUtensorMap (&maps)[6], const Params& P, int64_t max_tiles, cudaStream_t st) {
+cudaError_t launch_t(const CUtensorMap (&maps)[8], const Params& P, int64_t max_tiles, cudaStream_t st) {
   using C = Cfg<BN>;
   auto kern = grouped_gemm_kernel<BN, EPI>;
   static cudaError_t attr = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
   if (attr != cudaSuccess) return attr;
   const int64_t grid = max_tiles < num_sms() ? max_tiles : num_sms();
   if (grid <= 0) return cudaSuccess;
-  kern<<<(unsigned)grid, kThreads, C::kSmem, st>>>(maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], P);
+  kern<<<(unsigned)grid, kThreads, C::kSmem, st>>>(maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6],
+                                                    maps[7], P);
   return cudaGetLastError();
 }
 
 template <int EPI>
-cudaError_t launch_bn(int bn, const CUtensorMap (&maps)[6], const Params& P, int64_t max_tiles, cudaStream_t st) {
+cudaError_t launch_bn(int bn, const CUtensorMap (&maps)[8], const Params& P, int64_t max_tiles, cudaStream_t st) {
   switch (bn) {
     case 256: return launch_t<256, EPI>(maps, P, max_tiles, st);
     case 128: return launch_t<128, EPI>(maps, P, max_tiles, st);
@@ -623,6 +759,34 @@ int pick_bn(bool swiglu, int64_t c0, int64_t c1) {
 
 bool tc_gemm_available() { return tc::encode_fn() != nullptr; }
 
+// Router logits on the tensor cores: one group of N token rows against the E
+// router rows (zero-filled past E by the tensor map), fp32 output + logit bias.
+cudaError_t launch_router_logits_tc(const Plan& p, const void* x, const void* w_router, const float* logit_bias,
+                                    float* logits, int32_t* status, cudaStream_t st) {
+  using namespace tc;
+  const int bn = p.E <= 64 ? 64 : (p.E <= 128 ? 128 : 256);
+  CUtensorMap maps[8];
+  if (!make_map(&maps[0], x, p.N, p.d, BM)) return cudaErrorInvalidValue;
+  if (!make_map(&maps[1], w_router, p.E, p.d, bn)) return cudaErrorInvalidValue;
+  for (int i = 2; i < 8; ++i) maps[i] = maps[0];
+  Params P{};
+  Family& f0 = P.fam[0];
+  f0.groups = 1;
+  f0.m_fixed = (int32_t)p.N;
+  f0.n_tiles = (int32_t)ceil_div(p.E, bn);
+  f0.k_blocks = f0.kseg_blocks = (int32_t)(p.d / BK);
+  f0.a_map = 0;
+  f0.b_map = 1;
+  f0.b3_map = 1;
+  f0.out = logits;
+  f0.ld_out = p.E;
+  f0.bias_f32 = logit_bias;
+  f0.n_valid = p.E;
+  P.expert_off = nullptr;
+  P.status = status;
+  return launch_bn<kLogits>(bn, maps, P, ceil_div(p.N, BM) * f0.n_tiles, st);
+}
+
 // part: bit 0 = up-projections (routed + shared), bit 1 = down-projections.
 cudaError_t launch_ffn_bf16(const Plan& p, const void* xp, const int32_t* expert_off, const float* row_gate,
                             const void* x, const moe_weights* w, void* h, void* hs, void* yp, void* ys,
@@ -634,18 +798,22 @@ cudaError_t launch_ffn_bf16(const Plan& p, const void* xp, const int32_t* expert
     if (!bn) return cudaErrorInvalidValue;
     const int oc = p.swiglu ? bn / 2 : bn;
     const int brows = p.swiglu ? bn / 2 : bn;
-    CUtensorMap maps[6];
+    CUtensorMap maps[8];
     if (!make_map(&maps[0], xp, R, p.d, BM)) return cudaErrorInvalidValue;
-    for (int i = 1; i < 6; ++i) maps[i] = maps[0];  // unused slots hold a valid map
+    for (int i = 1; i < 8; ++i) maps[i] = maps[0];  // unused slots hold a valid map
     bool ok = make_map(&maps[2], w->w1, p.E * p.F, p.d, brows);
     if (p.swiglu) ok = ok && make_map(&maps[3], w->w3, p.E * p.F, p.d, brows);
     if (p.S > 0) {
       ok = ok && make_map(&maps[1], x, p.N, p.d, BM) && make_map(&maps[4], w->ws1, p.S * p.Fs, p.d, brows);
       if (p.swiglu) ok = ok && make_map(&maps[5], w->ws3, p.S * p.Fs, p.d, brows);
     }
+    ok = ok && make_out_map(&maps[6], h, R, p.F);
+    if (p.S > 0) ok = ok && make_out_map(&maps[7], hs, p.N, p.S * p.Fs);
     if (!ok) return cudaErrorInvalidValue;
     Params P{};
     Family& f0 = P.fam[0];
+    f0.tma_out = 1;
+    P.fam[1].tma_out = p.S > 0 ? 1 : 0;
     f0.groups = (int32_t)p.E;
     f0.m_from_off = 1;
     f0.n_tiles = (int32_t)(p.F / oc);
@@ -686,9 +854,9 @@ cudaError_t launch_ffn_bf16(const Plan& p, const void* xp, const int32_t* expert
   if (part & 2) {
     const int bn = pick_bn(false, p.d, 0);
     if (!bn) return cudaErrorInvalidValue;
-    CUtensorMap maps[6];
+    CUtensorMap maps[8];
     if (!make_map(&maps[0], h, R, p.F, BM)) return cudaErrorInvalidValue;
-    for (int i = 1; i < 6; ++i) maps[i] = maps[0];
+    for (int i = 1; i < 8; ++i) maps[i] = maps[0];
     bool ok = make_map(&maps[2], w->w2, p.E * p.d, p.F, bn);
     if (p.S > 0) ok = ok && make_map(&maps[1], hs, p.N, p.S * p.Fs, BM) && make_map(&maps[3], w->ws2, p.S * p.d, p.Fs, bn);
     if (!ok) return cudaErrorInvalidValue;

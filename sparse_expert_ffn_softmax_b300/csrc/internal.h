@@ -20,8 +20,6 @@ struct Plan {
   int64_t max_rows;  // rows reserved for xp / h / yp
   int64_t tiles;     // ceil(N / 32)
   int64_t words;     // ceil(E / 32): expert bitmap words per token (expert choice)
-  int router_tpw;    // tokens per router warp
-  int64_t router_blocks;
   moe_workspace_layout L;
   // scratch sub-buffers (byte offsets into the workspace)
   size_t part_p, part_cnt, part_lse;  // router partials
@@ -40,18 +38,32 @@ inline T* ws_at(void* ws, size_t off) {
   return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
 }
 
-// router.cu
+// router.cu. One router block per 32-token tile. tile_counts (nullable) receives
+// the per-tile expert counts [E][T] for the permute. finalize: reduce the
+// statistics in a separate kernel (stand-alone routing and expert choice);
+// otherwise a later kernel of the forward reduces the router's partials.
 cudaError_t launch_router(const Plan& p, const void* x, const moe_weights* w, int32_t* idx, float* gate,
-                          float* logits, float* probs, void* stats, void* ws, cudaStream_t st);
+                          float* logits, float* probs, void* stats, void* ws, cudaStream_t st,
+                          int32_t* tile_counts, bool finalize);
+bool router_uses_tc(const Plan& p);
 
-// permute.cu
+// permute.cu. Token choice needs per-tile expert counts and their prefix:
+//  kCountsFromIdx    count them from idx (stand-alone moe_permute);
+//  kCountsFromRouter the router wrote the counts; the scan kernel also
+//                    finalises the router statistics;
+//  kFusedOffsets     the router wrote the counts and every scatter block derives
+//                    its prefixes and the expert offsets itself (small E x T,
+//                    permute_fuses_offsets); the combine reduces the statistics.
+enum PermuteMode { kCountsFromIdx = 0, kCountsFromRouter = 1, kFusedOffsets = 2 };
+bool permute_fuses_offsets(const Plan& p);
 cudaError_t launch_ec_select(const Plan& p, const float* probs, int32_t* idx, float* gate, void* ws,
                              cudaStream_t st);
 cudaError_t launch_permute(const Plan& p, const void* x, const int32_t* idx, const float* gate, void* xp,
                            int32_t* tok_rows, int32_t* tok_off, int32_t* expert_off, int32_t* row_token,
-                           float* row_gate, void* stats, void* ws, cudaStream_t st);
+                           float* row_gate, void* stats, void* ws, cudaStream_t st, PermuteMode mode);
+// ws and stats non-null: block 0 also reduces the router statistics from ws.
 cudaError_t launch_combine(const Plan& p, const void* yp, const int32_t* tok_rows, const int32_t* tok_off,
-                           const void* ys, void* out, cudaStream_t st);
+                           const void* ys, void* out, cudaStream_t st, void* ws = nullptr, void* stats = nullptr);
 
 // ffn_simt.cu (fp32 layers)
 cudaError_t launch_ffn_f32(const Plan& p, const void* xp, const int32_t* expert_off, const float* row_gate,
@@ -63,5 +75,8 @@ cudaError_t launch_ffn_bf16(const Plan& p, const void* xp, const int32_t* expert
                             const void* x, const moe_weights* w, void* h, void* hs, void* yp, void* ys,
                             int32_t* status, cudaStream_t st, int part);
 bool tc_gemm_available();
+// logits[N, E] = x W_r^T + logit_bias on the tensor cores (bf16 layers).
+cudaError_t launch_router_logits_tc(const Plan& p, const void* x, const void* w_router, const float* logit_bias,
+                                    float* logits, int32_t* status, cudaStream_t st);
 
 }  // namespace moe

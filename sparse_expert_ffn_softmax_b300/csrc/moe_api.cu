@@ -69,10 +69,6 @@ moe_status make_plan(const moe_config* c, Plan* p) {
   if (p->max_rows >= (int64_t)1 << 31) return MOE_ERR_UNSUPPORTED;
   p->tiles = ceil_div(p->N, kTileTokens);
   p->words = ceil_div(p->E, 32);
-  int64_t tpw = ceil_div(p->N, (int64_t)kRouterWarps * 2 * 148);
-  p->router_tpw = (int)(tpw < 1 ? 1 : (tpw > 64 ? 64 : tpw));
-  p->router_blocks = ceil_div(p->N, (int64_t)kRouterWarps * p->router_tpw);
-  if (p->router_blocks < 1) p->router_blocks = 1;
 
   const size_t b = p->bf16 ? 2 : 4;
   const int64_t nsel = p->ec ? p->E * p->cap : p->N * p->k;
@@ -83,7 +79,7 @@ moe_status make_plan(const moe_config* c, Plan* p) {
     o += align_up(bytes > 0 ? bytes : 1);
     return at;
   };
-  L.status = take(16);
+  L.status = take(32);  // int32 error word [4] + last-block ticket
   L.logits = take((size_t)(p->N * p->E) * 4);
   L.probs = take((size_t)(p->N * p->E) * 4);
   L.idx = take((size_t)nsel * 4);
@@ -100,9 +96,9 @@ moe_status make_plan(const moe_config* c, Plan* p) {
   L.ys = take(p->S > 0 ? (size_t)p->N * (size_t)p->d * 4 : 0);
   L.stats = take(moe_stats_bytes(p->E));
   L.scratch = o;
-  p->part_p = take((size_t)(p->E * p->router_blocks) * 4);
-  p->part_cnt = take((size_t)(p->E * p->router_blocks) * 4);
-  p->part_lse = take((size_t)(2 * p->router_blocks) * 4);
+  p->part_p = take((size_t)(p->E * p->tiles) * 4);  // router partials, one block per tile
+  p->part_cnt = take((size_t)(p->E * p->tiles) * 4);
+  p->part_lse = take((size_t)(2 * p->tiles) * 4);
   p->tile_counts = take((size_t)(p->E * p->tiles) * 4);
   p->tile_base = take((size_t)(p->E * (p->tiles + 1)) * 4);
   p->ec_bits = take((size_t)(p->N * p->words) * 4);
@@ -140,11 +136,15 @@ moe_status check_weights(const Plan& p, const moe_weights* w, bool router, bool 
 
 void* stats_or_ws(const Plan& p, void* stats, void* ws) { return stats ? stats : ws_at<uint8_t>(ws, p.L.stats); }
 
+// tile_counts non-null (token choice inside moe_forward): the router also writes
+// the permute's per-tile counts and a later kernel reduces the statistics.
+// Otherwise (stand-alone routing, expert choice) the router finalises them.
 moe_status do_route(const Plan& p, const void* x, const moe_weights* w, int32_t* idx, float* gate, float* logits,
-                    float* probs, void* stats, void* ws, cudaStream_t st) {
+                    float* probs, void* stats, void* ws, cudaStream_t st, int32_t* tile_counts = nullptr) {
   float* pr = probs;
   if (p.ec && !pr) pr = ws_at<float>(ws, p.L.probs);
-  cudaError_t e = launch_router(p, x, w, idx, gate, logits, pr, stats_or_ws(p, stats, ws), ws, st);
+  cudaError_t e = launch_router(p, x, w, idx, gate, logits, pr, stats_or_ws(p, stats, ws), ws, st, tile_counts,
+                                tile_counts == nullptr);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   if (p.ec) {
     e = launch_ec_select(p, pr, idx, gate, ws, st);
@@ -215,7 +215,7 @@ moe_status moe_workspace_init(const moe_config* cfg, void* ws, size_t ws_bytes, 
   if (s != MOE_OK) return s;
   if ((s = check_ws(p, ws, ws_bytes)) != MOE_OK) return s;
   cudaGetLastError();
-  return cuda_status(cudaMemsetAsync(ws_at<uint8_t>(ws, p.L.status), 0, 16, (cudaStream_t)stream));
+  return cuda_status(cudaMemsetAsync(ws_at<uint8_t>(ws, p.L.status), 0, 32, (cudaStream_t)stream));
 }
 
 moe_status moe_route(const moe_config* cfg, const void* x, const moe_weights* w, int32_t* idx, float* gate,
@@ -250,7 +250,7 @@ moe_status moe_permute(const moe_config* cfg, const void* x, const int32_t* idx,
     return MOE_ERR_INVALID_ARG;
   cudaGetLastError();
   return cuda_status(launch_permute(p, x, idx, gate, xp, tok_rows, tok_off, expert_off, row_token, row_gate, stats,
-                                    ws, (cudaStream_t)stream));
+                                    ws, (cudaStream_t)stream, kCountsFromIdx));
 }
 
 moe_status moe_expert_ffn(const moe_config* cfg, const void* xp, const int32_t* expert_off, const float* row_gate,
@@ -315,19 +315,24 @@ moe_status moe_forward_traced(const moe_config* cfg, const void* x, const moe_we
   void* ys = p.S > 0 ? ws_at<uint8_t>(ws, L.ys) : nullptr;
   void* st_buf = stats_or_ws(p, stats, ws);
   if (!mark()) return MOE_ERR_CUDA;
+  int32_t* fused_counts = p.ec ? nullptr : ws_at<int32_t>(ws, p.tile_counts);
+  const bool fused_offsets = permute_fuses_offsets(p);
   if ((s = do_route(p, x, w, idx, gate, ws_at<float>(ws, L.logits), p.ec ? ws_at<float>(ws, L.probs) : nullptr,
-                    st_buf, ws, st)) != MOE_OK)
+                    st_buf, ws, st, fused_counts)) != MOE_OK)
     return s;
   if (!mark()) return MOE_ERR_CUDA;
-  if (launch_permute(p, x, idx, gate, xp, tok_rows, tok_off, expert_off, row_token, row_gate, st_buf, ws, st) !=
-      cudaSuccess)
+  const PermuteMode mode = p.ec ? kCountsFromIdx : (fused_offsets ? kFusedOffsets : kCountsFromRouter);
+  if (launch_permute(p, x, idx, gate, xp, tok_rows, tok_off, expert_off, row_token, row_gate, st_buf, ws, st,
+                     mode) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (!mark()) return MOE_ERR_CUDA;
   if ((s = do_ffn(p, xp, expert_off, row_gate, x, w, yp, ys, ws, st, 1)) != MOE_OK) return s;
   if (!mark()) return MOE_ERR_CUDA;
   if ((s = do_ffn(p, xp, expert_off, row_gate, x, w, yp, ys, ws, st, 2)) != MOE_OK) return s;
   if (!mark()) return MOE_ERR_CUDA;
-  if (launch_combine(p, yp, tok_rows, tok_off, ys, out, st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_combine(p, yp, tok_rows, tok_off, ys, out, st, fused_offsets ? ws : nullptr,
+                     fused_offsets ? st_buf : nullptr) != cudaSuccess)
+    return MOE_ERR_CUDA;
   if (!mark()) return MOE_ERR_CUDA;
   return MOE_OK;
 }
@@ -350,6 +355,7 @@ moe_status moe_get_device_status(const moe_config* cfg, void* ws, size_t ws_byte
     return MOE_ERR_CUDA;
   if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
   if (cudaMemsetAsync(ws_at<uint8_t>(ws, p.L.status), 0, sizeof word, st) != cudaSuccess) return MOE_ERR_CUDA;
+  // (the ticket after the error word is left alone: it is zero between calls)
   if (device_error) *device_error = word[0];
   if (word[0] & kErrTimeout) return MOE_ERR_TIMEOUT;
   if (word[0] & kErrIndex) return MOE_ERR_DEVICE_CHECK;

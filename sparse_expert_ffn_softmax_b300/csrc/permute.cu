@@ -29,6 +29,8 @@
 // order (a CSR: tok_off / tok_rows) for the copy and the combine.
 #include "common.cuh"
 #include "internal.h"
+#include "offsets.cuh"
+#include "stats.cuh"
 
 namespace moe {
 namespace {
@@ -60,123 +62,160 @@ __global__ void __launch_bounds__(kWarps * 32) count_kernel(const int32_t* __res
   for (int64_t e = lane; e < E; e += 32) tile_counts[e * T + tile] = h[e];
 }
 
-__global__ void __launch_bounds__(kWarps * 32) scan_kernel(const int32_t* __restrict__ tile_counts, int64_t E,
-                                                           int64_t T, int32_t* __restrict__ tile_base) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+struct RouterStatsArgs {
+  const float* part_p;
+  const int32_t* part_cnt;
+  const float* part_lse;
+  float alpha;
+};
+
+// Phase 1 (every block): one warp per expert, exclusive prefix of its tile
+// counts over the tiles -> tile_base[e][0..T-1], total in tile_base[e][T].
+// Phase 2 (the last block to finish, found with an atomic ticket; no block waits
+// for another): kept_e = min(count_e, C), expert_off = exclusive prefix of kept,
+// the dropping statistics and, when given the router partials, the router
+// statistics.
+__global__ void __launch_bounds__(kWarps * 32) scan_offsets_kernel(
+    const int32_t* __restrict__ tile_counts, int64_t E, int64_t T, int64_t cap, int64_t N, int64_t k,
+    int32_t* __restrict__ tile_base, int32_t* __restrict__ expert_off, void* stats, int32_t* ticket,
+    RouterStatsArgs rs) {
+  const int warp = threadIdx.x >> 5;
   const int64_t e = (int64_t)blockIdx.x * kWarps + warp;
-  if (e >= E) return;
-  const int32_t* src = tile_counts + e * T;
-  int32_t* dst = tile_base + e * (T + 1);
-  int carry = 0;
-  for (int64_t b = 0; b < T; b += 32) {
-    const int v = (b + lane < T) ? src[b + lane] : 0;
-    const int inc = warp_inclusive_scan(v);
-    if (b + lane < T) dst[b + lane] = carry + inc - v;
-    carry += __shfl_sync(kFull, inc, 31);
-  }
-  if (lane == 0) dst[T] = carry;
+  if (e < E) scan_expert_tiles(tile_counts + e * T, tile_base + e * (T + 1), T);
+  if (!last_block_ticket(ticket)) return;
+  offsets_from_totals(tile_base, E, T, cap, N, k, expert_off, stats);
+  if (stats && rs.part_p) finalize_router_stats(rs.part_p, rs.part_cnt, rs.part_lse, T, N, E, k, cap, 0, rs.alpha,
+                                                stats);
 }
 
-// Block-wide exclusive scan for blockDim.x <= 1024 (multiple of 32); returns the
-// exclusive prefix of v and writes the block total to *total.
-__device__ int block_exclusive_scan(int v, int* s_warp, int* total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  const int inc = warp_inclusive_scan(v);
-  if (lane == 31) s_warp[warp] = inc;
-  __syncthreads();
-  if (warp == 0) {
-    const int w = lane < nw ? s_warp[lane] : 0;
-    const int winc = warp_inclusive_scan(w);
-    if (lane < nw) s_warp[lane] = winc - w;
-    if (lane == 31) s_warp[32] = winc;
-  }
-  __syncthreads();
-  const int r = s_warp[warp] + inc - v;
-  *total = s_warp[32];
-  __syncthreads();
-  return r;
-}
-
-__global__ void __launch_bounds__(512) offsets_kernel(const int32_t* __restrict__ tile_base, int64_t E, int64_t T,
-                                                      int64_t cap, int64_t N, int64_t k,
-                                                      int32_t* __restrict__ expert_off, void* stats) {
-  __shared__ int s_warp[33];
-  const int e = threadIdx.x;
-  const int cnt = e < E ? tile_base[(int64_t)e * (T + 1) + T] : 0;
-  const int kept = (int)(cnt < cap ? cnt : cap);
-  int rows = 0, dropped_total = 0;
-  const int off = block_exclusive_scan(kept, s_warp, &rows);
-  block_exclusive_scan(cnt - kept, s_warp, &dropped_total);
-  if (e < E) expert_off[e] = off;
-  if (e == 0) expert_off[E] = rows;
-  if (stats) {
-    moe_stats_header* hdr = static_cast<moe_stats_header*>(stats);
-    int32_t* kept_out = reinterpret_cast<int32_t*>(reinterpret_cast<float*>(hdr + 1) + 2 * E) + E;
-    if (e < E) kept_out[e] = kept;
-    if (e == 0) {
-      hdr->dropped = dropped_total;
-      hdr->dropped_share = (float)((double)dropped_total / (double)(N * k));
-      hdr->capacity = (int32_t)cap;
-      hdr->rows = rows;
-      hdr->n_experts = (int32_t)E;
-    }
-  }
-}
-
-template <typename DT>
+// One block per tile of 32 tokens. Warp 0 ranks the tile's (token, choice)
+// pairs: the in-tile rank among the tile's tokens that chose the same expert is
+// the popcount of the lower lanes in a per-expert lane mask, so rank =
+// (assignments to e in earlier tiles) + in-tile rank is the exact token-order
+// rank. Kept pairs get row = expert_off[e] + rank. Then all 8 warps copy the
+// tile's token rows of x into xp with 16-byte vectors (each x row read once,
+// written once per kept choice).
+// kFused: the block itself derives what it needs from the router's per-tile
+// counts [E][T] -- the count of each expert in earlier tiles, the totals, and
+// expert_off (every block computes the same integers; block 0 also writes
+// expert_off and the dropping statistics) -- so no scan kernel runs before it.
+// Otherwise tile_base [E][T+1] and expert_off come from scan_offsets_kernel.
+template <typename DT, bool kFused>
 __global__ void __launch_bounds__(kWarps * 32) scatter_kernel(
     const DT* __restrict__ x, const int32_t* __restrict__ idx, const float* __restrict__ gate,
-    const int32_t* __restrict__ tile_base, const int32_t* __restrict__ expert_off, int64_t N, int64_t d, int64_t k,
+    const int32_t* __restrict__ counts_or_base, int32_t* __restrict__ expert_off, int64_t N, int64_t d, int64_t k,
     int64_t E, int64_t T, int64_t cap, DT* __restrict__ xp, int32_t* __restrict__ tok_rows,
-    int32_t* __restrict__ row_token, float* __restrict__ row_gate, int32_t* status) {
-  extern __shared__ uint32_t s_mask[];
+    int32_t* __restrict__ row_token, float* __restrict__ row_gate, void* stats, int32_t* status) {
+  extern __shared__ uint32_t s_dyn[];
+  uint32_t* msk = s_dyn;                                       // [E]
+  int32_t* s_rows = reinterpret_cast<int32_t*>(s_dyn + E);     // [32][k]
+  int32_t* s_pre = s_rows + kTileTokens * k;                   // [E]   (kFused)
+  int32_t* s_off = s_pre + E;                                  // [E+1] (kFused)
+  __shared__ int s_warp[33];
   using VT = Vec16<DT>;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int64_t tile = (int64_t)blockIdx.x * kWarps + warp;
-  if (tile >= T) return;
-  uint32_t* msk = s_mask + warp * E;
-  const int64_t t = tile * kTileTokens + lane;
-  const bool valid = t < N;
-  const uint32_t lt = (1u << lane) - 1u;
-  if (valid)
-    for (int64_t j = 0; j < k; ++j) {
-      const int32_t e = idx[t * k + j];
-      if (e >= 0 && e < E) msk[e] = 0u;
-    }
-  __syncwarp();
-  if (valid)
-    for (int64_t j = 0; j < k; ++j) {
-      const int32_t e = idx[t * k + j];
-      if (e >= 0 && e < E) {
-        const uint32_t old = atomicOr(&msk[e], 1u << lane);
-        if (old & (1u << lane)) record_error(status, kErrIndex, 104, (int32_t)t, e);  // expert listed twice
+  const int64_t tile = blockIdx.x;
+  if (kFused) {
+    for (int64_t e = warp; e < E; e += kWarps) {
+      const int32_t* cnt = counts_or_base + e * T;
+      int pre = 0, tot = 0;
+#pragma unroll 4
+      for (int64_t t = lane; t < T; t += 32) {
+        const int c = cnt[t];
+        tot += c;
+        pre += t < tile ? c : 0;
+      }
+      pre = warp_sum_int(pre);
+      tot = warp_sum_int(tot);
+      if (lane == 0) {
+        s_pre[e] = pre;
+        s_off[e] = tot;  // totals for now, offsets below
       }
     }
-  __syncwarp();
-  if (valid)
-    for (int64_t j = 0; j < k; ++j) {
-      const int32_t e = idx[t * k + j];
-      int32_t row = -1;
-      if (e >= 0 && e < E) {
-        const int64_t r = (int64_t)tile_base[(int64_t)e * (T + 1) + tile] + __popc(msk[e] & lt);
-        if (r < cap) {
-          row = expert_off[e] + (int32_t)r;
-          row_token[row] = (int32_t)t;
-          row_gate[row] = gate[t * k + j];
+    __syncthreads();
+    const int per = (int)ceil_div(E, (int64_t)blockDim.x);  // <= 2
+    const int64_t e0 = (int64_t)threadIdx.x * per;
+    int kept[2] = {0, 0}, ksum = 0, dsum = 0;
+    for (int i = 0; i < per && i < 2; ++i)
+      if (e0 + i < E) {
+        const int tot = s_off[e0 + i];
+        kept[i] = (int)(tot < cap ? tot : cap);
+        ksum += kept[i];
+        dsum += tot - kept[i];
+      }
+    int rows = 0, dropped = 0;
+    int off = block_exclusive_scan(ksum, s_warp, &rows);  // (syncs: all totals read before overwritten)
+    if (blockIdx.x == 0) block_exclusive_scan(dsum, s_warp, &dropped);
+    for (int i = 0; i < per && i < 2; ++i)
+      if (e0 + i < E) {
+        s_off[e0 + i] = off;
+        if (blockIdx.x == 0) expert_off[e0 + i] = off;
+        off += kept[i];
+      }
+    if (threadIdx.x == 0) {
+      s_off[E] = rows;
+      if (blockIdx.x == 0) expert_off[E] = rows;
+    }
+    if (blockIdx.x == 0 && stats) {
+      moe_stats_header* hdr = static_cast<moe_stats_header*>(stats);
+      int32_t* kept_out = reinterpret_cast<int32_t*>(reinterpret_cast<float*>(hdr + 1) + 2 * E) + E;
+      for (int i = 0; i < per && i < 2; ++i)
+        if (e0 + i < E) kept_out[e0 + i] = kept[i];
+      if (threadIdx.x == 0) {
+        hdr->dropped = dropped;
+        hdr->dropped_share = (float)((double)dropped / (double)(N * k));
+        hdr->capacity = (int32_t)cap;
+        hdr->rows = rows;
+        hdr->n_experts = (int32_t)E;
+      }
+    }
+    __syncthreads();
+  }
+  if (warp == 0) {
+    const int64_t t = tile * kTileTokens + lane;
+    const bool valid = t < N;
+    const uint32_t lt = (1u << lane) - 1u;
+    if (valid)
+      for (int64_t j = 0; j < k; ++j) {
+        const int32_t e = idx[t * k + j];
+        if (e >= 0 && e < E) msk[e] = 0u;
+      }
+    __syncwarp();
+    if (valid)
+      for (int64_t j = 0; j < k; ++j) {
+        const int32_t e = idx[t * k + j];
+        if (e >= 0 && e < E) {
+          const uint32_t old = atomicOr(&msk[e], 1u << lane);
+          if (old & (1u << lane)) record_error(status, kErrIndex, 104, (int32_t)t, e);  // expert listed twice
         }
-      } else {
-        record_error(status, kErrIndex, 102, (int32_t)t, e);
       }
-      tok_rows[t * k + j] = row;
+    __syncwarp();
+    for (int64_t j = 0; j < k; ++j) {
+      int32_t row = -1;
+      if (valid) {
+        const int32_t e = idx[t * k + j];
+        if (e >= 0 && e < E) {
+          const int64_t before = kFused ? s_pre[e] : counts_or_base[(int64_t)e * (T + 1) + tile];
+          const int64_t r = before + __popc(msk[e] & lt);
+          if (r < cap) {
+            row = (kFused ? s_off[e] : expert_off[e]) + (int32_t)r;
+            row_token[row] = (int32_t)t;
+            row_gate[row] = gate[t * k + j];
+          }
+        } else {
+          record_error(status, kErrIndex, 102, (int32_t)t, e);
+        }
+        tok_rows[t * k + j] = row;
+      }
+      s_rows[lane * k + j] = row;
     }
-  __syncwarp();
-  // copy the tile's tokens into their rows: x read once, written per kept choice.
-  // Every lane runs every chunk iteration so the row shuffles see the full warp.
+  }
+  __syncthreads();
   const int64_t nchunk = d / VT::n;
-  for (int tt = 0; tt < kTileTokens; ++tt) {
+  for (int tt = warp; tt < kTileTokens; tt += kWarps) {
     const int64_t tok = tile * kTileTokens + tt;
     if (tok >= N) break;
-    const int32_t my_row = lane < k ? tok_rows[tok * k + lane] : -1;
+    const int32_t my_row = lane < k ? s_rows[tt * k + lane] : -1;
     const uint4* src = reinterpret_cast<const uint4*>(x) + tok * nchunk;
     for (int64_t c0 = 0; c0 < nchunk; c0 += 32) {
       const int64_t c = c0 + lane;
@@ -351,7 +390,12 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(const float* __res
                                                               const int32_t* __restrict__ tok_rows,
                                                               const int32_t* __restrict__ tok_off,
                                                               const float* __restrict__ ys, int64_t N, int64_t d,
-                                                              int64_t k, TO* __restrict__ out) {
+                                                              int64_t k, TO* __restrict__ out, RouterStatsArgs fin,
+                                                              int64_t E, int64_t cap, void* stats) {
+  // Block 0 also reduces the router statistics when asked: nothing waits on them.
+  if (fin.part_p && blockIdx.x == 0)
+    finalize_router_stats(fin.part_p, fin.part_cnt, fin.part_lse, ceil_div(N, (int64_t)kTileTokens), N, E, k, cap,
+                          0, fin.alpha, stats);
   using VO = Vec16<TO>;
   constexpr int VN = VO::n;  // outputs per lane chunk: 8 (bf16) or 4 (fp32)
   constexpr int NV = VN / 4; // float4 loads per row and chunk
@@ -399,7 +443,7 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(const float* __res
 template <typename T>
 cudaError_t launch_permute_t(const Plan& p, const void* x, const int32_t* idx, const float* gate, void* xp,
                              int32_t* tok_rows, int32_t* tok_off, int32_t* expert_off, int32_t* row_token,
-                             float* row_gate, void* stats, void* ws, cudaStream_t st) {
+                             float* row_gate, void* stats, void* ws, cudaStream_t st, PermuteMode mode) {
   int32_t* status = status_ptr(p, ws);
   if (p.ec) {
     uint32_t* bits = ws_at<uint32_t>(ws, p.ec_bits);
@@ -419,14 +463,31 @@ cudaError_t launch_permute_t(const Plan& p, const void* x, const int32_t* idx, c
   }
   int32_t* tile_counts = ws_at<int32_t>(ws, p.tile_counts);
   int32_t* tile_base = ws_at<int32_t>(ws, p.tile_base);
-  const unsigned tb = (unsigned)ceil_div(p.tiles, kWarps);
-  const size_t hist_smem = (size_t)kWarps * p.E * 4;
-  count_kernel<<<tb, kWarps * 32, hist_smem, st>>>(idx, p.N, p.k, p.E, p.tiles, tile_counts, status);
-  scan_kernel<<<(unsigned)ceil_div(p.E, kWarps), kWarps * 32, 0, st>>>(tile_counts, p.E, p.tiles, tile_base);
-  offsets_kernel<<<1, 512, 0, st>>>(tile_base, p.E, p.tiles, p.cap, p.N, p.k, expert_off, stats);
-  scatter_kernel<T><<<tb, kWarps * 32, hist_smem, st>>>(static_cast<const T*>(x), idx, gate, tile_base, expert_off,
-                                                        p.N, p.d, p.k, p.E, p.tiles, p.cap, static_cast<T*>(xp),
-                                                        tok_rows, row_token, row_gate, status);
+  if (mode == kFusedOffsets) {
+    const size_t sc_smem = (size_t)p.E * 4 + (size_t)kTileTokens * p.k * 4 + (size_t)(2 * p.E + 1) * 4;
+    scatter_kernel<T, true><<<(unsigned)p.tiles, kWarps * 32, sc_smem, st>>>(
+        static_cast<const T*>(x), idx, gate, tile_counts, expert_off, p.N, p.d, p.k, p.E, p.tiles, p.cap,
+        static_cast<T*>(xp), tok_rows, row_token, row_gate, stats, status);
+    return cudaGetLastError();
+  }
+  if (mode == kCountsFromIdx) {
+    const size_t hist_smem = (size_t)kWarps * p.E * 4;
+    count_kernel<<<(unsigned)ceil_div(p.tiles, kWarps), kWarps * 32, hist_smem, st>>>(idx, p.N, p.k, p.E, p.tiles,
+                                                                                    tile_counts, status);
+  }
+  RouterStatsArgs rs{};
+  if (mode == kCountsFromRouter) {
+    rs.part_p = ws_at<float>(ws, p.part_p);
+    rs.part_cnt = ws_at<int32_t>(ws, p.part_cnt);
+    rs.part_lse = ws_at<float>(ws, p.part_lse);
+    rs.alpha = p.cfg.aux_alpha;
+  }
+  scan_offsets_kernel<<<(unsigned)ceil_div(p.E, kWarps), kWarps * 32, 0, st>>>(
+      tile_counts, p.E, p.tiles, p.cap, p.N, p.k, tile_base, expert_off, stats, status + 5, rs);
+  const size_t sc_smem = (size_t)p.E * 4 + (size_t)kTileTokens * p.k * 4;
+  scatter_kernel<T, false><<<(unsigned)p.tiles, kWarps * 32, sc_smem, st>>>(
+      static_cast<const T*>(x), idx, gate, tile_base, expert_off, p.N, p.d, p.k, p.E, p.tiles, p.cap,
+      static_cast<T*>(xp), tok_rows, row_token, row_gate, stats, status);
   return cudaGetLastError();
 }
 
@@ -441,26 +502,34 @@ cudaError_t launch_ec_select(const Plan& p, const float* probs, int32_t* idx, fl
 
 cudaError_t launch_permute(const Plan& p, const void* x, const int32_t* idx, const float* gate, void* xp,
                            int32_t* tok_rows, int32_t* tok_off, int32_t* expert_off, int32_t* row_token,
-                           float* row_gate, void* stats, void* ws, cudaStream_t st) {
+                           float* row_gate, void* stats, void* ws, cudaStream_t st, PermuteMode mode) {
   if (p.bf16)
     return launch_permute_t<__nv_bfloat16>(p, x, idx, gate, xp, tok_rows, tok_off, expert_off, row_token, row_gate,
-                                           stats, ws, st);
+                                           stats, ws, st, mode);
   return launch_permute_t<float>(p, x, idx, gate, xp, tok_rows, tok_off, expert_off, row_token, row_gate, stats, ws,
-                                 st);
+                                 st, mode);
 }
 
+bool permute_fuses_offsets(const Plan& p) { return !p.ec && p.E * p.tiles <= 8192; }
+
 cudaError_t launch_combine(const Plan& p, const void* yp, const int32_t* tok_rows, const int32_t* tok_off,
-                           const void* ys, void* out, cudaStream_t st) {
+                           const void* ys, void* out, cudaStream_t st, void* ws, void* stats) {
   const int64_t blocks = ceil_div(p.N, kWarps) < 148 * 16 ? ceil_div(p.N, kWarps) : 148 * 16;
+  RouterStatsArgs fin{};
+  if (ws && stats) {
+    fin.part_p = ws_at<float>(ws, p.part_p);
+    fin.part_cnt = ws_at<int32_t>(ws, p.part_cnt);
+    fin.part_lse = ws_at<float>(ws, p.part_lse);
+    fin.alpha = p.cfg.aux_alpha;
+  }
   if (p.bf16) {
     combine_kernel<__nv_bfloat16><<<(unsigned)blocks, kWarps * 32, 0, st>>>(
         static_cast<const float*>(yp), tok_rows, p.ec ? tok_off : nullptr, static_cast<const float*>(ys), p.N, p.d,
-        p.k, static_cast<__nv_bfloat16*>(out));
+        p.k, static_cast<__nv_bfloat16*>(out), fin, p.E, p.cap, stats);
   } else {
-    combine_kernel<float><<<(unsigned)blocks, kWarps * 32, 0, st>>>(static_cast<const float*>(yp), tok_rows,
-                                                                    p.ec ? tok_off : nullptr,
-                                                                    static_cast<const float*>(ys), p.N, p.d, p.k,
-                                                                    static_cast<float*>(out));
+    combine_kernel<float><<<(unsigned)blocks, kWarps * 32, 0, st>>>(
+        static_cast<const float*>(yp), tok_rows, p.ec ? tok_off : nullptr, static_cast<const float*>(ys), p.N, p.d,
+        p.k, static_cast<float*>(out), fin, p.E, p.cap, stats);
   }
   return cudaGetLastError();
 }

@@ -1,7 +1,6 @@
 // Router: logits = x W_r^T (+ per-expert offset), softmax over experts with its
 // log-normaliser, top-k (largest logit first, equal logits to the lower expert
-// id), the gate rule, and per-block partial sums for the balancing statistics;
-// then a one-block finaliser for f, P, aux loss and z-loss.
+// id), the gate rule, and per-block partial sums for the balancing statistics.
 //
 // Pages: "Mixture of Experts (MoE)" (learn.starphix.com) "Key Equations"
 // (router_logits = x @ W_router^T, top-k, weighted combination) and "Load
@@ -11,22 +10,23 @@
 // "MoE Architecture" (vanos001.github.io) TokenChoiceRouter (top-k on logits,
 // softmax over the k).
 //
-// One warp per token: the lanes split d into 16-byte vectors and keep one
-// partial dot product per expert of the current group of V experts; a
-// transpose-reduce (V/2 + ... + 1 shuffles, then a butterfly over the rest)
-// leaves lane l with the logit of expert (l mod V). The token's E logits then
-// sit in shared memory for the softmax and top-k. Block b owns a fixed range
-// of tokens and writes its partial sums in a fixed order, so the statistics
-// are deterministic.
+// One block = one tile of 32 consecutive tokens, one warp per token (8 warps,
+// 4 tokens each). Lane l keeps the logits of experts l, l+32, ... in registers.
+// For E <= 32 the lanes split d into 16-byte vectors and keep one partial dot
+// product per expert of a group of V experts; a transpose-reduce (V/2 + ... + 1
+// shuffles, then a butterfly over the rest) leaves lane l with the logit of
+// expert (l mod V). For more experts (bf16) the logits come from the
+// tensor-core GEMM (gemm_tc.cu). Each block writes its partial sums in a fixed
+// order, so the statistics are deterministic; they are reduced later (by the
+// permute's scan kernel, the combine kernel, or router_finalize_kernel).
 #include <cfloat>
 
 #include "common.cuh"
 #include "internal.h"
+#include "stats.cuh"
 
 namespace moe {
 namespace {
-
-constexpr int kEplMax = 16;  // experts per lane in the softmax / top-k stage: E <= 512
 
 template <int V>
 __device__ __forceinline__ void transpose_reduce(float (&a)[V], int lane) {
@@ -48,6 +48,7 @@ struct RouterArgs {
   const void* x;
   const void* wr;
   const float* logit_bias;
+  const float* logits_in;  // non-null: logits already computed (bias included), fp32 [N, E]
   int32_t* idx;
   float* gate;
   float* logits;  // nullable
@@ -55,14 +56,16 @@ struct RouterArgs {
   float* part_p;      // [E][blocks]
   int32_t* part_cnt;  // [E][blocks]
   float* part_lse;    // [blocks][2]
+  int32_t* tile_counts;  // [E][blocks] per-tile assignment counts for the permute, or null
   int32_t* status;
-  int64_t N, d, E, k;
+  int64_t N, d, E, k, cap;
   int gating;
-  int tpw;
+  float alpha;
 };
 
-// Dynamic shared memory: [W_r copy (if kWSmem)] [sL: warps x E floats] [sP: warps x E floats] [cnt: E ints]
-template <typename T, int V, bool kWSmem>
+// Dynamic shared memory: [W_r copy (kWSmem)] [sP: 8 warps x E] [cnt: E].
+// EPL = experts per lane (ceil(E / 32)); V = experts per dot-product group.
+template <typename T, int V, int CPL, int EPL, bool kWSmem, bool kLogitsIn>
 __global__ void __launch_bounds__(kRouterWarps * 32) router_kernel(RouterArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
   using VT = Vec16<T>;
@@ -71,75 +74,132 @@ __global__ void __launch_bounds__(kRouterWarps * 32) router_kernel(RouterArgs a)
   const int64_t E = a.E, d = a.d, k = a.k;
   const int64_t nchunk = d / VN;
   const uint4* wsrc = static_cast<const uint4*>(a.wr);
+  float* wsm = reinterpret_cast<float*>(smem);  // kWSmem: W_r widened to fp32, [E][d]
   uint8_t* cur = smem;
   if (kWSmem) {
-    uint4* wdst = reinterpret_cast<uint4*>(smem);
-    for (int64_t i = threadIdx.x; i < E * nchunk; i += blockDim.x) wdst[i] = wsrc[i];
-    wsrc = wdst;
-    cur += E * nchunk * 16;
+    // stage W_r as fp32 with 8 loads in flight per thread
+    const int64_t n = E * nchunk;
+    for (int64_t i0 = threadIdx.x; i0 < n; i0 += (int64_t)blockDim.x * 8) {
+      uint4 tmp[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int64_t i = i0 + (int64_t)u * blockDim.x;
+        if (i < n) tmp[u] = __ldg(wsrc + i);
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int64_t i = i0 + (int64_t)u * blockDim.x;
+        if (i < n) {
+          float f[VN];
+          VT::unpack(tmp[u], f);
+          float4* dst = reinterpret_cast<float4*>(wsm + i * VN);
+#pragma unroll
+          for (int q = 0; q < VN / 4; ++q) dst[q] = make_float4(f[4 * q], f[4 * q + 1], f[4 * q + 2], f[4 * q + 3]);
+        }
+      }
+    }
+    cur += E * d * 4;
   }
-  float* sL = reinterpret_cast<float*>(cur) + warp * E;
-  float* sPall = reinterpret_cast<float*>(cur) + kRouterWarps * E;
+  float* sPall = reinterpret_cast<float*>(cur);
   int32_t* sCnt = reinterpret_cast<int32_t*>(sPall + kRouterWarps * E);
   for (int64_t e = threadIdx.x; e < E; e += blockDim.x) sCnt[e] = 0;
   __syncthreads();
 
-  float pacc[kEplMax];
+  float pacc[EPL];
 #pragma unroll
-  for (int i = 0; i < kEplMax; ++i) pacc[i] = 0.f;
+  for (int i = 0; i < EPL; ++i) pacc[i] = 0.f;
   float lse_sum = 0.f, lse_sq = 0.f;
   const bool ec = a.gating == MOE_GATE_EXPERT_CHOICE;
 
-  const int64_t tok0 = (int64_t)blockIdx.x * kRouterWarps * a.tpw + (int64_t)warp * a.tpw;
-  for (int it = 0; it < a.tpw; ++it) {
-    const int64_t t = tok0 + it;
+  for (int it = 0; it < kTileTokens / kRouterWarps; ++it) {
+    const int64_t t = (int64_t)blockIdx.x * kTileTokens + it * kRouterWarps + warp;
     if (t >= a.N) break;
-    // ---- logits of token t into sL ----
-    const uint4* xrow = static_cast<const uint4*>(a.x) + t * nchunk;
-    for (int64_t eb = 0; eb < E; eb += V) {
-      float acc[V];
+    // ---- logits of token t: lane l holds expert l + 32 i in Lr[i] ----
+    float Lr[EPL];
+    if (kLogitsIn) {
 #pragma unroll
-      for (int v = 0; v < V; ++v) acc[v] = 0.f;
-      for (int64_t c = lane; c < nchunk; c += 32) {
-        float xv[VN];
-        VT::unpack(__ldg(xrow + c), xv);
+      for (int i = 0; i < EPL; ++i) {
+        const int64_t e = lane + 32 * i;
+        Lr[i] = e < E ? a.logits_in[t * E + e] : -FLT_MAX;
+      }
+    } else {
+      const uint4* xrow = static_cast<const uint4*>(a.x) + t * nchunk;
 #pragma unroll
-        for (int v = 0; v < V; ++v) {
-          if (eb + v < E) {
-            float wv[VN];
-            uint4 wu = kWSmem ? wsrc[(eb + v) * nchunk + c] : __ldg(wsrc + (eb + v) * nchunk + c);
-            VT::unpack(wu, wv);
+      for (int gi = 0; gi < EPL; ++gi) {
+        // experts eb .. eb+V-1 (V = 32 whenever EPL > 1)
+        const int64_t eb = (int64_t)gi * 32;
+        float acc[V];
 #pragma unroll
-            for (int i = 0; i < VN; ++i) acc[v] = fmaf(xv[i], wv[i], acc[v]);
+        for (int v = 0; v < V; ++v) acc[v] = 0.f;
+        for (int64_t cb = 0; cb < nchunk; cb += CPL * 32) {
+          uint4 xr[CPL];
+#pragma unroll
+          for (int i = 0; i < CPL; ++i) {
+            const int64_t c = cb + lane + 32 * i;
+            xr[i] = c < nchunk ? __ldg(xrow + c) : make_uint4(0, 0, 0, 0);
+          }
+#pragma unroll
+          for (int i = 0; i < CPL; ++i) {
+            const int64_t c = cb + lane + 32 * i;
+            if (c < nchunk) {
+              float xv[VN];
+              VT::unpack(xr[i], xv);
+#pragma unroll
+              for (int v = 0; v < V; ++v) {
+                if (eb + v < E) {
+                  float wv[VN];
+                  if (kWSmem) {
+                    const float4* wp = reinterpret_cast<const float4*>(wsm + ((eb + v) * nchunk + c) * VN);
+#pragma unroll
+                    for (int q = 0; q < VN / 4; ++q) {
+                      const float4 w4 = wp[q];
+                      wv[4 * q] = w4.x;
+                      wv[4 * q + 1] = w4.y;
+                      wv[4 * q + 2] = w4.z;
+                      wv[4 * q + 3] = w4.w;
+                    }
+                  } else {
+                    VT::unpack(__ldg(wsrc + (eb + v) * nchunk + c), wv);
+                  }
+#pragma unroll
+                  for (int q = 0; q < VN; ++q) acc[v] = fmaf(xv[q], wv[q], acc[v]);
+                }
+              }
+            }
           }
         }
+        transpose_reduce<V>(acc, lane);  // lane l: expert eb + (l mod V)
+        const int64_t e = eb + lane;
+        Lr[gi] = (lane < V && e < E) ? acc[0] + (a.logit_bias ? a.logit_bias[e] : 0.f) : -FLT_MAX;
       }
-      transpose_reduce<V>(acc, lane);
-      const int64_t e = eb + lane;
-      if (lane < V && e < E) sL[e] = acc[0] + (a.logit_bias ? a.logit_bias[e] : 0.f);
     }
-    __syncwarp();
     // ---- softmax over experts, log-normaliser ----
     float m = -FLT_MAX;
-    for (int64_t e = lane; e < E; e += 32) m = fmaxf(m, sL[e]);
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) m = fmaxf(m, Lr[i]);
     m = warp_max(m);
+    float ex[EPL];
     float s = 0.f;
-    for (int64_t e = lane; e < E; e += 32) s += expf(sL[e] - m);
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+      ex[i] = lane + 32 * i < E ? __expf(Lr[i] - m) : 0.f;
+      s += ex[i];
+    }
     s = warp_sum(s);
-    const float lse = m + logf(s);
+    const float lse = m + __logf(s);
+    const float inv_s = __fdividef(1.f, s);
     if (lane == 0) {
       lse_sum += lse;
       lse_sq += lse * lse;
     }
 #pragma unroll
-    for (int i = 0; i < kEplMax; ++i) {
+    for (int i = 0; i < EPL; ++i) {
       const int64_t e = lane + 32 * i;
       if (e < E) {
-        const float L = sL[e];
-        const float pe = expf(L - m) / s;
+        const float pe = ex[i] * inv_s;
         pacc[i] += pe;
         if (a.probs) a.probs[t * E + e] = pe;
-        if (a.logits) a.logits[t * E + e] = L;
+        if (a.logits && !kLogitsIn) a.logits[t * E + e] = Lr[i];
       }
     }
     if (!ec) {
@@ -151,14 +211,11 @@ __global__ void __launch_bounds__(kRouterWarps * 32) router_kernel(RouterArgs a)
         float bv = -FLT_MAX;
         int be = 0x7fffffff;
 #pragma unroll
-        for (int i = 0; i < kEplMax; ++i) {
+        for (int i = 0; i < EPL; ++i) {
           const int e = lane + 32 * i;
-          if (e < E && !((taken >> i) & 1u)) {
-            const float v = sL[e];
-            if (v > bv || (v == bv && e < be)) {
-              bv = v;
-              be = e;
-            }
+          if (e < E && !((taken >> i) & 1u) && (Lr[i] > bv || (Lr[i] == bv && e < be))) {
+            bv = Lr[i];
+            be = e;
           }
         }
 #pragma unroll
@@ -181,14 +238,14 @@ __global__ void __launch_bounds__(kRouterWarps * 32) router_kernel(RouterArgs a)
       const bool mine = lane < k;
       if (a.gating == MOE_GATE_TOPK_SOFTMAX) {
         const float l0 = __shfl_sync(kFull, my_l, 0);
-        const float num = mine ? expf(my_l - l0) : 0.f;
+        const float num = mine ? __expf(my_l - l0) : 0.f;
         const float den = warp_sum(num);
-        g = num / den;
+        g = __fdividef(num, den);
       } else {
-        const float pj = mine ? expf(my_l - m) / s : 0.f;
+        const float pj = mine ? __expf(my_l - m) * inv_s : 0.f;
         if (a.gating == MOE_GATE_SOFTMAX_TOPK_RENORM) {
           const float den = warp_sum(pj);
-          g = pj / den;
+          g = __fdividef(pj, den);
         } else {
           g = pj;
         }
@@ -199,12 +256,11 @@ __global__ void __launch_bounds__(kRouterWarps * 32) router_kernel(RouterArgs a)
         atomicAdd(&sCnt[my_e], 1);
       }
     }
-    __syncwarp();
   }
   // ---- block partials in a fixed order ----
   float* sP = sPall + warp * E;
 #pragma unroll
-  for (int i = 0; i < kEplMax; ++i) {
+  for (int i = 0; i < EPL; ++i) {
     const int64_t e = lane + 32 * i;
     if (e < E) sP[e] = pacc[i];
   }
@@ -219,6 +275,7 @@ __global__ void __launch_bounds__(kRouterWarps * 32) router_kernel(RouterArgs a)
     for (int w = 0; w < kRouterWarps; ++w) acc += sPall[w * E + e];
     a.part_p[e * gridDim.x + blockIdx.x] = acc;
     a.part_cnt[e * gridDim.x + blockIdx.x] = sCnt[e];
+    if (a.tile_counts) a.tile_counts[e * gridDim.x + blockIdx.x] = sCnt[e];
   }
   if (threadIdx.x == 0) {
     float s0 = 0.f, s1 = 0.f;
@@ -231,97 +288,78 @@ __global__ void __launch_bounds__(kRouterWarps * 32) router_kernel(RouterArgs a)
   }
 }
 
-// Statistics from the block partials, summed in a fixed order in fp64.
-// f_e = count_e / total assignments (token choice: before dropping; expert
-// choice: C per expert), P_e = mean_t p[t,e], aux = alpha * E * sum f P,
-// z = (mean lse)^2, mean_lse_sq = mean lse^2. Partials are laid out [E][blocks];
-// warp w reduces experts w, w+16, ... with its lanes striding over the blocks.
+}  // namespace
+
 __global__ void __launch_bounds__(512) router_finalize_kernel(const float* part_p, const int32_t* part_cnt,
                                                               const float* part_lse, int64_t blocks, int64_t N,
                                                               int64_t E, int64_t k, int64_t cap, int ec,
                                                               float alpha, void* stats) {
-  __shared__ double red[3][512];
-  moe_stats_header* hdr = static_cast<moe_stats_header*>(stats);
-  float* f_out = reinterpret_cast<float*>(hdr + 1);
-  float* P_out = f_out + E;
-  int32_t* cnt_out = reinterpret_cast<int32_t*>(P_out + E);
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
-  const double total = ec ? (double)E * (double)cap : (double)N * (double)k;
-  double aux_part = 0.0;
-  for (int64_t e = warp; e < E; e += nwarps) {
-    double P = 0.0;
-    long long cnt = 0;
-    for (int64_t b = lane; b < blocks; b += 32) {
-      P += part_p[e * blocks + b];
-      cnt += part_cnt[e * blocks + b];
-    }
-#pragma unroll
-    for (int s = 16; s >= 1; s >>= 1) {
-      P += __shfl_xor_sync(kFull, P, s);
-      cnt += __shfl_xor_sync(kFull, cnt, s);
-    }
-    if (ec) cnt = cap;
-    P /= (double)N;
-    const double f = total > 0 ? (double)cnt / total : 0.0;
-    if (lane == 0) {
-      f_out[e] = (float)f;
-      P_out[e] = (float)P;
-      cnt_out[e] = (int32_t)cnt;
-      aux_part += f * P;
-    }
-  }
-  double l0 = 0.0, l1 = 0.0;
-  for (int64_t b = threadIdx.x; b < blocks; b += blockDim.x) {
-    l0 += part_lse[2 * b];
-    l1 += part_lse[2 * b + 1];
-  }
-  red[0][threadIdx.x] = aux_part;
-  red[1][threadIdx.x] = l0;
-  red[2][threadIdx.x] = l1;
-  __syncthreads();
-  for (int s = 256; s >= 1; s >>= 1) {
-    if ((int)threadIdx.x < s) {
-#pragma unroll
-      for (int q = 0; q < 3; ++q) red[q][threadIdx.x] += red[q][threadIdx.x + s];
-    }
-    __syncthreads();
-  }
-  if (threadIdx.x == 0) {
-    const double ml = red[1][0] / (double)N;
-    hdr->aux_loss = (float)((double)alpha * (double)E * red[0][0]);
-    hdr->z_loss = (float)(ml * ml);
-    hdr->mean_lse_sq = (float)(red[2][0] / (double)N);
-    hdr->n_experts = (int32_t)E;
-  }
+  finalize_router_stats(part_p, part_cnt, part_lse, blocks, N, E, k, cap, ec, alpha, stats);
 }
 
-template <typename T, int V, bool kWSmem>
+namespace {
+
+template <typename T, int V, int CPL, int EPL, bool kWSmem, bool kLogitsIn>
 cudaError_t launch_router_t(const Plan& p, RouterArgs a, cudaStream_t st) {
-  const size_t wbytes = kWSmem ? (size_t)(p.E * p.d * sizeof(T)) : 0;
-  const size_t smem = wbytes + (size_t)(2 * kRouterWarps * p.E) * 4 + (size_t)p.E * 4;
-  auto kern = router_kernel<T, V, kWSmem>;
+  const size_t wbytes = kWSmem ? (size_t)(p.E * p.d * 4) : 0;
+  const size_t smem = wbytes + (size_t)(kRouterWarps * p.E) * 4 + (size_t)p.E * 4;
+  auto kern = router_kernel<T, V, CPL, EPL, kWSmem, kLogitsIn>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
-  kern<<<(unsigned)p.router_blocks, kRouterWarps * 32, smem, st>>>(a);
+  kern<<<(unsigned)p.tiles, kRouterWarps * 32, smem, st>>>(a);
   return cudaGetLastError();
 }
 
+template <typename T, int V, int CPL, int EPL>
+cudaError_t launch_router_w(const Plan& p, RouterArgs a, cudaStream_t st) {
+  const bool wsm = (size_t)(p.E * p.d * 4) <= 128 * 1024;
+  return wsm ? launch_router_t<T, V, CPL, EPL, true, false>(p, a, st)
+             : launch_router_t<T, V, CPL, EPL, false, false>(p, a, st);
+}
+
+template <typename T, int V, int EPL>
+cudaError_t launch_router_c(const Plan& p, RouterArgs a, cudaStream_t st) {
+  const int64_t cpl = ceil_div(p.d / (16 / (int64_t)sizeof(T)), 32);
+  if (cpl <= 2) return launch_router_w<T, V, 2, EPL>(p, a, st);
+  if (cpl <= 4) return launch_router_w<T, V, 4, EPL>(p, a, st);
+  if (cpl <= 8) return launch_router_w<T, V, 8, EPL>(p, a, st);
+  return launch_router_w<T, V, 16, EPL>(p, a, st);
+}
+
 template <typename T>
-cudaError_t launch_router_dt(const Plan& p, RouterArgs a, cudaStream_t st) {
-  const bool wsm = (size_t)(p.E * p.d * sizeof(T)) <= 96 * 1024;
-  if (p.E <= 8) return wsm ? launch_router_t<T, 8, true>(p, a, st) : launch_router_t<T, 8, false>(p, a, st);
-  if (p.E <= 16) return wsm ? launch_router_t<T, 16, true>(p, a, st) : launch_router_t<T, 16, false>(p, a, st);
-  return wsm ? launch_router_t<T, 32, true>(p, a, st) : launch_router_t<T, 32, false>(p, a, st);
+cudaError_t launch_router_logits_in(const Plan& p, RouterArgs a, cudaStream_t st) {
+  if (p.E <= 32) return launch_router_t<T, 32, 1, 1, false, true>(p, a, st);
+  if (p.E <= 64) return launch_router_t<T, 32, 1, 2, false, true>(p, a, st);
+  if (p.E <= 128) return launch_router_t<T, 32, 1, 4, false, true>(p, a, st);
+  if (p.E <= 256) return launch_router_t<T, 32, 1, 8, false, true>(p, a, st);
+  return launch_router_t<T, 32, 1, 16, false, true>(p, a, st);
+}
+
+template <typename T>
+cudaError_t launch_router_simt(const Plan& p, RouterArgs a, cudaStream_t st) {
+  if (p.E <= 8) return launch_router_c<T, 8, 1>(p, a, st);
+  if (p.E <= 16) return launch_router_c<T, 16, 1>(p, a, st);
+  if (p.E <= 32) return launch_router_c<T, 32, 1>(p, a, st);
+  if (p.E <= 64) return launch_router_c<T, 32, 2>(p, a, st);
+  if (p.E <= 128) return launch_router_c<T, 32, 4>(p, a, st);
+  if (p.E <= 256) return launch_router_c<T, 32, 8>(p, a, st);
+  return launch_router_c<T, 32, 16>(p, a, st);
 }
 
 }  // namespace
 
+// Router on the tensor cores for many experts: logits = x W_r^T + bias by the
+// grouped GEMM (gemm_tc.cu), then the softmax / top-k kernel reads them.
+bool router_uses_tc(const Plan& p) { return p.bf16 && p.E > 32; }
+
 cudaError_t launch_router(const Plan& p, const void* x, const moe_weights* w, int32_t* idx, float* gate,
-                          float* logits, float* probs, void* stats, void* ws, cudaStream_t st) {
-  RouterArgs a;
+                          float* logits, float* probs, void* stats, void* ws, cudaStream_t st,
+                          int32_t* tile_counts, bool finalize) {
+  RouterArgs a{};
   a.x = x;
   a.wr = w->w_router;
   a.logit_bias = w->logit_bias;
+  a.logits_in = nullptr;
   a.idx = idx;
   a.gate = gate;
   a.logits = logits;
@@ -329,17 +367,30 @@ cudaError_t launch_router(const Plan& p, const void* x, const moe_weights* w, in
   a.part_p = ws_at<float>(ws, p.part_p);
   a.part_cnt = ws_at<int32_t>(ws, p.part_cnt);
   a.part_lse = ws_at<float>(ws, p.part_lse);
+  a.tile_counts = tile_counts;
   a.status = status_ptr(p, ws);
   a.N = p.N;
   a.d = p.d;
   a.E = p.E;
   a.k = p.k;
+  a.cap = p.cap;
   a.gating = p.cfg.gating;
-  a.tpw = p.router_tpw;
-  cudaError_t err = p.bf16 ? launch_router_dt<__nv_bfloat16>(p, a, st) : launch_router_dt<float>(p, a, st);
+  a.alpha = p.cfg.aux_alpha;
+  cudaError_t err;
+  if (router_uses_tc(p)) {
+    float* lg = logits ? logits : ws_at<float>(ws, p.L.logits);
+    err = launch_router_logits_tc(p, x, w->w_router, w->logit_bias, lg, a.status, st);
+    if (err != cudaSuccess) return err;
+    a.logits_in = lg;
+    err = p.bf16 ? launch_router_logits_in<__nv_bfloat16>(p, a, st) : launch_router_logits_in<float>(p, a, st);
+  } else {
+    err = p.bf16 ? launch_router_simt<__nv_bfloat16>(p, a, st) : launch_router_simt<float>(p, a, st);
+  }
   if (err != cudaSuccess) return err;
-  router_finalize_kernel<<<1, 512, 0, st>>>(a.part_p, a.part_cnt, a.part_lse, p.router_blocks, p.N, p.E, p.k,
-                                            p.cap, p.ec ? 1 : 0, p.cfg.aux_alpha, stats);
+  if (finalize) {
+    router_finalize_kernel<<<1, 512, 0, st>>>(a.part_p, a.part_cnt, a.part_lse, p.tiles, p.N, p.E, p.k, p.cap,
+                                              p.ec ? 1 : 0, p.cfg.aux_alpha, stats);
+  }
   return cudaGetLastError();
 }
 
