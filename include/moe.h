@@ -253,6 +253,28 @@ MOE_API moe_status moe_forward_traced(const moe_config* cfg, const void* x, cons
                               void* stats, void* ws, size_t ws_bytes, void* stream, void* const* events,
                               int32_t n_events);
 
+/* moe_route without a workspace, for callers that cannot allocate device memory
+ * (a plugin handed only its input and output buffers by a framework that owns all
+ * device memory through its own pool; a latency-critical caller that must not
+ * enter the CUDA allocator, whose cudaMalloc / cudaFree can synchronise the
+ * device). The pages have no counterpart: this is a deployment variant of
+ * moe_route with the same arguments and results.
+ *  - Scratch (the router's per-block partial sums and an error word) is a fixed
+ *    4 MiB device array inside the library, held on every device that runs this
+ *    call until the process exits. A layer needing more -- 16*E*ceil(N/32) + 288
+ *    bytes -- returns MOE_ERR_UNSUPPORTED before anything is launched.
+ *  - All calls on a device share that array and it keeps the last call's
+ *    contents: calls that overlap on the GPU race, so serialise them.
+ *  - The first call on each device looks up the array's address; make it before
+ *    any stream capture.
+ *  - stats is required. Layers routed on the tensor cores (bf16, E > 32) need
+ *    logits, and expert choice needs probs (the buffers moe_route would otherwise
+ *    keep in its workspace); missing ones give MOE_ERR_INVALID_ARG.
+ *  - Device-side conditions are not reported back (there is no workspace error
+ *    word to read); arguments are checked on the host as for moe_route. */
+MOE_API moe_status moe_route_noalloc(const moe_config* cfg, const void* x, const moe_weights* w, int32_t* idx,
+                                     float* gate, float* logits, float* probs, void* stats, void* stream);
+
 /* Synchronises `stream`, reads and clears the workspace's device error word.
  * *device_error receives the raw word (0 = none). Returns MOE_OK, or
  * MOE_ERR_DEVICE_CHECK / MOE_ERR_TIMEOUT when a kernel recorded one. */

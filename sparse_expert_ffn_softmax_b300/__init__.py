@@ -59,7 +59,7 @@ class moe_stats_header(ctypes.Structure):
 
 def _load():
     if not os.path.exists(LIB_PATH):
-        raise ImportError(f"{LIB_PATH} is missing: build it with `python -m sparse_expert_ffn_softmax_b300.build` "
+        raise ImportError(f"{LIB_PATH} is missing: build it with `python sparse_expert_ffn_softmax_b300/build.py` "
                           "(the layer has no CPU path)")
     lib = ctypes.CDLL(LIB_PATH)
     P, S = ctypes.c_void_p, ctypes.c_size_t
@@ -78,6 +78,7 @@ def _load():
         "moe_forward": ([P, P, P, P, P, P, S, P], c),
         "moe_forward_traced": ([P, P, P, P, P, P, S, P, P, c], c),
         "moe_get_device_status": ([P, P, S, P, P], c),
+        "moe_route_noalloc": ([P, P, P, P, P, P, P, P, P], c),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -194,6 +195,13 @@ def ws_view(ws: torch.Tensor, offset: int, shape: Sequence[int], dtype: torch.dt
 def route(cfg, x, w: moe_weights, idx, gate, logits=None, probs=None, stats=None, ws=None, stream=None):
     _check(_lib.moe_route(ctypes.byref(cfg), _ptr(x), ctypes.byref(w), _ptr(idx), _ptr(gate), _ptr(logits),
                           _ptr(probs), _ptr(stats), _ptr(ws), ws.numel(), _stream(stream)), "moe_route")
+
+
+def route_noalloc(cfg, x, w: moe_weights, idx, gate, logits=None, probs=None, stats=None, stream=None):
+    """moe_route with no workspace: its scratch is a fixed device array inside the library
+    (for callers that cannot allocate; calls must not overlap on the GPU)."""
+    _check(_lib.moe_route_noalloc(ctypes.byref(cfg), _ptr(x), ctypes.byref(w), _ptr(idx), _ptr(gate),
+                                  _ptr(logits), _ptr(probs), _ptr(stats), _stream(stream)), "moe_route_noalloc")
 
 
 def permute(cfg, x, idx, gate, xp, tok_rows, tok_off, expert_off, row_token, row_gate, stats=None, ws=None,

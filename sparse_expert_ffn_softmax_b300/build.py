@@ -3,7 +3,8 @@
 Each ``csrc/*.cu`` is compiled to an object in parallel, then linked into one
 shared library with the CUDA runtime linked statically (the driver API entry
 point for tensor maps is looked up at run time, so the library loads on a
-machine without a GPU driver). Usage: ``python -m sparse_expert_ffn_softmax_b300.build``.
+machine without a GPU driver). Usage: ``python sparse_expert_ffn_softmax_b300/build.py``
+(run it by path: importing the package loads the library being rebuilt).
 """
 from __future__ import annotations
 
