@@ -98,6 +98,20 @@ class ClockSampler:
                 "reasons": sorted(reasons)}
 
 
+def measured_traffic(workload: str, kernel: str):
+    """DRAM bytes per launch of the up/down grouped GEMM from the committed ncu capture
+    (profiles/gemm_traffic_<workload>.json), or None when the GEMM source has changed since."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", f"gemm_traffic_{workload}.json")
+    if not os.path.exists(path):
+        return None
+    rec = json.load(open(path))
+    src = os.path.join(ROOT, "sparse_expert_ffn_softmax_b300", "csrc", "gemm_tc.cu")
+    if hashlib.sha256(open(src, "rb").read()).hexdigest() != rec.get("gemm_tc_cu_sha256"):
+        return None
+    return rec.get("traffic_bytes_up" if kernel == "up" else "traffic_bytes_down")
+
+
 def algorithmic(w, rows, touched):
     """Algorithmic FLOPs / bytes per forward (kept rows only, each operand once)."""
     b = 4 if w.dtype == "f32" else 2
@@ -298,7 +312,8 @@ def main():
                    "l2": "flushed between steps (256 MiB write)"},
         "roofline": {"kernel": "grouped_gemm " + ("up" if gi == 2 else "down"), "bound": "tensor",
                      "achieved": achieved_tflops, "peak": pk["bf16"], "unit": "TFLOP/s",
-                     "frac": achieved_tflops / pk["bf16"], "traffic": None,
+                     "frac": achieved_tflops / pk["bf16"],
+                     "traffic": measured_traffic(w.name, "up" if gi == 2 else "down"),
                      "peak_source": f"{pk['source']} bf16 dense burst"},
         "stages_ms": {s: float(v) for s, v in zip(STAGES, stage_avg)},
         "grouped_gemm_pct_bf16_peak": {
