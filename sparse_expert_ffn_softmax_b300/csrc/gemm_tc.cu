@@ -40,7 +40,8 @@ namespace tc {
 constexpr int BM = 128;
 constexpr int BK = 64;  // one 128-byte swizzle atom of bf16
 constexpr int UMMA_K = 16;
-constexpr int kEpiWarps = 8;
+constexpr int kEpiWarps = 12;          // 3 per TMEM lane quadrant
+constexpr int kEpiParts = kEpiWarps / 4;  // warps sharing a quadrant split its 32-column chunks
 constexpr int kThreads = 64 + kEpiWarps * 32;
 constexpr int kMaxGroups = 512 + 64;  // E <= 512 routed + S <= 64 shared groups
 constexpr unsigned long long kTimeoutNs = 2000000000ull;
@@ -510,7 +511,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------- epilogue warps ----------------
     const int ew = warp - 2;
     const int q = warp & 3;       // TMEM lane quadrant this warp may read
-    const int half = ew >> 2;     // which interleaved half of the 32-column chunks
+    const int part = ew >> 2;     // which interleaved share of the 32-column chunks
     const int r = q * 32 + lane;  // row inside the tile
     uint8_t* staging = smem + kStages * C::kStageBytes + ew * C::kStagingBytes;
     bool store_pending = false;
@@ -547,20 +548,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       float gate = 1.f;
       if (EPI == kLinear && F.row_gate && valid) gate = F.row_gate[grow];
 
-      // one 32-column chunk: registers v (and u, the W3 half for SwiGLU) -> outputs
+      // one 32-column chunk: registers v (and u, the W3 half for SwiGLU) -> outputs.
+      // bf16 results are packed in place (pk), fp32 results overwrite v.
       auto finish_chunk = [&](uint32_t(&v)[32], uint32_t(&u)[32], int c) {
-        float o[32];
+        uint32_t pk[16];
         if (EPI == kSwiglu) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const float a = __uint_as_float(v[i]);
-            o[i] = a / (1.f + __expf(-a)) * __uint_as_float(u[i]);
+          for (int i = 0; i < 16; ++i) {
+            const float a0 = __uint_as_float(v[2 * i]), a1 = __uint_as_float(v[2 * i + 1]);
+            const float h0 = a0 * rcp_ftz(1.f + ex2_ftz(-1.4426950408889634f * a0)) * __uint_as_float(u[2 * i]);
+            const float h1 =
+                a1 * rcp_ftz(1.f + ex2_ftz(-1.4426950408889634f * a1)) * __uint_as_float(u[2 * i + 1]);
+            const __nv_bfloat162 hb = __floats2bfloat162_rn(h0, h1);
+            pk[i] = *reinterpret_cast<const uint32_t*>(&hb);
           }
         } else {
-          float bsum[32];
+          // bias: one bf16 vector (common case) kept packed, or a sum of several added in place
+          uint4 braw[4] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0),
+                           make_uint4(0, 0, 0, 0)};
+          const bool one_bias = bias && F.bias_nsum == 1;
+          if (one_bias) {
+            const uint4* bp = reinterpret_cast<const uint4*>(bias + bcol0 + c);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) bsum[i] = 0.f;
-          if (bias) {
+            for (int q4 = 0; q4 < 4; ++q4) braw[q4] = __ldg(bp + q4);
+          } else if (bias) {
             for (int s = 0; s < F.bias_nsum; ++s) {
               const uint4* bp = reinterpret_cast<const uint4*>(bias + s * F.bias_sum_stride + bcol0 + c);
 #pragma unroll
@@ -568,7 +579,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float bv[8];
                 Vec16<__nv_bfloat16>::unpack(__ldg(bp + q4), bv);
 #pragma unroll
-                for (int i = 0; i < 8; ++i) bsum[8 * q4 + i] += bv[i];
+                for (int i = 0; i < 8; ++i) v[8 * q4 + i] = __float_as_uint(__uint_as_float(v[8 * q4 + i]) + bv[i]);
               }
             }
           }
@@ -576,13 +587,27 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
               const int64_t col = bcol0 + c + i;
-              bsum[i] += col < F.n_valid ? __ldg(F.bias_f32 + col) : 0.f;
+              if (col < F.n_valid) v[i] = __float_as_uint(__uint_as_float(v[i]) + __ldg(F.bias_f32 + col));
             }
           }
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const float a = __uint_as_float(v[i]) + bsum[i];
-            o[i] = EPI == kGelu ? gelu_as7126(a) : (EPI == kLogits ? a : a * gate);
+          for (int i = 0; i < 16; ++i) {
+            float a0 = __uint_as_float(v[2 * i]), a1 = __uint_as_float(v[2 * i + 1]);
+            if (one_bias) {
+              const uint32_t bw = (&braw[i >> 2].x)[i & 3];  // bf16x2: low half = column 2i
+              a0 += __uint_as_float(bw << 16);
+              a1 += __uint_as_float(bw & 0xFFFF0000u);
+            }
+            if (EPI == kGelu) {
+              const __nv_bfloat162 hb = __floats2bfloat162_rn(gelu_as7126(a0), gelu_as7126(a1));
+              pk[i] = *reinterpret_cast<const uint32_t*>(&hb);
+            } else if (EPI == kLinear) {
+              v[2 * i] = __float_as_uint(a0 * gate);
+              v[2 * i + 1] = __float_as_uint(a1 * gate);
+            } else {
+              v[2 * i] = __float_as_uint(a0);
+              v[2 * i + 1] = __float_as_uint(a1);
+            }
           }
         }
         if (use_tma) {
@@ -592,7 +617,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int j = 0; j < 4; ++j)
             *reinterpret_cast<uint4*>(staging + lane * 64 + 16 * (j ^ ((lane >> 1) & 3))) =
-                Vec16<__nv_bfloat16>::pack(o + 8 * j);
+                make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
@@ -605,54 +630,34 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int64_t col0 = bcol0 + c;
           if (col0 + 32 <= F.n_valid && (F.ld_out & 3) == 0) {  // rows 16-byte aligned
 #pragma unroll
-            for (int i = 0; i < 8; ++i) reinterpret_cast<uint4*>(dst)[i] = Vec16<float>::pack(o + 4 * i);
+            for (int i = 0; i < 8; ++i)
+              reinterpret_cast<uint4*>(dst)[i] = make_uint4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
           } else {
 #pragma unroll
             for (int i = 0; i < 32; ++i)
-              if (col0 + i < F.n_valid) dst[i] = o[i];
+              if (col0 + i < F.n_valid) dst[i] = __uint_as_float(v[i]);
           }
         } else if (valid) {
           if (EPI == kLinear) {
             uint4* dst = reinterpret_cast<uint4*>(static_cast<float*>(F.out) + out_off + c);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) dst[i] = Vec16<float>::pack(o + 4 * i);
+            for (int i = 0; i < 8; ++i) dst[i] = make_uint4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
           } else {
             uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(F.out) + out_off + c);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) dst[i] = Vec16<__nv_bfloat16>::pack(o + 8 * i);
+            for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
           }
         }
       };
-      auto load_chunk = [&](uint32_t(&v)[32], uint32_t(&u)[32], int c) {
-        tmem_ld32(tbase + (uint32_t)c, v);
-        if (EPI == kSwiglu) tmem_ld32(tbase + (uint32_t)(BN / 2 + c), u);
-      };
-      auto wait_chunk = [&](uint32_t(&v)[32], uint32_t(&u)[32]) {
-        tmem_ld_wait(v);
-        if (EPI == kSwiglu) reg_fence(u);
-      };
 
-      // chunks c = half*32, half*32 + 64, ...: the next chunk's TMEM load is in
-      // flight while the current one is converted and stored
-      uint32_t va[32], ua[32], vb[32], ub[32];
-      int c = half * 32;
-      if (EPI == kSwiglu) {  // two TMEM halves per chunk: no room to double-buffer
-        for (; c < kOutCols; c += 64) {
-          load_chunk(va, ua, c);
-          wait_chunk(va, ua);
-          finish_chunk(va, ua, c);
-        }
-      }
-      if (c < kOutCols) load_chunk(va, ua, c);
-      for (; c < kOutCols; c += 128) {
-        wait_chunk(va, ua);
-        if (c + 64 < kOutCols) load_chunk(vb, ub, c + 64);
+      // chunks c = part*32, part*32 + 32*kEpiParts, ...
+      uint32_t va[32], ua[32];
+      for (int c = part * 32; c < kOutCols; c += 32 * kEpiParts) {
+        tmem_ld32(tbase + (uint32_t)c, va);
+        if (EPI == kSwiglu) tmem_ld32(tbase + (uint32_t)(BN / 2 + c), ua);
+        tmem_ld_wait(va);
+        if (EPI == kSwiglu) reg_fence(ua);
         finish_chunk(va, ua, c);
-        if (c + 64 < kOutCols) {
-          wait_chunk(vb, ub);
-          if (c + 128 < kOutCols) load_chunk(va, ua, c + 128);
-          finish_chunk(vb, ub, c + 64);
-        }
       }
       tc_fence_before();
       __syncwarp();

@@ -9,7 +9,7 @@
 namespace moe {
 
 constexpr int kRouterWarps = 8;
-constexpr int kTileTokens = 32;  // permute tiles: one warp's 32 consecutive tokens
+constexpr int kMaxTileTokens = 32;  // a tile is ranked by one warp, one token per lane
 
 // Everything the launchers need, derived once from a validated moe_config.
 struct Plan {
@@ -18,7 +18,8 @@ struct Plan {
   bool bf16, swiglu, ec, bias;
   int64_t cap;       // C
   int64_t max_rows;  // rows reserved for xp / h / yp
-  int64_t tiles;     // ceil(N / 32)
+  int64_t tile;      // tokens per tile (8, 16 or 32): one router block, one permute block
+  int64_t tiles;     // ceil(N / tile)
   int64_t words;     // ceil(E / 32): expert bitmap words per token (expert choice)
   moe_workspace_layout L;
   // scratch sub-buffers (byte offsets into the workspace)

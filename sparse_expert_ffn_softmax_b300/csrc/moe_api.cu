@@ -67,7 +67,9 @@ moe_status make_plan(const moe_config* c, Plan* p) {
   if (p->cap < 0) p->cap = 0;
   p->max_rows = p->ec ? p->E * p->cap : p->N * p->k;
   if (p->max_rows >= (int64_t)1 << 31) return MOE_ERR_UNSUPPORTED;
-  p->tiles = ceil_div(p->N, kTileTokens);
+  // smaller tiles for smaller batches, so routing and permuting still spread over the SMs
+  p->tile = p->N >= 16384 ? 32 : (p->N >= 4096 ? 16 : 8);
+  p->tiles = ceil_div(p->N, p->tile);
   p->words = ceil_div(p->E, 32);
 
   const size_t b = p->bf16 ? 2 : 4;

@@ -38,8 +38,8 @@ namespace {
 constexpr int kWarps = 8;
 
 __global__ void __launch_bounds__(kWarps * 32) count_kernel(const int32_t* __restrict__ idx, int64_t N, int64_t k,
-                                                            int64_t E, int64_t T, int32_t* __restrict__ tile_counts,
-                                                            int32_t* status) {
+                                                            int64_t E, int64_t T, int64_t TT,
+                                                            int32_t* __restrict__ tile_counts, int32_t* status) {
   extern __shared__ int32_t s_hist[];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t tile = (int64_t)blockIdx.x * kWarps + warp;
@@ -47,8 +47,8 @@ __global__ void __launch_bounds__(kWarps * 32) count_kernel(const int32_t* __res
   int32_t* h = s_hist + warp * E;
   for (int64_t e = lane; e < E; e += 32) h[e] = 0;
   __syncwarp();
-  const int64_t t = tile * kTileTokens + lane;
-  if (t < N) {
+  const int64_t t = tile * TT + lane;
+  if (lane < TT && t < N) {
     for (int64_t j = 0; j < k; ++j) {
       const int32_t e = idx[t * k + j];
       if (e < 0 || e >= E) {
@@ -88,7 +88,7 @@ __global__ void __launch_bounds__(kWarps * 32) scan_offsets_kernel(
                                                 stats);
 }
 
-// One block per tile of 32 tokens. Warp 0 ranks the tile's (token, choice)
+// One block per tile of 8-32 tokens. Warp 0 ranks the tile's (token, choice)
 // pairs: the in-tile rank among the tile's tokens that chose the same expert is
 // the popcount of the lower lanes in a per-expert lane mask, so rank =
 // (assignments to e in earlier tiles) + in-tile rank is the exact token-order
@@ -104,12 +104,16 @@ template <typename DT, bool kFused>
 __global__ void __launch_bounds__(kWarps * 32) scatter_kernel(
     const DT* __restrict__ x, const int32_t* __restrict__ idx, const float* __restrict__ gate,
     const int32_t* __restrict__ counts_or_base, int32_t* __restrict__ expert_off, int64_t N, int64_t d, int64_t k,
-    int64_t E, int64_t T, int64_t cap, DT* __restrict__ xp, int32_t* __restrict__ tok_rows,
+    int64_t E, int64_t T, int64_t TT, int64_t cap, DT* __restrict__ xp, int32_t* __restrict__ tok_rows,
     int32_t* __restrict__ row_token, float* __restrict__ row_gate, void* stats, int32_t* status) {
+  // blockIdx.y selects a slice of the row's 16-byte chunks: small batches copy
+  // their rows with more blocks. Every slice ranks the tile (cheap); slice 0
+  // writes the row metadata.
+  const bool meta = blockIdx.y == 0;
   extern __shared__ uint32_t s_dyn[];
   uint32_t* msk = s_dyn;                                       // [E]
   int32_t* s_rows = reinterpret_cast<int32_t*>(s_dyn + E);     // [32][k]
-  int32_t* s_pre = s_rows + kTileTokens * k;                   // [E]   (kFused)
+  int32_t* s_pre = s_rows + kMaxTileTokens * k;                // [E]   (kFused)
   int32_t* s_off = s_pre + E;                                  // [E+1] (kFused)
   __shared__ int s_warp[33];
   using VT = Vec16<DT>;
@@ -144,19 +148,20 @@ __global__ void __launch_bounds__(kWarps * 32) scatter_kernel(
         dsum += tot - kept[i];
       }
     int rows = 0, dropped = 0;
+    const bool first = blockIdx.x == 0 && blockIdx.y == 0;
     int off = block_exclusive_scan(ksum, s_warp, &rows);  // (syncs: all totals read before overwritten)
-    if (blockIdx.x == 0) block_exclusive_scan(dsum, s_warp, &dropped);
+    if (first) block_exclusive_scan(dsum, s_warp, &dropped);
     for (int i = 0; i < per && i < 2; ++i)
       if (e0 + i < E) {
         s_off[e0 + i] = off;
-        if (blockIdx.x == 0) expert_off[e0 + i] = off;
+        if (first) expert_off[e0 + i] = off;
         off += kept[i];
       }
     if (threadIdx.x == 0) {
       s_off[E] = rows;
-      if (blockIdx.x == 0) expert_off[E] = rows;
+      if (first) expert_off[E] = rows;
     }
-    if (blockIdx.x == 0 && stats) {
+    if (first && stats) {
       moe_stats_header* hdr = static_cast<moe_stats_header*>(stats);
       int32_t* kept_out = reinterpret_cast<int32_t*>(reinterpret_cast<float*>(hdr + 1) + 2 * E) + E;
       for (int i = 0; i < per && i < 2; ++i)
@@ -172,8 +177,8 @@ __global__ void __launch_bounds__(kWarps * 32) scatter_kernel(
     __syncthreads();
   }
   if (warp == 0) {
-    const int64_t t = tile * kTileTokens + lane;
-    const bool valid = t < N;
+    const int64_t t = tile * TT + lane;
+    const bool valid = lane < TT && t < N;
     const uint32_t lt = (1u << lane) - 1u;
     if (valid)
       for (int64_t j = 0; j < k; ++j) {
@@ -186,7 +191,7 @@ __global__ void __launch_bounds__(kWarps * 32) scatter_kernel(
         const int32_t e = idx[t * k + j];
         if (e >= 0 && e < E) {
           const uint32_t old = atomicOr(&msk[e], 1u << lane);
-          if (old & (1u << lane)) record_error(status, kErrIndex, 104, (int32_t)t, e);  // expert listed twice
+          if ((old & (1u << lane)) && meta) record_error(status, kErrIndex, 104, (int32_t)t, e);  // listed twice
         }
       }
     __syncwarp();
@@ -199,27 +204,31 @@ __global__ void __launch_bounds__(kWarps * 32) scatter_kernel(
           const int64_t r = before + __popc(msk[e] & lt);
           if (r < cap) {
             row = (kFused ? s_off[e] : expert_off[e]) + (int32_t)r;
-            row_token[row] = (int32_t)t;
-            row_gate[row] = gate[t * k + j];
+            if (meta) {
+              row_token[row] = (int32_t)t;
+              row_gate[row] = gate[t * k + j];
+            }
           }
-        } else {
+        } else if (meta) {
           record_error(status, kErrIndex, 102, (int32_t)t, e);
         }
-        tok_rows[t * k + j] = row;
+        if (meta) tok_rows[t * k + j] = row;
       }
       s_rows[lane * k + j] = row;
     }
   }
   __syncthreads();
   const int64_t nchunk = d / VT::n;
-  for (int tt = warp; tt < kTileTokens; tt += kWarps) {
-    const int64_t tok = tile * kTileTokens + tt;
+  const int64_t cs = ceil_div(nchunk, (int64_t)gridDim.y);
+  const int64_t cbeg = (int64_t)blockIdx.y * cs, cend = cbeg + cs < nchunk ? cbeg + cs : nchunk;
+  for (int tt = warp; tt < TT; tt += kWarps) {
+    const int64_t tok = tile * TT + tt;
     if (tok >= N) break;
     const int32_t my_row = lane < k ? s_rows[tt * k + lane] : -1;
     const uint4* src = reinterpret_cast<const uint4*>(x) + tok * nchunk;
-    for (int64_t c0 = 0; c0 < nchunk; c0 += 32) {
+    for (int64_t c0 = cbeg; c0 < cend; c0 += 32) {
       const int64_t c = c0 + lane;
-      const bool act = c < nchunk;
+      const bool act = c < cend;
       uint4 v = make_uint4(0, 0, 0, 0);
       if (act) v = __ldg(src + c);
       for (int j = 0; j < k; ++j) {
@@ -391,16 +400,18 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(const float* __res
                                                               const int32_t* __restrict__ tok_off,
                                                               const float* __restrict__ ys, int64_t N, int64_t d,
                                                               int64_t k, TO* __restrict__ out, RouterStatsArgs fin,
-                                                              int64_t E, int64_t cap, void* stats) {
-  // Block 0 also reduces the router statistics when asked: nothing waits on them.
-  if (fin.part_p && blockIdx.x == 0)
-    finalize_router_stats(fin.part_p, fin.part_cnt, fin.part_lse, ceil_div(N, (int64_t)kTileTokens), N, E, k, cap,
-                          0, fin.alpha, stats);
+                                                              int64_t E, int64_t cap, int64_t tiles, void* stats) {
+  // Block (0, 0) also reduces the router statistics when asked: nothing waits on them.
+  if (fin.part_p && blockIdx.x == 0 && blockIdx.y == 0)
+    finalize_router_stats(fin.part_p, fin.part_cnt, fin.part_lse, tiles, N, E, k, cap, 0, fin.alpha, stats);
   using VO = Vec16<TO>;
   constexpr int VN = VO::n;  // outputs per lane chunk: 8 (bf16) or 4 (fp32)
   constexpr int NV = VN / 4; // float4 loads per row and chunk
   const int lane = threadIdx.x & 31;
   const int64_t nchunk = d / VN;
+  // blockIdx.y selects a slice of the row's chunks (more blocks for small batches)
+  const int64_t cs = ceil_div(nchunk, (int64_t)gridDim.y);
+  const int64_t cbeg = (int64_t)blockIdx.y * cs, cend = cbeg + cs < nchunk ? cbeg + cs : nchunk;
   for (int64_t t = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5); t < N; t += (int64_t)gridDim.x * kWarps) {
     int64_t beg, n;
     if (tok_off) {
@@ -411,9 +422,9 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(const float* __res
       n = k;
     }
     const int32_t my_row = lane < n ? tok_rows[beg + lane] : -1;
-    for (int64_t c0 = 0; c0 < nchunk; c0 += 32) {
+    for (int64_t c0 = cbeg; c0 < cend; c0 += 32) {
       const int64_t c = c0 + lane;
-      const bool act = c < nchunk;
+      const bool act = c < cend;
       float acc[VN];
 #pragma unroll
       for (int i = 0; i < VN; ++i) acc[i] = 0.f;
@@ -463,17 +474,23 @@ cudaError_t launch_permute_t(const Plan& p, const void* x, const int32_t* idx, c
   }
   int32_t* tile_counts = ws_at<int32_t>(ws, p.tile_counts);
   int32_t* tile_base = ws_at<int32_t>(ws, p.tile_base);
+  // row slices per tile so that about two blocks per SM copy rows
+  const int64_t nchunk = p.d / (16 / (int64_t)sizeof(T));
+  int64_t slices = ceil_div(2 * 148, p.tiles);
+  const int64_t max_slices = ceil_div(nchunk, 32);
+  if (slices > max_slices) slices = max_slices;
+  if (slices < 1) slices = 1;
   if (mode == kFusedOffsets) {
-    const size_t sc_smem = (size_t)p.E * 4 + (size_t)kTileTokens * p.k * 4 + (size_t)(2 * p.E + 1) * 4;
-    scatter_kernel<T, true><<<(unsigned)p.tiles, kWarps * 32, sc_smem, st>>>(
-        static_cast<const T*>(x), idx, gate, tile_counts, expert_off, p.N, p.d, p.k, p.E, p.tiles, p.cap,
+    const size_t sc_smem = (size_t)p.E * 4 + (size_t)kMaxTileTokens * p.k * 4 + (size_t)(2 * p.E + 1) * 4;
+    scatter_kernel<T, true><<<dim3((unsigned)p.tiles, (unsigned)slices), kWarps * 32, sc_smem, st>>>(
+        static_cast<const T*>(x), idx, gate, tile_counts, expert_off, p.N, p.d, p.k, p.E, p.tiles, p.tile, p.cap,
         static_cast<T*>(xp), tok_rows, row_token, row_gate, stats, status);
     return cudaGetLastError();
   }
   if (mode == kCountsFromIdx) {
     const size_t hist_smem = (size_t)kWarps * p.E * 4;
     count_kernel<<<(unsigned)ceil_div(p.tiles, kWarps), kWarps * 32, hist_smem, st>>>(idx, p.N, p.k, p.E, p.tiles,
-                                                                                    tile_counts, status);
+                                                                                    p.tile, tile_counts, status);
   }
   RouterStatsArgs rs{};
   if (mode == kCountsFromRouter) {
@@ -484,9 +501,9 @@ cudaError_t launch_permute_t(const Plan& p, const void* x, const int32_t* idx, c
   }
   scan_offsets_kernel<<<(unsigned)ceil_div(p.E, kWarps), kWarps * 32, 0, st>>>(
       tile_counts, p.E, p.tiles, p.cap, p.N, p.k, tile_base, expert_off, stats, status + 5, rs);
-  const size_t sc_smem = (size_t)p.E * 4 + (size_t)kTileTokens * p.k * 4;
-  scatter_kernel<T, false><<<(unsigned)p.tiles, kWarps * 32, sc_smem, st>>>(
-      static_cast<const T*>(x), idx, gate, tile_base, expert_off, p.N, p.d, p.k, p.E, p.tiles, p.cap,
+  const size_t sc_smem = (size_t)p.E * 4 + (size_t)kMaxTileTokens * p.k * 4;
+  scatter_kernel<T, false><<<dim3((unsigned)p.tiles, (unsigned)slices), kWarps * 32, sc_smem, st>>>(
+      static_cast<const T*>(x), idx, gate, tile_base, expert_off, p.N, p.d, p.k, p.E, p.tiles, p.tile, p.cap,
       static_cast<T*>(xp), tok_rows, row_token, row_gate, stats, status);
   return cudaGetLastError();
 }
@@ -515,6 +532,12 @@ bool permute_fuses_offsets(const Plan& p) { return !p.ec && p.E * p.tiles <= 819
 cudaError_t launch_combine(const Plan& p, const void* yp, const int32_t* tok_rows, const int32_t* tok_off,
                            const void* ys, void* out, cudaStream_t st, void* ws, void* stats) {
   const int64_t blocks = ceil_div(p.N, kWarps) < 148 * 16 ? ceil_div(p.N, kWarps) : 148 * 16;
+  const int64_t nchunk = p.d / (p.bf16 ? 8 : 4);
+  int64_t slices = ceil_div(4 * 148, blocks);  // small batches: split rows so ~4 blocks per SM combine
+  const int64_t max_slices = ceil_div(nchunk, 32);
+  if (slices > max_slices) slices = max_slices;
+  if (slices < 1) slices = 1;
+  const dim3 grid((unsigned)blocks, (unsigned)slices);
   RouterStatsArgs fin{};
   if (ws && stats) {
     fin.part_p = ws_at<float>(ws, p.part_p);
@@ -523,13 +546,13 @@ cudaError_t launch_combine(const Plan& p, const void* yp, const int32_t* tok_row
     fin.alpha = p.cfg.aux_alpha;
   }
   if (p.bf16) {
-    combine_kernel<__nv_bfloat16><<<(unsigned)blocks, kWarps * 32, 0, st>>>(
+    combine_kernel<__nv_bfloat16><<<grid, kWarps * 32, 0, st>>>(
         static_cast<const float*>(yp), tok_rows, p.ec ? tok_off : nullptr, static_cast<const float*>(ys), p.N, p.d,
-        p.k, static_cast<__nv_bfloat16*>(out), fin, p.E, p.cap, stats);
+        p.k, static_cast<__nv_bfloat16*>(out), fin, p.E, p.cap, p.tiles, stats);
   } else {
-    combine_kernel<float><<<(unsigned)blocks, kWarps * 32, 0, st>>>(
+    combine_kernel<float><<<grid, kWarps * 32, 0, st>>>(
         static_cast<const float*>(yp), tok_rows, p.ec ? tok_off : nullptr, static_cast<const float*>(ys), p.N, p.d,
-        p.k, static_cast<float*>(out), fin, p.E, p.cap, stats);
+        p.k, static_cast<float*>(out), fin, p.E, p.cap, p.tiles, stats);
   }
   return cudaGetLastError();
 }

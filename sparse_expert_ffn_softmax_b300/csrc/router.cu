@@ -10,8 +10,8 @@
 // "MoE Architecture" (vanos001.github.io) TokenChoiceRouter (top-k on logits,
 // softmax over the k).
 //
-// One block = one tile of 32 consecutive tokens, one warp per token (8 warps,
-// 4 tokens each). Lane l keeps the logits of experts l, l+32, ... in registers.
+// One block = one tile of 8, 16 or 32 consecutive tokens, one warp per token
+// (8 warps, 1-4 tokens each). Lane l keeps the logits of experts l, l+32, ... in registers.
 // For E <= 32 the lanes split d into 16-byte vectors and keep one partial dot
 // product per expert of a group of V experts; a transpose-reduce (V/2 + ... + 1
 // shuffles, then a butterfly over the rest) leaves lane l with the logit of
@@ -58,7 +58,7 @@ struct RouterArgs {
   float* part_lse;    // [blocks][2]
   int32_t* tile_counts;  // [E][blocks] per-tile assignment counts for the permute, or null
   int32_t* status;
-  int64_t N, d, E, k, cap;
+  int64_t N, d, E, k, cap, tile;
   int gating;
   float alpha;
 };
@@ -111,8 +111,8 @@ __global__ void __launch_bounds__(kRouterWarps * 32) router_kernel(RouterArgs a)
   float lse_sum = 0.f, lse_sq = 0.f;
   const bool ec = a.gating == MOE_GATE_EXPERT_CHOICE;
 
-  for (int it = 0; it < kTileTokens / kRouterWarps; ++it) {
-    const int64_t t = (int64_t)blockIdx.x * kTileTokens + it * kRouterWarps + warp;
+  for (int64_t it = 0; it < a.tile / kRouterWarps; ++it) {
+    const int64_t t = (int64_t)blockIdx.x * a.tile + it * kRouterWarps + warp;
     if (t >= a.N) break;
     // ---- logits of token t: lane l holds expert l + 32 i in Lr[i] ----
     float Lr[EPL];
@@ -374,6 +374,7 @@ cudaError_t launch_router(const Plan& p, const void* x, const moe_weights* w, in
   a.E = p.E;
   a.k = p.k;
   a.cap = p.cap;
+  a.tile = p.tile;
   a.gating = p.cfg.gating;
   a.alpha = p.cfg.aux_alpha;
   cudaError_t err;
