@@ -259,11 +259,11 @@ MOE_API moe_status moe_forward_traced(const moe_config* cfg, const void* x, cons
  * enter the CUDA allocator, whose cudaMalloc / cudaFree can synchronise the
  * device). The pages have no counterpart: this is a deployment variant of
  * moe_route with the same arguments and results.
- *  - Scratch (the router's per-block partial sums and an error word) is a fixed
- *    4 MiB device array inside the library, held on every device that runs this
- *    call until the process exits. A layer needing more -- 16*E*T + 288 bytes, T =
- *    ceil(N/32) for N >= 16384, ceil(N/16) for N >= 4096, ceil(N/8) below -- returns
- *    MOE_ERR_UNSUPPORTED before anything is launched.
+ *  - Scratch (an error word and the router's statistic accumulators, 12*E + 16
+ *    bytes) is a fixed 4 KiB device array inside the library, held on every device
+ *    that runs this call until the process exits. Layers with more than 318
+ *    routed experts need more and return MOE_ERR_UNSUPPORTED before anything is
+ *    launched.
  *  - All calls on a device share that array and it keeps the last call's
  *    contents: calls that overlap on the GPU race, so serialise them.
  *  - The first call on each device looks up the array's address; make it before

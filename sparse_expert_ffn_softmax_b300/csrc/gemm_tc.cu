@@ -534,7 +534,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool valid = ti.mt * BM + r < ti.m;
       // bf16 outputs of a warp whose 32 rows all belong to the group go out as one
       // TMA block store; a group's ragged last rows are stored row by row.
-      const bool use_tma = (EPI == kGelu || EPI == kSwiglu) && F.tma_out && ti.mt * BM + q * 32 + 32 <= ti.m;
+      const bool use_tma = EPI != kLogits && F.tma_out && ti.mt * BM + q * 32 + 32 <= ti.m;
       const int64_t grow = (int64_t)ti.a_row0 + r;
       const uint32_t tbase = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(q * 32) << 16);
       // H tiles (GELU / SwiGLU) are stored as bf16 for the next GEMM; gate-scaled
@@ -611,20 +611,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (use_tma) {
-          // staging: row `lane`, 16-byte chunk j at chunk j ^ ((row >> 1) & 3) (64-byte swizzle)
-          if (lane == 0 && store_pending) bulk_wait_read0();
-          __syncwarp();
+          // 64-byte rows through the staging block: row `lane`, 16-byte chunk j stored at
+          // chunk j ^ ((row >> 1) & 3) (64-byte swizzle). bf16: one 32-column block;
+          // fp32: two 16-column blocks.
 #pragma unroll
-          for (int j = 0; j < 4; ++j)
-            *reinterpret_cast<uint4*>(staging + lane * 64 + 16 * (j ^ ((lane >> 1) & 3))) =
-                make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            tma_store_2d(omap, staging, ox0 + c, oy);
-            bulk_commit();
+          for (int h = 0; h < (EPI == kLinear ? 2 : 1); ++h) {
+            if (lane == 0 && store_pending) bulk_wait_read0();
+            __syncwarp();
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const uint4 val = EPI == kLinear
+                                    ? make_uint4(v[16 * h + 4 * j], v[16 * h + 4 * j + 1], v[16 * h + 4 * j + 2],
+                                                 v[16 * h + 4 * j + 3])
+                                    : make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+              *reinterpret_cast<uint4*>(staging + lane * 64 + 16 * (j ^ ((lane >> 1) & 3))) = val;
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(omap, staging, ox0 + c + 16 * h, oy);
+              bulk_commit();
+            }
+            store_pending = true;
           }
-          store_pending = true;
         } else if (valid && EPI == kLogits) {
           float* dst = static_cast<float*>(F.out) + out_off + c;
           const int64_t col0 = bcol0 + c;
@@ -716,9 +725,13 @@ bool make_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int b
                      CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-// Output blocks: bf16, 32 x 32, 64-byte swizzle (matches the epilogue staging layout).
+// Output blocks of 32 rows x 64 bytes, 64-byte swizzle (the epilogue staging layout):
+// bf16 32 columns, or fp32 16 columns.
 bool make_out_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols) {
   return make_map_ex(m, ptr, rows, cols, 32, 32, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, CU_TENSOR_MAP_SWIZZLE_64B);
+}
+bool make_out_map_f32(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols) {
+  return make_map_ex(m, ptr, rows, cols, 16, 32, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
 int num_sms() {
@@ -864,9 +877,13 @@ cudaError_t launch_ffn_bf16(const Plan& p, const void* xp, const int32_t* expert
     for (int i = 1; i < 8; ++i) maps[i] = maps[0];
     bool ok = make_map(&maps[2], w->w2, p.E * p.d, p.F, bn);
     if (p.S > 0) ok = ok && make_map(&maps[1], hs, p.N, p.S * p.Fs, BM) && make_map(&maps[3], w->ws2, p.S * p.d, p.Fs, bn);
+    ok = ok && make_out_map_f32(&maps[6], yp, R, p.d);
+    if (p.S > 0) ok = ok && make_out_map_f32(&maps[7], ys, p.N, p.d);
     if (!ok) return cudaErrorInvalidValue;
     Params P{};
     Family& f0 = P.fam[0];
+    f0.tma_out = 1;
+    P.fam[1].tma_out = p.S > 0 ? 1 : 0;
     f0.groups = (int32_t)p.E;
     f0.m_from_off = 1;
     f0.n_tiles = (int32_t)(p.d / bn);

@@ -23,7 +23,7 @@ struct Plan {
   int64_t words;     // ceil(E / 32): expert bitmap words per token (expert choice)
   moe_workspace_layout L;
   // scratch sub-buffers (byte offsets into the workspace)
-  size_t part_p, part_cnt, part_lse;  // router partials
+  size_t stat_acc;                    // fixed-point router statistic accumulators (stats.cuh)
   size_t tile_counts, tile_base;      // permute [E][T], [E][T+1]
   size_t ec_bits;                     // [N][words]
   size_t logits_raw;                  // unused for now
@@ -54,7 +54,7 @@ bool router_uses_tc(const Plan& p);
 //                    finalises the router statistics;
 //  kFusedOffsets     the router wrote the counts and every scatter block derives
 //                    its prefixes and the expert offsets itself (small E x T,
-//                    permute_fuses_offsets); the combine reduces the statistics.
+//                    permute_fuses_offsets); scatter block 0 finalises the statistics.
 enum PermuteMode { kCountsFromIdx = 0, kCountsFromRouter = 1, kFusedOffsets = 2 };
 bool permute_fuses_offsets(const Plan& p);
 cudaError_t launch_ec_select(const Plan& p, const float* probs, int32_t* idx, float* gate, void* ws,
@@ -62,9 +62,8 @@ cudaError_t launch_ec_select(const Plan& p, const float* probs, int32_t* idx, fl
 cudaError_t launch_permute(const Plan& p, const void* x, const int32_t* idx, const float* gate, void* xp,
                            int32_t* tok_rows, int32_t* tok_off, int32_t* expert_off, int32_t* row_token,
                            float* row_gate, void* stats, void* ws, cudaStream_t st, PermuteMode mode);
-// ws and stats non-null: block 0 also reduces the router statistics from ws.
 cudaError_t launch_combine(const Plan& p, const void* yp, const int32_t* tok_rows, const int32_t* tok_off,
-                           const void* ys, void* out, cudaStream_t st, void* ws = nullptr, void* stats = nullptr);
+                           const void* ys, void* out, cudaStream_t st);
 
 // ffn_simt.cu (fp32 layers)
 cudaError_t launch_ffn_f32(const Plan& p, const void* xp, const int32_t* expert_off, const float* row_gate,

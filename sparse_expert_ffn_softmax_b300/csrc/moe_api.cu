@@ -7,6 +7,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "stats.cuh"
 
 namespace moe {
 namespace {
@@ -98,9 +99,7 @@ moe_status make_plan(const moe_config* c, Plan* p) {
   L.ys = take(p->S > 0 ? (size_t)p->N * (size_t)p->d * 4 : 0);
   L.stats = take(moe_stats_bytes(p->E));
   L.scratch = o;
-  p->part_p = take((size_t)(p->E * p->tiles) * 4);  // router partials, one block per tile
-  p->part_cnt = take((size_t)(p->E * p->tiles) * 4);
-  p->part_lse = take((size_t)(2 * p->tiles) * 4);
+  p->stat_acc = take(stats_acc_bytes(p->E));  // zeroed by moe_workspace_init, reset by each finaliser
   p->tile_counts = take((size_t)(p->E * p->tiles) * 4);
   p->tile_base = take((size_t)(p->E * (p->tiles + 1)) * 4);
   p->ec_bits = take((size_t)(p->N * p->words) * 4);
@@ -217,7 +216,9 @@ moe_status moe_workspace_init(const moe_config* cfg, void* ws, size_t ws_bytes, 
   if (s != MOE_OK) return s;
   if ((s = check_ws(p, ws, ws_bytes)) != MOE_OK) return s;
   cudaGetLastError();
-  return cuda_status(cudaMemsetAsync(ws_at<uint8_t>(ws, p.L.status), 0, 32, (cudaStream_t)stream));
+  cudaStream_t st = (cudaStream_t)stream;
+  if (cudaMemsetAsync(ws_at<uint8_t>(ws, p.L.status), 0, 32, st) != cudaSuccess) return MOE_ERR_CUDA;
+  return cuda_status(cudaMemsetAsync(ws_at<uint8_t>(ws, p.stat_acc), 0, stats_acc_bytes(p.E), st));
 }
 
 moe_status moe_route(const moe_config* cfg, const void* x, const moe_weights* w, int32_t* idx, float* gate,
@@ -332,9 +333,7 @@ moe_status moe_forward_traced(const moe_config* cfg, const void* x, const moe_we
   if (!mark()) return MOE_ERR_CUDA;
   if ((s = do_ffn(p, xp, expert_off, row_gate, x, w, yp, ys, ws, st, 2)) != MOE_OK) return s;
   if (!mark()) return MOE_ERR_CUDA;
-  if (launch_combine(p, yp, tok_rows, tok_off, ys, out, st, fused_offsets ? ws : nullptr,
-                     fused_offsets ? st_buf : nullptr) != cudaSuccess)
-    return MOE_ERR_CUDA;
+  if (launch_combine(p, yp, tok_rows, tok_off, ys, out, st) != cudaSuccess) return MOE_ERR_CUDA;
   if (!mark()) return MOE_ERR_CUDA;
   return MOE_OK;
 }

@@ -3,8 +3,9 @@
 // output buffers by a host framework that owns every byte of device memory
 // through its own pool, or a latency-critical caller that must not enter the
 // CUDA allocator (cudaMalloc / cudaFree can synchronise the device). Its
-// scratch memory (the router's per-block partial sums and an error word) lives
-// in a file-scope device array of fixed size, so the call allocates nothing.
+// scratch memory (an error word and the router's fixed-point statistic
+// accumulators) lives in a file-scope device array of fixed size, so the call
+// allocates nothing.
 //
 // The array is shared by every call in the process on a given device and keeps
 // the last call's contents; calls that overlap on the GPU (different streams,
@@ -17,11 +18,12 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "stats.cuh"
 
 namespace moe {
 namespace {
 
-constexpr size_t kNoAllocScratchBytes = size_t(4) << 20;  // 4 MiB per device, held until process exit
+constexpr size_t kNoAllocScratchBytes = 4096;  // per device, held until process exit: E <= 318
 constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) uint8_t g_route_scratch[kNoAllocScratchBytes];
@@ -67,24 +69,22 @@ extern "C" MOE_API moe_status moe_route_noalloc(const moe_config* cfg, const voi
   if (router_uses_tc(p) && !logits) return MOE_ERR_INVALID_ARG;  // tensor-core router writes logits first
   if (p.ec && !probs) return MOE_ERR_INVALID_ARG;                 // expert choice selects on the probabilities
   if (p.N == 0) return MOE_OK;
-  // Scratch layout inside the static array: error word, then the router partials.
+  // Scratch layout inside the static array: error word, then the statistic accumulators.
   size_t o = 0;
   const size_t status_off = o;
   o += align256(32);
-  p.part_p = o;
-  o += align256((size_t)(p.E * p.tiles) * 4);
-  p.part_cnt = o;
-  o += align256((size_t)(p.E * p.tiles) * 4);
-  p.part_lse = o;
-  o += align256((size_t)(2 * p.tiles) * 4);
+  p.stat_acc = o;
+  o += align256(stats_acc_bytes(p.E));
   if (o > kNoAllocScratchBytes) return MOE_ERR_UNSUPPORTED;  // layer too large for the fixed scratch
   p.L.status = status_off;
   void* scratch = nullptr;
   if ((s = scratch_address(&scratch)) != MOE_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaGetLastError();
-  // The error word must start at zero; the partials are fully rewritten by the router.
-  if (cudaMemsetAsync(static_cast<uint8_t*>(scratch) + status_off, 0, 32, st) != cudaSuccess) return MOE_ERR_CUDA;
+  // The error word and the statistic accumulators must start at zero.
+  if (cudaMemsetAsync(static_cast<uint8_t*>(scratch) + status_off, 0, p.stat_acc + stats_acc_bytes(p.E) - status_off,
+                      st) != cudaSuccess)
+    return MOE_ERR_CUDA;
   if (launch_router(p, x, w, idx, gate, logits, probs, stats, scratch, st, nullptr, true) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (p.ec && launch_ec_select(p, probs, idx, gate, scratch, st) != cudaSuccess) return MOE_ERR_CUDA;

@@ -62,10 +62,8 @@ __global__ void __launch_bounds__(kWarps * 32) count_kernel(const int32_t* __res
   for (int64_t e = lane; e < E; e += 32) tile_counts[e * T + tile] = h[e];
 }
 
-struct RouterStatsArgs {
-  const float* part_p;
-  const int32_t* part_cnt;
-  const float* part_lse;
+struct RouterStatsArgs {  // finalise the router statistics from these accumulators (acc.p null: no)
+  StatsAcc acc;
   float alpha;
 };
 
@@ -84,8 +82,7 @@ __global__ void __launch_bounds__(kWarps * 32) scan_offsets_kernel(
   if (e < E) scan_expert_tiles(tile_counts + e * T, tile_base + e * (T + 1), T);
   if (!last_block_ticket(ticket)) return;
   offsets_from_totals(tile_base, E, T, cap, N, k, expert_off, stats);
-  if (stats && rs.part_p) finalize_router_stats(rs.part_p, rs.part_cnt, rs.part_lse, T, N, E, k, cap, 0, rs.alpha,
-                                                stats);
+  if (stats && rs.acc.p) finalize_router_stats(rs.acc, N, E, k, cap, 0, rs.alpha, stats);
 }
 
 // One block per tile of 8-32 tokens. Warp 0 ranks the tile's (token, choice)
@@ -98,14 +95,17 @@ __global__ void __launch_bounds__(kWarps * 32) scan_offsets_kernel(
 // kFused: the block itself derives what it needs from the router's per-tile
 // counts [E][T] -- the count of each expert in earlier tiles, the totals, and
 // expert_off (every block computes the same integers; block 0 also writes
-// expert_off and the dropping statistics) -- so no scan kernel runs before it.
+// expert_off and the dropping statistics) -- so no scan kernel runs before it;
+// one extra block (blockIdx.x == T) turns the router's accumulators into the
+// router statistics.
 // Otherwise tile_base [E][T+1] and expert_off come from scan_offsets_kernel.
 template <typename DT, bool kFused>
 __global__ void __launch_bounds__(kWarps * 32) scatter_kernel(
     const DT* __restrict__ x, const int32_t* __restrict__ idx, const float* __restrict__ gate,
     const int32_t* __restrict__ counts_or_base, int32_t* __restrict__ expert_off, int64_t N, int64_t d, int64_t k,
     int64_t E, int64_t T, int64_t TT, int64_t cap, DT* __restrict__ xp, int32_t* __restrict__ tok_rows,
-    int32_t* __restrict__ row_token, float* __restrict__ row_gate, void* stats, int32_t* status) {
+    int32_t* __restrict__ row_token, float* __restrict__ row_gate, void* stats, int32_t* status,
+    RouterStatsArgs rs) {
   // blockIdx.y selects a slice of the row's 16-byte chunks: small batches copy
   // their rows with more blocks. Every slice ranks the tile (cheap); slice 0
   // writes the row metadata.
@@ -119,6 +119,10 @@ __global__ void __launch_bounds__(kWarps * 32) scatter_kernel(
   using VT = Vec16<DT>;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t tile = blockIdx.x;
+  if (tile >= T) {  // the extra block: router statistics, off the other blocks' path
+    if (stats && rs.acc.p && blockIdx.y == 0) finalize_router_stats(rs.acc, N, E, k, cap, 0, rs.alpha, stats);
+    return;
+  }
   if (kFused) {
     for (int64_t e = warp; e < E; e += kWarps) {
       const int32_t* cnt = counts_or_base + e * T;
@@ -399,11 +403,7 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(const float* __res
                                                               const int32_t* __restrict__ tok_rows,
                                                               const int32_t* __restrict__ tok_off,
                                                               const float* __restrict__ ys, int64_t N, int64_t d,
-                                                              int64_t k, TO* __restrict__ out, RouterStatsArgs fin,
-                                                              int64_t E, int64_t cap, int64_t tiles, void* stats) {
-  // Block (0, 0) also reduces the router statistics when asked: nothing waits on them.
-  if (fin.part_p && blockIdx.x == 0 && blockIdx.y == 0)
-    finalize_router_stats(fin.part_p, fin.part_cnt, fin.part_lse, tiles, N, E, k, cap, 0, fin.alpha, stats);
+                                                              int64_t k, TO* __restrict__ out) {
   using VO = Vec16<TO>;
   constexpr int VN = VO::n;  // outputs per lane chunk: 8 (bf16) or 4 (fp32)
   constexpr int NV = VN / 4; // float4 loads per row and chunk
@@ -481,10 +481,13 @@ cudaError_t launch_permute_t(const Plan& p, const void* x, const int32_t* idx, c
   if (slices > max_slices) slices = max_slices;
   if (slices < 1) slices = 1;
   if (mode == kFusedOffsets) {
+    RouterStatsArgs fin{};
+    fin.acc = stats_acc_at(ws_at<uint8_t>(ws, p.stat_acc), p.E);
+    fin.alpha = p.cfg.aux_alpha;
     const size_t sc_smem = (size_t)p.E * 4 + (size_t)kMaxTileTokens * p.k * 4 + (size_t)(2 * p.E + 1) * 4;
-    scatter_kernel<T, true><<<dim3((unsigned)p.tiles, (unsigned)slices), kWarps * 32, sc_smem, st>>>(
+    scatter_kernel<T, true><<<dim3((unsigned)p.tiles + 1, (unsigned)slices), kWarps * 32, sc_smem, st>>>(
         static_cast<const T*>(x), idx, gate, tile_counts, expert_off, p.N, p.d, p.k, p.E, p.tiles, p.tile, p.cap,
-        static_cast<T*>(xp), tok_rows, row_token, row_gate, stats, status);
+        static_cast<T*>(xp), tok_rows, row_token, row_gate, stats, status, fin);
     return cudaGetLastError();
   }
   if (mode == kCountsFromIdx) {
@@ -494,9 +497,7 @@ cudaError_t launch_permute_t(const Plan& p, const void* x, const int32_t* idx, c
   }
   RouterStatsArgs rs{};
   if (mode == kCountsFromRouter) {
-    rs.part_p = ws_at<float>(ws, p.part_p);
-    rs.part_cnt = ws_at<int32_t>(ws, p.part_cnt);
-    rs.part_lse = ws_at<float>(ws, p.part_lse);
+    rs.acc = stats_acc_at(ws_at<uint8_t>(ws, p.stat_acc), p.E);
     rs.alpha = p.cfg.aux_alpha;
   }
   scan_offsets_kernel<<<(unsigned)ceil_div(p.E, kWarps), kWarps * 32, 0, st>>>(
@@ -504,7 +505,7 @@ cudaError_t launch_permute_t(const Plan& p, const void* x, const int32_t* idx, c
   const size_t sc_smem = (size_t)p.E * 4 + (size_t)kMaxTileTokens * p.k * 4;
   scatter_kernel<T, false><<<dim3((unsigned)p.tiles, (unsigned)slices), kWarps * 32, sc_smem, st>>>(
       static_cast<const T*>(x), idx, gate, tile_base, expert_off, p.N, p.d, p.k, p.E, p.tiles, p.tile, p.cap,
-      static_cast<T*>(xp), tok_rows, row_token, row_gate, stats, status);
+      static_cast<T*>(xp), tok_rows, row_token, row_gate, stats, status, RouterStatsArgs{});
   return cudaGetLastError();
 }
 
@@ -530,7 +531,7 @@ cudaError_t launch_permute(const Plan& p, const void* x, const int32_t* idx, con
 bool permute_fuses_offsets(const Plan& p) { return !p.ec && p.E * p.tiles <= 8192; }
 
 cudaError_t launch_combine(const Plan& p, const void* yp, const int32_t* tok_rows, const int32_t* tok_off,
-                           const void* ys, void* out, cudaStream_t st, void* ws, void* stats) {
+                           const void* ys, void* out, cudaStream_t st) {
   const int64_t blocks = ceil_div(p.N, kWarps) < 148 * 16 ? ceil_div(p.N, kWarps) : 148 * 16;
   const int64_t nchunk = p.d / (p.bf16 ? 8 : 4);
   int64_t slices = ceil_div(4 * 148, blocks);  // small batches: split rows so ~4 blocks per SM combine
@@ -538,21 +539,14 @@ cudaError_t launch_combine(const Plan& p, const void* yp, const int32_t* tok_row
   if (slices > max_slices) slices = max_slices;
   if (slices < 1) slices = 1;
   const dim3 grid((unsigned)blocks, (unsigned)slices);
-  RouterStatsArgs fin{};
-  if (ws && stats) {
-    fin.part_p = ws_at<float>(ws, p.part_p);
-    fin.part_cnt = ws_at<int32_t>(ws, p.part_cnt);
-    fin.part_lse = ws_at<float>(ws, p.part_lse);
-    fin.alpha = p.cfg.aux_alpha;
-  }
   if (p.bf16) {
     combine_kernel<__nv_bfloat16><<<grid, kWarps * 32, 0, st>>>(
         static_cast<const float*>(yp), tok_rows, p.ec ? tok_off : nullptr, static_cast<const float*>(ys), p.N, p.d,
-        p.k, static_cast<__nv_bfloat16*>(out), fin, p.E, p.cap, p.tiles, stats);
+        p.k, static_cast<__nv_bfloat16*>(out));
   } else {
     combine_kernel<float><<<grid, kWarps * 32, 0, st>>>(
         static_cast<const float*>(yp), tok_rows, p.ec ? tok_off : nullptr, static_cast<const float*>(ys), p.N, p.d,
-        p.k, static_cast<float*>(out), fin, p.E, p.cap, p.tiles, stats);
+        p.k, static_cast<float*>(out));
   }
   return cudaGetLastError();
 }

@@ -17,8 +17,9 @@
 // shuffles, then a butterfly over the rest) leaves lane l with the logit of
 // expert (l mod V). For more experts (bf16) the logits come from the
 // tensor-core GEMM (gemm_tc.cu). Each block writes its partial sums in a fixed
-// order, so the statistics are deterministic; they are reduced later (by the
-// permute's scan kernel, the combine kernel, or router_finalize_kernel).
+// order and adds them to fixed-point accumulators, so the statistics are
+// deterministic; a later kernel (the permute's, or router_finalize_kernel) turns
+// them into the statistics.
 #include <cfloat>
 
 #include "common.cuh"
@@ -53,9 +54,7 @@ struct RouterArgs {
   float* gate;
   float* logits;  // nullable
   float* probs;   // nullable
-  float* part_p;      // [E][blocks]
-  int32_t* part_cnt;  // [E][blocks]
-  float* part_lse;    // [blocks][2]
+  StatsAcc acc;       // fixed-point statistic accumulators (stats.cuh)
   int32_t* tile_counts;  // [E][blocks] per-tile assignment counts for the permute, or null
   int32_t* status;
   int64_t N, d, E, k, cap, tile;
@@ -273,8 +272,8 @@ __global__ void __launch_bounds__(kRouterWarps * 32) router_kernel(RouterArgs a)
   for (int64_t e = threadIdx.x; e < E; e += blockDim.x) {
     float acc = 0.f;
     for (int w = 0; w < kRouterWarps; ++w) acc += sPall[w * E + e];
-    a.part_p[e * gridDim.x + blockIdx.x] = acc;
-    a.part_cnt[e * gridDim.x + blockIdx.x] = sCnt[e];
+    atomicAdd(a.acc.p + e, to_fixed((double)acc, kPScale));
+    if (sCnt[e]) atomicAdd(a.acc.cnt + e, sCnt[e]);
     if (a.tile_counts) a.tile_counts[e * gridDim.x + blockIdx.x] = sCnt[e];
   }
   if (threadIdx.x == 0) {
@@ -283,18 +282,16 @@ __global__ void __launch_bounds__(kRouterWarps * 32) router_kernel(RouterArgs a)
       s0 += sLse[w][0];
       s1 += sLse[w][1];
     }
-    a.part_lse[blockIdx.x * 2 + 0] = s0;
-    a.part_lse[blockIdx.x * 2 + 1] = s1;
+    atomicAdd(a.acc.lse, to_fixed((double)s0, kLseScale));
+    atomicAdd(a.acc.lse + 1, to_fixed((double)s1, kLse2Scale));
   }
 }
 
 }  // namespace
 
-__global__ void __launch_bounds__(512) router_finalize_kernel(const float* part_p, const int32_t* part_cnt,
-                                                              const float* part_lse, int64_t blocks, int64_t N,
-                                                              int64_t E, int64_t k, int64_t cap, int ec,
-                                                              float alpha, void* stats) {
-  finalize_router_stats(part_p, part_cnt, part_lse, blocks, N, E, k, cap, ec, alpha, stats);
+__global__ void __launch_bounds__(512) router_finalize_kernel(StatsAcc acc, int64_t N, int64_t E, int64_t k,
+                                                              int64_t cap, int ec, float alpha, void* stats) {
+  finalize_router_stats(acc, N, E, k, cap, ec, alpha, stats);
 }
 
 namespace {
@@ -364,9 +361,7 @@ cudaError_t launch_router(const Plan& p, const void* x, const moe_weights* w, in
   a.gate = gate;
   a.logits = logits;
   a.probs = probs;
-  a.part_p = ws_at<float>(ws, p.part_p);
-  a.part_cnt = ws_at<int32_t>(ws, p.part_cnt);
-  a.part_lse = ws_at<float>(ws, p.part_lse);
+  a.acc = stats_acc_at(ws_at<uint8_t>(ws, p.stat_acc), p.E);
   a.tile_counts = tile_counts;
   a.status = status_ptr(p, ws);
   a.N = p.N;
@@ -389,8 +384,7 @@ cudaError_t launch_router(const Plan& p, const void* x, const moe_weights* w, in
   }
   if (err != cudaSuccess) return err;
   if (finalize) {
-    router_finalize_kernel<<<1, 512, 0, st>>>(a.part_p, a.part_cnt, a.part_lse, p.tiles, p.N, p.E, p.k, p.cap,
-                                              p.ec ? 1 : 0, p.cfg.aux_alpha, stats);
+    router_finalize_kernel<<<1, 512, 0, st>>>(a.acc, p.N, p.E, p.k, p.cap, p.ec ? 1 : 0, p.cfg.aux_alpha, stats);
   }
   return cudaGetLastError();
 }

@@ -1,8 +1,15 @@
-// Router statistics from per-block partial sums, reduced by one thread block in
-// a fixed order (fp64), so the result does not depend on scheduling.
-//   f_e = count_e / total assignments (token choice: before dropping; expert
-//         choice: C per expert), P_e = mean_t p[t,e],
-//   aux = alpha * E * sum_e f_e P_e, z = (mean_t lse_t)^2, mean_lse_sq = mean_t lse_t^2.
+// Router statistics, accumulated in fixed point so the totals do not depend on
+// the order in which blocks finish (integer addition is associative):
+//   P_sum[e]  = sum_t p[t,e]         int64, units of 2^-40
+//   cnt[e]    = assignments to e     int32
+//   lse_sum   = sum_t lse_t          int64, units of 2^-32 (|lse| < 2^16 assumed)
+//   lse2_sum  = sum_t lse_t^2        int64, units of 2^-24
+// Each router block adds its fp32 block partials (summed over its tokens in a
+// fixed order) once. The finaliser computes
+//   f_e = cnt_e / total assignments (token choice: before dropping; expert
+//         choice: C per expert), P_e = P_sum[e] / N,
+//   aux = alpha * E * sum_e f_e P_e, z = (lse_sum / N)^2, mean_lse_sq = lse2_sum / N,
+// writes the statistics and zeroes the accumulators for the next call.
 // Pages: "Mixture of Experts" (aigrafen.se) auxiliary loss; "Mixture of Experts
 // (MoE)" (learn.starphix.com) "Load Balancing (Critical)" (load_balancing_loss, z_loss).
 #pragma once
@@ -11,8 +18,35 @@
 
 namespace moe {
 
-// Block-wide sum of a double in a fixed order (warp shuffles, then warp 0 over
-// the per-warp sums). Every thread of the block must call it; all get the sum.
+constexpr double kPScale = 1099511627776.0;  // 2^40
+constexpr double kLseScale = 4294967296.0;   // 2^32
+constexpr double kLse2Scale = 16777216.0;    // 2^24
+
+// Accumulator layout (bytes): [P_sum: E x int64][lse_sum, lse2_sum: 2 x int64][cnt: E x int32]
+inline __host__ __device__ size_t stats_acc_bytes(int64_t E) { return (size_t)E * 12 + 16; }
+
+struct StatsAcc {
+  unsigned long long* p;    // [E]
+  unsigned long long* lse;  // [2]
+  int32_t* cnt;             // [E]
+};
+__host__ __device__ inline StatsAcc stats_acc_at(void* base, int64_t E) {
+  StatsAcc a;
+  a.p = static_cast<unsigned long long*>(base);
+  a.lse = a.p + E;
+  a.cnt = reinterpret_cast<int32_t*>(a.lse + 2);
+  return a;
+}
+
+__device__ inline unsigned long long to_fixed(double v, double scale) {
+  return static_cast<unsigned long long>(__double2ll_rn(v * scale));
+}
+__device__ inline double from_fixed(unsigned long long v, double scale) {
+  return static_cast<double>(static_cast<long long>(v)) / scale;
+}
+
+// Block-wide sum of a double in a fixed order (warp shuffles, then the per-warp
+// sums in order). Every thread of the block must call it; all get the sum.
 __device__ inline double block_sum_fixed(double v, double* s_warp /* >= 32 */) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
 #pragma unroll
@@ -26,55 +60,41 @@ __device__ inline double block_sum_fixed(double v, double* s_warp /* >= 32 */) {
   return t;
 }
 
-// part_p / part_cnt are [E][blocks], part_lse is [blocks][2].
-__device__ inline void finalize_router_stats(const float* part_p, const int32_t* part_cnt, const float* part_lse,
-                                             int64_t blocks, int64_t N, int64_t E, int64_t k, int64_t cap, int ec,
+// Whole block: statistics from the accumulators, then the accumulators are zeroed.
+__device__ inline void finalize_router_stats(StatsAcc acc, int64_t N, int64_t E, int64_t k, int64_t cap, int ec,
                                              float alpha, void* stats) {
   __shared__ double s_warp[32];
   moe_stats_header* hdr = static_cast<moe_stats_header*>(stats);
   float* f_out = reinterpret_cast<float*>(hdr + 1);
   float* P_out = f_out + E;
   int32_t* cnt_out = reinterpret_cast<int32_t*>(P_out + E);
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
   const double total = ec ? (double)E * (double)cap : (double)N * (double)k;
   double aux_part = 0.0;
-  for (int64_t e = warp; e < E; e += nwarps) {
-    double P = 0.0;
-    long long cnt = 0;
-#pragma unroll 4
-    for (int64_t b = lane; b < blocks; b += 32) {
-      P += part_p[e * blocks + b];
-      cnt += part_cnt[e * blocks + b];
-    }
-#pragma unroll
-    for (int s = 16; s >= 1; s >>= 1) {
-      P += __shfl_xor_sync(kFull, P, s);
-      cnt += __shfl_xor_sync(kFull, cnt, s);
-    }
-    if (ec) cnt = cap;
-    P /= (double)N;
+  for (int64_t e = threadIdx.x; e < E; e += blockDim.x) {
+    const double P = from_fixed(*((volatile unsigned long long*)(acc.p + e)), kPScale) / (double)N;
+    const int32_t cnt = ec ? (int32_t)cap : *((volatile int32_t*)(acc.cnt + e));
     const double f = total > 0 ? (double)cnt / total : 0.0;
-    if (lane == 0) {
-      f_out[e] = (float)f;
-      P_out[e] = (float)P;
-      cnt_out[e] = (int32_t)cnt;
-      aux_part += f * P;
-    }
-  }
-  double l0 = 0.0, l1 = 0.0;
-  for (int64_t b = threadIdx.x; b < blocks; b += blockDim.x) {
-    l0 += part_lse[2 * b];
-    l1 += part_lse[2 * b + 1];
+    f_out[e] = (float)f;
+    P_out[e] = (float)P;
+    cnt_out[e] = cnt;
+    aux_part += f * P;
   }
   const double aux = block_sum_fixed(aux_part, s_warp);
-  const double ls = block_sum_fixed(l0, s_warp);
-  const double ls2 = block_sum_fixed(l1, s_warp);
   if (threadIdx.x == 0) {
-    const double ml = ls / (double)N;
+    const double ml = from_fixed(*((volatile unsigned long long*)(acc.lse)), kLseScale) / (double)N;
     hdr->aux_loss = (float)((double)alpha * (double)E * aux);
     hdr->z_loss = (float)(ml * ml);
-    hdr->mean_lse_sq = (float)(ls2 / (double)N);
+    hdr->mean_lse_sq = (float)(from_fixed(*((volatile unsigned long long*)(acc.lse + 1)), kLse2Scale) / (double)N);
     hdr->n_experts = (int32_t)E;
+  }
+  __syncthreads();  // every read above is done before the reset
+  for (int64_t e = threadIdx.x; e < E; e += blockDim.x) {
+    acc.p[e] = 0ull;
+    acc.cnt[e] = 0;
+  }
+  if (threadIdx.x == 0) {
+    acc.lse[0] = 0ull;
+    acc.lse[1] = 0ull;
   }
 }
 

@@ -57,8 +57,8 @@ def test_noalloc_matches_route(w):
 
 
 def test_noalloc_rejects_layers_beyond_its_scratch():
-    """16 * E * T + 288 bytes (T token tiles) must fit in the 4 MiB array; checked before any launch."""
-    w = Workload("na_too_big", 1 << 20, 64, 64, 256, 8, 0.0, "softmax_topk", "gelu", "bf16")
+    """The 4 KiB scratch holds the accumulators of at most 318 experts; checked before any launch."""
+    w = Workload("na_too_big", 4096, 64, 64, 320, 8, 0.0, "softmax_topk", "gelu", "bf16")
     cfg = moe.config(w)
     fake = torch.empty(0)
     lib = moe._lib
