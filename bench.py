@@ -112,6 +112,28 @@ def measured_traffic(workload: str, kernel: str):
     return rec.get("traffic_bytes_up" if kernel == "up" else "traffic_bytes_down")
 
 
+def max_over_ranks(value: float, device=None) -> float:
+    """The largest of every rank's value (a single process returns its own)."""
+    import torch.distributed as td
+    if not (td.is_available() and td.is_initialized()) or td.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    td.all_reduce(t, op=td.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(tokens_per_rank: int, steps: int, world: int, max_ms: float) -> float:
+    """Whole-job throughput: every rank's tokens over the slowest rank's time (weak scaling)."""
+    return tokens_per_rank * steps * world / (max_ms / 1e3)
+
+
+def rank_inputs(w, rank: int, device):
+    """A data-parallel rank's inputs: the replicated weights (seed of the workload) and a
+    batch of its own (seed of the workload + rank)."""
+    import sparse_expert_ffn_softmax_b300 as moe
+    return moe.make_inputs(w, device, x_seed=w.seed + rank)
+
+
 def algorithmic(w, rows, touched):
     """Algorithmic FLOPs / bytes per forward (kept rows only, each operand once)."""
     b = 4 if w.dtype == "f32" else 2
@@ -211,7 +233,7 @@ def main():
         import torch.distributed as td
         td.init_process_group("nccl", device_id=dev)
 
-    t = moe.make_inputs(w, dev)
+    t = rank_inputs(w, rank, dev)
     layer = moe.Layer(w, t, device=dev)
     x = t["x"]
     out = torch.empty_like(x)
@@ -242,11 +264,8 @@ def main():
             stage_ms += np.array(times)
             step_ms.append(ev[0].elapsed_time(ev[5]))
         torch.cuda.synchronize(dev)
-    total_ms = float(np.sum(step_ms))
+    total_ms = max_over_ranks(float(np.sum(step_ms)), dev)
     if dist:
-        tt = torch.tensor([total_ms], device=dev)
-        td.all_reduce(tt, op=td.ReduceOp.MAX)
-        total_ms = float(tt.item())
         td.barrier()
     code, word = moe.get_device_status(layer.cfg, layer.ws)
     if code != 0:
@@ -272,10 +291,7 @@ def main():
         e1.record()
         e1.synchronize()
         e2e_ms += e0.elapsed_time(e1)
-    if dist:
-        tt = torch.tensor([e2e_ms], device=dev)
-        td.all_reduce(tt, op=td.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
+    e2e_ms = max_over_ranks(e2e_ms, dev)
     clk.__exit__(None, None, None)
 
     st = layer.read_stats()
@@ -290,8 +306,8 @@ def main():
     flops = alg["up_flops"] if gi == 2 else alg["down_flops"]
     dom_s = stage_avg[gi] / 1e3
     achieved_tflops = flops / dom_s / 1e12
-    value = w.n_tokens * args.steps * world / (total_ms / 1e3)
-    e2e_value = w.n_tokens * args.steps * world / (e2e_ms / 1e3)
+    value = job_tokens_per_s(w.n_tokens, args.steps, world, total_ms)
+    e2e_value = job_tokens_per_s(w.n_tokens, args.steps, world, e2e_ms)
     b = 4 if w.dtype == "f32" else 2
     line = {
         "metric": METRIC,

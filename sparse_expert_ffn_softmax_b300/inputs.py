@@ -115,8 +115,12 @@ def normal(name: str, shape, std: float, dtype: torch.dtype, device, seed: int =
     return out
 
 
-def make_inputs(w: Workload, device="cpu", with_weights: bool = True) -> Dict[str, Optional[torch.Tensor]]:
+def make_inputs(w: Workload, device="cpu", with_weights: bool = True,
+                x_seed: Optional[int] = None) -> Dict[str, Optional[torch.Tensor]]:
     """Tokens ``x [N, d]`` and the layer's weights, in nn.Linear ``[out, in]`` layout.
+
+    ``x_seed`` draws the tokens from another seed than the weights (data-parallel
+    ranks: replicated weights, a batch of their own).
 
     Keys: x, w_router [E,d], logit_bias [E] fp32 or None, w1/w3 [E,F,d], b1 [E,F],
     w2 [E,d,F], b2 [E,d], ws1/ws3 [S,Fs,d], bs1 [S,Fs], ws2 [S,d,Fs], bs2 [S,d].
@@ -125,7 +129,7 @@ def make_inputs(w: Workload, device="cpu", with_weights: bool = True) -> Dict[st
     dt = w.torch_dtype
     N, d, F, E, S, Fs = w.n_tokens, w.d_model, w.d_ff, w.n_experts, w.n_shared, w.d_ff_shared
     out: Dict[str, Optional[torch.Tensor]] = {}
-    out["x"] = normal("x", (N, d), 1.0, dt, device, w.seed)
+    out["x"] = normal("x", (N, d), 1.0, dt, device, w.seed if x_seed is None else x_seed)
     if not with_weights:
         return out
     out["w_router"] = normal("w_router", (E, d), 1.0 / math.sqrt(d), dt, device, w.seed)
