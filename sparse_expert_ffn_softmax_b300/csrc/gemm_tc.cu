@@ -58,7 +58,7 @@ struct Family {
   int32_t b_rows_group; // B-map row offset of group g: g * b_rows_group
   int32_t b_rows_kseg;  // B-map row offset of K segment s: s * b_rows_kseg
   int32_t a_map, b_map, b3_map;
-  int32_t pad0;
+  int32_t k_group;      // K-block offset of group g: g * k_group (split-K groups), else 0
   void* out;
   int64_t ld_out;         // elements between output rows
   int64_t out_col_group;  // output column offset of group g: g * out_col_group
@@ -420,6 +420,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const CUtensorMap* ma = pick_map(F.a_map, m0, m1, m2, m3, m4, m5);
         const CUtensorMap* mb = pick_map(F.b_map, m0, m1, m2, m3, m4, m5);
         const CUtensorMap* mb3 = pick_map(F.b3_map, m0, m1, m2, m3, m4, m5);
+        const int k0 = ti.g * F.k_group;  // split-K groups start further along K
         for (int kb = 0; kb < F.k_blocks; ++kb) {
           if (!mbar_wait<false>(&empty_bar[stage], phase ^ 1u, abort_flag)) {
             ok = false;
@@ -427,9 +428,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           mbar_arrive_expect_tx(&full_bar[stage], C::kStageBytes);
           last_parity[stage] = (int32_t)phase;
-          tma_load_2d(ma, &full_bar[stage], sA + stage * C::kABytes, kb * BK, ti.a_row0);
+          tma_load_2d(ma, &full_bar[stage], sA + stage * C::kABytes, (k0 + kb) * BK, ti.a_row0);
           const int kseg = kb / F.kseg_blocks;
-          const int kin = kb - kseg * F.kseg_blocks;
+          const int kin = k0 + kb - kseg * F.kseg_blocks;
           if (EPI == kSwiglu) {
             const int by = ti.g * F.b_rows_group + kseg * F.b_rows_kseg + ti.nt * (BN / 2);
             tma_load_2d(mb, &full_bar[stage], sB + stage * C::kBBytes, kin * BK, by);
@@ -777,32 +778,39 @@ int pick_bn(bool swiglu, int64_t c0, int64_t c1) {
 
 bool tc_gemm_available() { return tc::encode_fn() != nullptr; }
 
-// Router logits on the tensor cores: one group of N token rows against the E
-// router rows (zero-filled past E by the tensor map), fp32 output + logit bias.
+// Router logits on the tensor cores: N token rows against the E router rows
+// (zero-filled past E by the tensor map), fp32 out. splits = 1: logits + bias into
+// `out` [N, E]. splits > 1: the K range is cut into `splits` groups of equal
+// length, group g writing its partial sums (no bias) to slab g of `out`
+// ([splits][N][E]); the routing kernel adds the slabs in order and the bias.
 cudaError_t launch_router_logits_tc(const Plan& p, const void* x, const void* w_router, const float* logit_bias,
-                                    float* logits, int32_t* status, cudaStream_t st) {
+                                    float* out, int splits, int32_t* status, cudaStream_t st) {
   using namespace tc;
   const int bn = p.E <= 64 ? 64 : (p.E <= 128 ? 128 : 256);
+  const int64_t kb = p.d / BK;
+  if (splits < 1 || kb % splits) return cudaErrorInvalidValue;
   CUtensorMap maps[8];
   if (!make_map(&maps[0], x, p.N, p.d, BM)) return cudaErrorInvalidValue;
   if (!make_map(&maps[1], w_router, p.E, p.d, bn)) return cudaErrorInvalidValue;
   for (int i = 2; i < 8; ++i) maps[i] = maps[0];
   Params P{};
   Family& f0 = P.fam[0];
-  f0.groups = 1;
+  f0.groups = splits;
   f0.m_fixed = (int32_t)p.N;
   f0.n_tiles = (int32_t)ceil_div(p.E, bn);
-  f0.k_blocks = f0.kseg_blocks = (int32_t)(p.d / BK);
+  f0.k_blocks = f0.kseg_blocks = (int32_t)(kb / splits);
+  f0.k_group = (int32_t)(kb / splits);
   f0.a_map = 0;
   f0.b_map = 1;
   f0.b3_map = 1;
-  f0.out = logits;
+  f0.out = out;
   f0.ld_out = p.E;
-  f0.bias_f32 = logit_bias;
+  f0.out_col_group = p.N * p.E;  // slab g
+  f0.bias_f32 = splits == 1 ? logit_bias : nullptr;
   f0.n_valid = p.E;
   P.expert_off = nullptr;
   P.status = status;
-  return launch_bn<kLogits>(bn, maps, P, ceil_div(p.N, BM) * f0.n_tiles, st);
+  return launch_bn<kLogits>(bn, maps, P, ceil_div(p.N, BM) * f0.n_tiles * splits, st);
 }
 
 // part: bit 0 = up-projections (routed + shared), bit 1 = down-projections.

@@ -26,8 +26,17 @@ struct Plan {
   size_t stat_acc;                    // fixed-point router statistic accumulators (stats.cuh)
   size_t tile_counts, tile_base;      // permute [E][T], [E][T+1]
   size_t ec_bits;                     // [N][words]
-  size_t logits_raw;                  // unused for now
+  int64_t rsplit;                     // bf16 router GEMM split along K into this many groups (1: none)
+  size_t logits_part;                 // [rsplit][N][E] fp32 partial logits when rsplit > 1
 };
+
+// K groups of the bf16 logits GEMM (layers with more than 32 experts) for a batch
+// of N tokens, a function of the shapes alone: fewer than 16 128-token tiles with a
+// long K leave most SMs idle, so the K range is split until about one CTA per SM
+// runs (each keeping >= 4 K blocks).
+constexpr int64_t kRouterTcMinE = 33;        // bf16 layers with more experts route from tensor-core logits
+constexpr int64_t kRouterSplitMaxTiles = 16;  // K split only below this many 128-token tiles
+int64_t router_k_splits(int64_t N, int64_t d, int64_t E);
 
 moe_status make_plan(const moe_config* cfg, Plan* p);
 
@@ -46,6 +55,8 @@ inline T* ws_at(void* ws, size_t off) {
 cudaError_t launch_router(const Plan& p, const void* x, const moe_weights* w, int32_t* idx, float* gate,
                           float* logits, float* probs, void* stats, void* ws, cudaStream_t st,
                           int32_t* tile_counts, bool finalize);
+// True when the router writes the logits to memory before a second kernel reads
+// them (bf16 layers that the fused tensor-core router does not cover).
 bool router_uses_tc(const Plan& p);
 
 // permute.cu. Token choice needs per-tile expert counts and their prefix:
@@ -75,8 +86,10 @@ cudaError_t launch_ffn_bf16(const Plan& p, const void* xp, const int32_t* expert
                             const void* x, const moe_weights* w, void* h, void* hs, void* yp, void* ys,
                             int32_t* status, cudaStream_t st, int part);
 bool tc_gemm_available();
-// logits[N, E] = x W_r^T + logit_bias on the tensor cores (bf16 layers).
+// Router logits x W_r^T on the tensor cores (bf16 layers), fp32: splits = 1 writes
+// logits + logit_bias [N, E]; splits > 1 writes [splits][N][E] partial sums over
+// equal K ranges without the bias (splits divides d / 64).
 cudaError_t launch_router_logits_tc(const Plan& p, const void* x, const void* w_router, const float* logit_bias,
-                                    float* logits, int32_t* status, cudaStream_t st);
+                                    float* out, int splits, int32_t* status, cudaStream_t st);
 
 }  // namespace moe

@@ -103,10 +103,22 @@ moe_status make_plan(const moe_config* c, Plan* p) {
   p->tile_counts = take((size_t)(p->E * p->tiles) * 4);
   p->tile_base = take((size_t)(p->E * (p->tiles + 1)) * 4);
   p->ec_bits = take((size_t)(p->N * p->words) * 4);
+  p->rsplit = p->bf16 ? router_k_splits(p->N, p->d, p->E) : 1;
+  p->logits_part = take(p->rsplit > 1 ? (size_t)(p->rsplit * p->N * p->E) * 4 : 0);
   L.total_bytes = o;
   L.max_rows = p->max_rows;
   L.capacity = p->cap;
   return MOE_OK;
+}
+
+int64_t router_k_splits(int64_t N, int64_t d, int64_t E) {
+  constexpr int64_t kSms = 148, kBM = 128, kBK = 64, kMinBlocks = 4;
+  const int64_t kb = d / kBK, mt = (N + kBM - 1) / kBM;
+  if (N <= 0 || kb <= 0 || E < kRouterTcMinE || mt >= kRouterSplitMaxTiles) return 1;
+  int64_t s = kSms / mt;
+  if (s > kb / kMinBlocks) s = kb / kMinBlocks;
+  while (s > 1 && kb % s) --s;  // equal K ranges
+  return s > 2 ? s : 1;         // two halves do not pay for the extra pass over partial sums
 }
 
 namespace {

@@ -59,6 +59,7 @@ extern "C" MOE_API moe_status moe_route_noalloc(const moe_config* cfg, const voi
   moe_status s = make_plan(cfg, &p);
   if (s != MOE_OK) return s;
   if (!w || !x || !idx || !gate || !stats) return MOE_ERR_INVALID_ARG;
+  p.rsplit = 1;  // no workspace for partial logits
   if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(idx) | reinterpret_cast<uintptr_t>(gate) |
        reinterpret_cast<uintptr_t>(logits) | reinterpret_cast<uintptr_t>(probs) |
        reinterpret_cast<uintptr_t>(stats) | reinterpret_cast<uintptr_t>(w->w_router) |

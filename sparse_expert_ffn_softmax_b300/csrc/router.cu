@@ -49,7 +49,9 @@ struct RouterArgs {
   const void* x;
   const void* wr;
   const float* logit_bias;
-  const float* logits_in;  // non-null: logits already computed (bias included), fp32 [N, E]
+  const float* logits_in;  // non-null: fp32 logits [N, E] (bias included) or, splits > 1,
+                           // [splits][N, E] partial sums without the bias
+  int64_t splits, part_stride;  // slabs of logits_in and the elements between them
   int32_t* idx;
   float* gate;
   float* logits;  // nullable
@@ -119,7 +121,17 @@ __global__ void __launch_bounds__(kRouterWarps * 32) router_kernel(RouterArgs a)
 #pragma unroll
       for (int i = 0; i < EPL; ++i) {
         const int64_t e = lane + 32 * i;
-        Lr[i] = e < E ? a.logits_in[t * E + e] : -FLT_MAX;
+        float acc = 0.f;
+        if (e < E) {
+          const float* src = a.logits_in + t * E + e;
+          if (a.splits == 1) {
+            acc = src[0];  // bias included
+          } else {
+            for (int64_t sp = 0; sp < a.splits; ++sp) acc += src[sp * a.part_stride];  // slabs in order
+            if (a.logit_bias) acc += a.logit_bias[e];
+          }
+        }
+        Lr[i] = e < E ? acc : -FLT_MAX;
       }
     } else {
       const uint4* xrow = static_cast<const uint4*>(a.x) + t * nchunk;
@@ -198,7 +210,7 @@ __global__ void __launch_bounds__(kRouterWarps * 32) router_kernel(RouterArgs a)
         const float pe = ex[i] * inv_s;
         pacc[i] += pe;
         if (a.probs) a.probs[t * E + e] = pe;
-        if (a.logits && !kLogitsIn) a.logits[t * E + e] = Lr[i];
+        if (a.logits) a.logits[t * E + e] = Lr[i];
       }
     }
     if (!ec) {
@@ -314,13 +326,21 @@ cudaError_t launch_router_w(const Plan& p, RouterArgs a, cudaStream_t st) {
              : launch_router_t<T, V, CPL, EPL, false, false>(p, a, st);
 }
 
+// CPL: 16-byte chunks of the token row each lane holds at once (the loop over
+// the row covers any d). Layers with more than 64 experts, whose unrolled dot
+// products are long already, take the shortest, which keeps the number of
+// instantiations (and the build time) small.
 template <typename T, int V, int EPL>
 cudaError_t launch_router_c(const Plan& p, RouterArgs a, cudaStream_t st) {
   const int64_t cpl = ceil_div(p.d / (16 / (int64_t)sizeof(T)), 32);
-  if (cpl <= 2) return launch_router_w<T, V, 2, EPL>(p, a, st);
-  if (cpl <= 4) return launch_router_w<T, V, 4, EPL>(p, a, st);
-  if (cpl <= 8) return launch_router_w<T, V, 8, EPL>(p, a, st);
-  return launch_router_w<T, V, 16, EPL>(p, a, st);
+  if constexpr (EPL > 2) {
+    return launch_router_w<T, V, 2, EPL>(p, a, st);
+  } else {
+    if (cpl <= 2) return launch_router_w<T, V, 2, EPL>(p, a, st);
+    if (cpl <= 4) return launch_router_w<T, V, 4, EPL>(p, a, st);
+    if (cpl <= 8) return launch_router_w<T, V, 8, EPL>(p, a, st);
+    return launch_router_w<T, V, 16, EPL>(p, a, st);
+  }
 }
 
 template <typename T>
@@ -337,17 +357,24 @@ cudaError_t launch_router_simt(const Plan& p, RouterArgs a, cudaStream_t st) {
   if (p.E <= 8) return launch_router_c<T, 8, 1>(p, a, st);
   if (p.E <= 16) return launch_router_c<T, 16, 1>(p, a, st);
   if (p.E <= 32) return launch_router_c<T, 32, 1>(p, a, st);
-  if (p.E <= 64) return launch_router_c<T, 32, 2>(p, a, st);
-  if (p.E <= 128) return launch_router_c<T, 32, 4>(p, a, st);
-  if (p.E <= 256) return launch_router_c<T, 32, 8>(p, a, st);
-  return launch_router_c<T, 32, 16>(p, a, st);
+  if constexpr (sizeof(T) == 2) {
+    return cudaErrorInvalidValue;  // bf16 layers with E > 32 route from tensor-core logits
+  } else {
+    if (p.E <= 64) return launch_router_c<T, 32, 2>(p, a, st);
+    if (p.E <= 128) return launch_router_c<T, 32, 4>(p, a, st);
+    if (p.E <= 256) return launch_router_c<T, 32, 8>(p, a, st);
+    return launch_router_c<T, 32, 16>(p, a, st);
+  }
 }
 
 }  // namespace
 
-// Router on the tensor cores for many experts: logits = x W_r^T + bias by the
-// grouped GEMM (gemm_tc.cu), then the softmax / top-k kernel reads them.
-bool router_uses_tc(const Plan& p) { return p.bf16 && p.E > 32; }
+// Router per layer shape:
+//  - bf16 with more than 32 experts: the tensor cores write the logits (K split
+//    for small batches, router_k_splits), then this file's kernel routes;
+//  - fp32 layers and bf16 layers with up to 32 experts: the SIMT router (dot
+//    products on the CUDA cores, one warp per token).
+bool router_uses_tc(const Plan& p) { return p.bf16 && p.E >= kRouterTcMinE; }
 
 cudaError_t launch_router(const Plan& p, const void* x, const moe_weights* w, int32_t* idx, float* gate,
                           float* logits, float* probs, void* stats, void* ws, cudaStream_t st,
@@ -374,11 +401,17 @@ cudaError_t launch_router(const Plan& p, const void* x, const moe_weights* w, in
   a.alpha = p.cfg.aux_alpha;
   cudaError_t err;
   if (router_uses_tc(p)) {
+    // partial logits (K split) in the workspace, else the logits themselves
+    const bool split = p.rsplit > 1;
     float* lg = logits ? logits : ws_at<float>(ws, p.L.logits);
-    err = launch_router_logits_tc(p, x, w->w_router, w->logit_bias, lg, a.status, st);
+    float* part = split ? ws_at<float>(ws, p.logits_part) : lg;
+    err = launch_router_logits_tc(p, x, w->w_router, w->logit_bias, part, (int)p.rsplit, a.status, st);
     if (err != cudaSuccess) return err;
-    a.logits_in = lg;
-    err = p.bf16 ? launch_router_logits_in<__nv_bfloat16>(p, a, st) : launch_router_logits_in<float>(p, a, st);
+    a.logits_in = part;
+    a.splits = p.rsplit;
+    a.part_stride = p.N * p.E;
+    a.logits = split ? logits : nullptr;  // unsplit: the GEMM wrote the logits (bias included)
+    err = launch_router_logits_in<__nv_bfloat16>(p, a, st);
   } else {
     err = p.bf16 ? launch_router_simt<__nv_bfloat16>(p, a, st) : launch_router_simt<float>(p, a, st);
   }
