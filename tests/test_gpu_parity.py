@@ -2,9 +2,8 @@
 
 Small layers are compared in full; they span several 128-row GEMM tiles, a
 ragged last tile, every gate rule, drops, shared experts, GELU and SwiGLU, fp32
-and bf16, the tile widths 64/128/256, and the three routers (routing fused into
-the tensor-core router GEMM, tensor-core logits with a routing kernel, the SIMT
-router). The workload shapes themselves run at
+and bf16, the tile widths 64/128/256, and both routers (SIMT dot products;
+tensor-core logits, whole or split along K, with the routing kernel). The workload shapes themselves run at
 full size with routing compared on every token and outputs on sampled tokens.
 """
 import numpy as np
@@ -48,13 +47,13 @@ SMALL = [
        act="swiglu", n_shared=2, d_ff_shared=128, logit_bias_max=2.0),
     wl("bf16_heavy_drops", n_tokens=1000, d_model=64, d_ff=128, n_experts=8, top_k=2, capacity_factor=0.3,
        logit_bias_max=4.0),
-    # routing in the router GEMM's epilogue (E <= 32 and >= 16 token tiles): top-2,
-    # top-5 of 32 experts with a logit offset, expert choice
-    wl("bf16_fused_route_B", n_tokens=2100, d_model=128, d_ff=64, n_experts=8, top_k=2, capacity_factor=1.25,
+    # 16+ token tiles (the router's tile counts and the permute's fused offsets over
+    # many blocks): top-2, top-5 of 32 experts with a logit offset, expert choice
+    wl("bf16_2k_tokens_B", n_tokens=2100, d_model=128, d_ff=64, n_experts=8, top_k=2, capacity_factor=1.25,
        gating="topk_softmax", has_bias=True),
-    wl("bf16_fused_route_k5", n_tokens=2049, d_model=64, d_ff=64, n_experts=32, top_k=5, capacity_factor=1.0,
+    wl("bf16_2k_tokens_k5", n_tokens=2049, d_model=64, d_ff=64, n_experts=32, top_k=5, capacity_factor=1.0,
        gating="softmax_topk_renorm", act="swiglu", logit_bias_max=1.0),
-    wl("bf16_fused_route_ec", n_tokens=2048, d_model=64, d_ff=64, n_experts=12, top_k=2, capacity_factor=1.0,
+    wl("bf16_2k_tokens_ec", n_tokens=2048, d_model=64, d_ff=64, n_experts=12, top_k=2, capacity_factor=1.0,
        gating="expert_choice", act="swiglu", n_shared=1, d_ff_shared=64),
     # tensor-core logits + routing kernel for many experts, with a column count that
     # is not a multiple of 4 and partly filled column chunks
