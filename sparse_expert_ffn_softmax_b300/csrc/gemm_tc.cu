@@ -263,8 +263,8 @@ __device__ __forceinline__ float rcp_ftz(float x) {
 // z >= 0, |error| <= 1.5e-7 -- far below the bf16 rounding of the stored result.
 // Substituting z = s / sqrt(log2 e) with s = |u| sqrt(log2(e) / 2) gives
 // exp(-z^2) = 2^(-s^2) and t = 1 / (1 + p' s), p' = p / sqrt(log2 e); the
-// polynomial coefficients carry the factor 1/2 of Phi. Branch-free:
-// u >= 0 gives u - u q/2, u < 0 gives u q/2.
+// polynomial coefficients carry the factor 1/2 of Phi. Since Phi(-|u|) = q/2,
+// GELU(u) = max(u, 0) - |u| q / 2 for either sign of u (no select).
 __device__ __forceinline__ float gelu_as7126(float u) {
   constexpr float kS = 0.8493218002880191f;  // sqrt(log2(e) / 2)
   constexpr float kP = 0.2727374808792225f;  // 0.3275911 / sqrt(log2 e)
@@ -276,8 +276,8 @@ __device__ __forceinline__ float gelu_as7126(float u) {
   poly = fmaf(poly, t, kA3);
   poly = fmaf(poly, t, kA2);
   poly = fmaf(poly, t, kA1);
-  const float hq = u * (poly * t) * ex2_ftz(-s * s);  // u q / 2
-  return u >= 0.f ? u - hq : hq;
+  const float hq = (poly * t) * ex2_ftz(-s * s);  // q / 2
+  return fmaf(-fabsf(u), hq, fmaxf(u, 0.f));
 }
 
 template <int BN>

@@ -398,7 +398,9 @@ __global__ void __launch_bounds__(kWarps * 32) copy_rows_csr_kernel(const T* __r
 
 // out[t] = ys[t] + sum of yp over t's rows in list order: fp32 inputs, fp32
 // accumulation, one rounding to the output type. A lane owns 16 output bytes.
-template <typename TO>
+// The first KU rows of a token are loaded together (all loads in flight before
+// the first add); rows past KU follow one at a time. Same order of additions.
+template <typename TO, int KU>
 __global__ void __launch_bounds__(kWarps * 32) combine_kernel(const float* __restrict__ yp,
                                                               const int32_t* __restrict__ tok_rows,
                                                               const int32_t* __restrict__ tok_off,
@@ -433,7 +435,26 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(const float* __res
 #pragma unroll
         for (int q = 0; q < NV; ++q) Vec16<float>::unpack(__ldg(src + q), acc + 4 * q);
       }
-      for (int64_t j = 0; j < n; ++j) {
+      {
+        float v[KU][VN];
+#pragma unroll
+        for (int j = 0; j < KU; ++j) {
+          const int32_t row = __shfl_sync(kFull, my_row, j);
+          if (act && j < n && row >= 0) {
+            const uint4* src = reinterpret_cast<const uint4*>(yp + (int64_t)row * d + c * VN);
+#pragma unroll
+            for (int q = 0; q < NV; ++q) Vec16<float>::unpack(__ldg(src + q), v[j] + 4 * q);
+          } else {
+#pragma unroll
+            for (int i = 0; i < VN; ++i) v[j][i] = -0.f;  // x + (-0) == x for every x, signed zeros included
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < KU; ++j)
+#pragma unroll
+          for (int i = 0; i < VN; ++i) acc[i] += v[j][i];
+      }
+      for (int64_t j = KU; j < n; ++j) {
         const int32_t row = j < 32 ? __shfl_sync(kFull, my_row, (int)j) : tok_rows[beg + j];
         if (act && row >= 0) {
           const uint4* src = reinterpret_cast<const uint4*>(yp + (int64_t)row * d + c * VN);
@@ -539,14 +560,23 @@ cudaError_t launch_combine(const Plan& p, const void* yp, const int32_t* tok_row
   if (slices > max_slices) slices = max_slices;
   if (slices < 1) slices = 1;
   const dim3 grid((unsigned)blocks, (unsigned)slices);
+  const int32_t* toff = p.ec ? tok_off : nullptr;
+  const float* ysf = static_cast<const float*>(ys);
+  const float* ypf = static_cast<const float*>(yp);
+  // rows loaded together: top-k's k (expert choice: a token has up to E rows, 2 on average for cf 1)
+  const int64_t ku = p.ec ? 2 : p.k;
   if (p.bf16) {
-    combine_kernel<__nv_bfloat16><<<grid, kWarps * 32, 0, st>>>(
-        static_cast<const float*>(yp), tok_rows, p.ec ? tok_off : nullptr, static_cast<const float*>(ys), p.N, p.d,
-        p.k, static_cast<__nv_bfloat16*>(out));
+    __nv_bfloat16* o = static_cast<__nv_bfloat16*>(out);
+    if (ku <= 1) combine_kernel<__nv_bfloat16, 1><<<grid, kWarps * 32, 0, st>>>(ypf, tok_rows, toff, ysf, p.N, p.d, p.k, o);
+    else if (ku <= 2) combine_kernel<__nv_bfloat16, 2><<<grid, kWarps * 32, 0, st>>>(ypf, tok_rows, toff, ysf, p.N, p.d, p.k, o);
+    else if (ku <= 4) combine_kernel<__nv_bfloat16, 4><<<grid, kWarps * 32, 0, st>>>(ypf, tok_rows, toff, ysf, p.N, p.d, p.k, o);
+    else combine_kernel<__nv_bfloat16, 8><<<grid, kWarps * 32, 0, st>>>(ypf, tok_rows, toff, ysf, p.N, p.d, p.k, o);
   } else {
-    combine_kernel<float><<<grid, kWarps * 32, 0, st>>>(
-        static_cast<const float*>(yp), tok_rows, p.ec ? tok_off : nullptr, static_cast<const float*>(ys), p.N, p.d,
-        p.k, static_cast<float*>(out));
+    float* o = static_cast<float*>(out);
+    if (ku <= 1) combine_kernel<float, 1><<<grid, kWarps * 32, 0, st>>>(ypf, tok_rows, toff, ysf, p.N, p.d, p.k, o);
+    else if (ku <= 2) combine_kernel<float, 2><<<grid, kWarps * 32, 0, st>>>(ypf, tok_rows, toff, ysf, p.N, p.d, p.k, o);
+    else if (ku <= 4) combine_kernel<float, 4><<<grid, kWarps * 32, 0, st>>>(ypf, tok_rows, toff, ysf, p.N, p.d, p.k, o);
+    else combine_kernel<float, 8><<<grid, kWarps * 32, 0, st>>>(ypf, tok_rows, toff, ysf, p.N, p.d, p.k, o);
   }
   return cudaGetLastError();
 }
