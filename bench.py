@@ -334,8 +334,19 @@ def main():
     # dominant kernel: the larger of the two grouped-GEMM launches
     gi = 2 if stage_avg[2] >= stage_avg[3] else 3
     flops = alg["up_flops"] if gi == 2 else alg["down_flops"]
+    gbytes = alg["up_bytes"] if gi == 2 else alg["down_bytes"]
     dom_s = stage_avg[gi] / 1e3
     achieved_tflops = flops / dom_s / 1e12
+    # bound: whichever roof takes longer at its peak (decode batches stream the weights: HBM)
+    hbm_bound = gbytes / (pk["hbm"] * 1e9) > flops / (pk["bf16"] * 1e12)
+    if hbm_bound:
+        roof = {"bound": "hbm", "achieved": gbytes / dom_s / 1e9, "peak": pk["hbm"], "unit": "GB/s",
+                "frac": gbytes / dom_s / 1e9 / pk["hbm"], "traffic": measured_traffic(w.name, "up" if gi == 2 else "down"),
+                "peak_source": f"{pk['source']} HBM copy"}
+    else:
+        roof = {"bound": "tensor", "achieved": achieved_tflops, "peak": pk["bf16"], "unit": "TFLOP/s",
+                "frac": achieved_tflops / pk["bf16"], "traffic": measured_traffic(w.name, "up" if gi == 2 else "down"),
+                "peak_source": f"{pk['source']} bf16 dense burst"}
     value = job_tokens_per_s(w.n_tokens, args.steps, world, total_ms)
     e2e_value = job_tokens_per_s(w.n_tokens, args.steps, world, e2e_ms)
     b = 4 if w.dtype == "f32" else 2
@@ -356,11 +367,7 @@ def main():
                    "n_experts": w.n_experts, "top_k": w.top_k, "capacity_factor": w.capacity_factor,
                    "gating": w.gating, "act": w.act, "n_shared": w.n_shared, "parallelism": f"dp{world}",
                    "l2": "flushed between steps (256 MiB write)"},
-        "roofline": {"kernel": "grouped_gemm " + ("up" if gi == 2 else "down"), "bound": "tensor",
-                     "achieved": achieved_tflops, "peak": pk["bf16"], "unit": "TFLOP/s",
-                     "frac": achieved_tflops / pk["bf16"],
-                     "traffic": measured_traffic(w.name, "up" if gi == 2 else "down"),
-                     "peak_source": f"{pk['source']} bf16 dense burst"},
+        "roofline": {"kernel": "grouped_gemm " + ("up" if gi == 2 else "down"), **roof},
         "stages_ms": {s: float(v) for s, v in zip(STAGES, stage_avg)},
         "grouped_gemm_pct_bf16_peak": {
             "up": 100 * alg["up_flops"] / (stage_avg[2] / 1e3) / 1e12 / pk["bf16"],
@@ -368,6 +375,8 @@ def main():
         "hbm_gbs": {"route": alg["route_bytes"] / (stage_avg[0] / 1e3) / 1e9,
                     "permute": alg["permute_bytes"] / (stage_avg[1] / 1e3) / 1e9,
                     "combine": alg["combine_bytes"] / (stage_avg[4] / 1e3) / 1e9,
+                    "up": alg["up_bytes"] / (stage_avg[2] / 1e3) / 1e9,
+                    "down": alg["down_bytes"] / (stage_avg[3] / 1e3) / 1e9,
                     "peak": pk["hbm"]},
         "rows": rows,
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": int(x.numel() * b),
