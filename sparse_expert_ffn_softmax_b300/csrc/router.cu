@@ -299,6 +299,227 @@ __global__ void __launch_bounds__(kRouterWarps * 32) router_kernel(RouterArgs a)
   }
 }
 
+
+// ---- router for bf16 layers with up to 32 experts: warp-level tensor-core MMAs ----
+// A 16-token group of the batch is one m16 tile; the router's E <= 32 rows are up to
+// four n8 tiles. KS warps share a group (4; 16 for batches of fewer groups than
+// SMs), each taking every KS-th 32-deep slice of K: thread (gid = lane / 4, tig = lane % 4) loads 16 bytes of
+// token rows gid and gid + 8 and of router row gid of each n-tile at columns
+// 8 tig .. 8 tig + 7 of the slice, which feeds two m16n8k16 MMAs. (The order of
+// the K positions inside a slice is the same permutation for both operands, so
+// the dot products are unchanged.) The partial accumulators of the warps are
+// added in warp order through shared memory, then the group's first warp routes:
+// the four lanes of a quad hold the E logits of tokens gid and gid + 8, so the
+// softmax, the top-k (larger logit first, equal logits by lower expert id) and
+// the gate rule take two shuffle rounds per reduction. Statistics: probability
+// sums per expert and lse sums added to the fixed-point accumulators once per
+// group; assignment counts per permute tile through shared memory.
+__device__ __forceinline__ void mma_16816_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// NT n8 tiles (E <= 8 NT), top-k lists of up to KMAX, KS warps per group; G
+// 16-token groups per block (blockDim = 32 KS G, G <= 2, G = 1 for KS = 16);
+// TB = 16 G tokens per block = a whole number of permute tiles of a.tile tokens.
+template <int NT, int KMAX, int KS>
+__global__ void __launch_bounds__(KS == 16 ? 512 : 256, KS == 16 ? 1 : 2) router_mma_kernel(RouterArgs a) {
+  constexpr int NV = 2 * NT;  // logits per thread and token
+  constexpr int kMmaKSplit = KS;
+  __shared__ float s_red[KS == 16 ? 1 : 2][KS][NT * 4][32];
+  __shared__ int32_t s_cnt[2][32];  // per permute tile of the block (at most 2) and expert
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int G = (int)(blockDim.x / (32 * kMmaKSplit));
+  const int grp = warp / kMmaKSplit, ks = warp % kMmaKSplit;
+  const int gid = lane >> 2, tig = lane & 3;
+  const int64_t N = a.N, E = a.E, d = a.d, k = a.k, TT = a.tile;
+  const int64_t TB = 16 * (int64_t)G;
+  const int64_t blk_t0 = (int64_t)blockIdx.x * TB;
+  const int64_t t0 = blk_t0 + grp * 16;
+  const int64_t r0 = t0 + gid, r1 = t0 + gid + 8;
+  const bool v0 = r0 < N, v1 = r1 < N;
+  const bool ec = a.gating == MOE_GATE_EXPERT_CHOICE;
+  for (int i = threadIdx.x; i < 2 * 32; i += blockDim.x) (&s_cnt[0][0])[i] = 0;
+
+  // ---- logits: this warp's K slices ----
+  const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(a.x);
+  const __nv_bfloat16* wr = static_cast<const __nv_bfloat16*>(a.wr);
+  const __nv_bfloat16* xr0 = x + (v0 ? r0 : 0) * d + tig * 8;
+  const __nv_bfloat16* xr1 = x + (v1 ? r1 : 0) * d + tig * 8;
+  float c[NT][4];
+#pragma unroll
+  for (int j = 0; j < NT; ++j) c[j][0] = c[j][1] = c[j][2] = c[j][3] = 0.f;
+  const int64_t kslices = d / 32;
+#pragma unroll 4
+  for (int64_t kb = ks; kb < kslices; kb += kMmaKSplit) {
+    const int64_t col = kb * 32;
+    const uint4 xa = v0 ? __ldg(reinterpret_cast<const uint4*>(xr0 + col)) : make_uint4(0, 0, 0, 0);
+    const uint4 xb = v1 ? __ldg(reinterpret_cast<const uint4*>(xr1 + col)) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+      const int64_t e = 8 * j + gid;
+      const uint4 w = e < E ? __ldg(reinterpret_cast<const uint4*>(wr + e * d + col + tig * 8)) : make_uint4(0, 0, 0, 0);
+      mma_16816_bf16(c[j], xa.x, xb.x, xa.y, xb.y, w.x, w.y);
+      mma_16816_bf16(c[j], xa.z, xb.z, xa.w, xb.w, w.z, w.w);
+    }
+  }
+  // ---- add the K-split partials in warp order ----
+#pragma unroll
+  for (int j = 0; j < NT; ++j)
+#pragma unroll
+    for (int q = 0; q < 4; ++q) s_red[grp][ks][4 * j + q][lane] = c[j][q];
+  __syncthreads();
+  if (ks == 0) {
+#pragma unroll
+    for (int j = 0; j < NT; ++j)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        float v = s_red[grp][0][4 * j + q][lane];
+#pragma unroll
+        for (int w = 1; w < kMmaKSplit; ++w) v += s_red[grp][w][4 * j + q][lane];
+        c[j][q] = v;
+      }
+    // ---- route tokens gid (h = 0) and gid + 8 (h = 1) ----
+    float pacc[NV];
+#pragma unroll
+    for (int i = 0; i < NV; ++i) pacc[i] = 0.f;
+    float lse_sum = 0.f, lse_sq = 0.f;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int64_t t = h ? r1 : r0;
+      const bool valid = h ? v1 : v0;
+      float L[NV];
+#pragma unroll
+      for (int i = 0; i < NV; ++i) {
+        const int64_t e = 8 * (i >> 1) + 2 * tig + (i & 1);
+        L[i] = e < E ? c[i >> 1][2 * h + (i & 1)] + (a.logit_bias ? a.logit_bias[e] : 0.f) : -FLT_MAX;
+      }
+      float m = -FLT_MAX;
+#pragma unroll
+      for (int i = 0; i < NV; ++i) m = fmaxf(m, L[i]);
+      m = fmaxf(m, __shfl_xor_sync(kFull, m, 1));
+      m = fmaxf(m, __shfl_xor_sync(kFull, m, 2));
+      float ex[NV];
+      float s = 0.f;
+#pragma unroll
+      for (int i = 0; i < NV; ++i) {
+        const int64_t e = 8 * (i >> 1) + 2 * tig + (i & 1);
+        ex[i] = e < E ? __expf(L[i] - m) : 0.f;
+        s += ex[i];
+      }
+      s += __shfl_xor_sync(kFull, s, 1);
+      s += __shfl_xor_sync(kFull, s, 2);
+      const float lse = m + __logf(s);
+      const float inv_s = __fdividef(1.f, s);
+      if (valid && tig == 0) {
+        lse_sum += lse;
+        lse_sq += lse * lse;
+      }
+#pragma unroll
+      for (int i = 0; i < NV; ++i) {
+        const int64_t e = 8 * (i >> 1) + 2 * tig + (i & 1);
+        if (valid && e < E) {
+          const float pe = ex[i] * inv_s;
+          pacc[i] += pe;
+          if (a.probs) a.probs[t * E + e] = pe;
+          if (a.logits) a.logits[t * E + e] = L[i];
+        }
+      }
+      if (!ec) {
+        // ---- top-k: repeated quad arg-max, ties to the lower expert id ----
+        uint32_t taken = 0;
+        float topv[KMAX];
+        int topi[KMAX];
+#pragma unroll
+        for (int r = 0; r < KMAX; ++r) {
+          topv[r] = -FLT_MAX;
+          topi[r] = 0x7fffffff;
+          if (r < k) {
+            float bv = -FLT_MAX;
+            int be = 0x7fffffff;
+#pragma unroll
+            for (int i = 0; i < NV; ++i) {
+              const int e = 8 * (i >> 1) + 2 * tig + (i & 1);
+              if (e < E && !((taken >> i) & 1u) && (L[i] > bv || (L[i] == bv && e < be))) {
+                bv = L[i];
+                be = e;
+              }
+            }
+#pragma unroll
+            for (int sh = 1; sh <= 2; sh <<= 1) {
+              const float ov = __shfl_xor_sync(kFull, bv, sh);
+              const int oe = __shfl_xor_sync(kFull, be, sh);
+              if (ov > bv || (ov == bv && oe < be)) {
+                bv = ov;
+                be = oe;
+              }
+            }
+#pragma unroll
+            for (int i = 0; i < NV; ++i)
+              if (8 * (i >> 1) + 2 * tig + (i & 1) == be) taken |= 1u << i;
+            topv[r] = bv;
+            topi[r] = be;
+          }
+        }
+        // ---- gates ----
+        float g[KMAX];
+        float den = 0.f;
+#pragma unroll
+        for (int r = 0; r < KMAX; ++r) {
+          g[r] = 0.f;
+          if (r < k) {
+            g[r] = a.gating == MOE_GATE_TOPK_SOFTMAX ? __expf(topv[r] - topv[0]) : __expf(topv[r] - m) * inv_s;
+            den += g[r];
+          }
+        }
+        const bool renorm = a.gating == MOE_GATE_TOPK_SOFTMAX || a.gating == MOE_GATE_SOFTMAX_TOPK_RENORM;
+        const float ginv = renorm ? __fdividef(1.f, den) : 1.f;
+        if (valid && tig == 0) {
+          const int tl = (int)((t - blk_t0) / TT);
+#pragma unroll
+          for (int r = 0; r < KMAX; ++r)
+            if (r < k) {
+              a.idx[t * k + r] = topi[r];
+              a.gate[t * k + r] = g[r] * ginv;
+              if ((unsigned)topi[r] < (unsigned)E) atomicAdd(&s_cnt[tl][topi[r]], 1);
+            }
+        }
+      }
+    }
+    // ---- statistics of this group: probability sums per expert, lse sums ----
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+      float v = pacc[i];
+      v += __shfl_xor_sync(kFull, v, 4);
+      v += __shfl_xor_sync(kFull, v, 8);
+      v += __shfl_xor_sync(kFull, v, 16);
+      const int64_t e = 8 * (i >> 1) + 2 * tig + (i & 1);
+      if (gid == 0 && e < E) atomicAdd(a.acc.p + e, to_fixed((double)v, kPScale));
+    }
+    const float l1 = warp_sum(lse_sum), l2 = warp_sum(lse_sq);
+    if (lane == 0) {
+      atomicAdd(a.acc.lse, to_fixed((double)l1, kLseScale));
+      atomicAdd(a.acc.lse + 1, to_fixed((double)l2, kLse2Scale));
+    }
+  }
+  __syncthreads();
+  // ---- complete per-tile assignment counts ----
+  if (!ec) {
+    const int ntl = (int)(TB / TT);
+    for (int i = threadIdx.x; i < ntl * E; i += blockDim.x) {
+      const int tl = i / (int)E, e = i - tl * (int)E;
+      const int64_t tile = (int64_t)blockIdx.x * ntl + tl;
+      const int cnt = s_cnt[tl][e];
+      if (a.tile_counts && tile * TT < N) a.tile_counts[(int64_t)e * ((N + TT - 1) / TT) + tile] = cnt;
+      if (cnt) atomicAdd(a.acc.cnt + e, cnt);
+    }
+  }
+}
+
 }  // namespace
 
 __global__ void __launch_bounds__(512) router_finalize_kernel(StatsAcc acc, int64_t N, int64_t E, int64_t k,
@@ -369,11 +590,37 @@ cudaError_t launch_router_simt(const Plan& p, RouterArgs a, cudaStream_t st) {
 
 }  // namespace
 
+template <int NT, int KMAX>
+cudaError_t launch_router_mma_t(const Plan& p, RouterArgs a, cudaStream_t st) {
+  const int G = p.tile >= 32 ? 2 : 1;  // a block routes a whole number of permute tiles
+  const int64_t TB = 16 * G;
+  const int64_t blocks = ceil_div(p.N, TB);
+  if (G == 1 && blocks < 148) {  // few groups: more warps split each group's K range
+    router_mma_kernel<NT, KMAX, 16><<<(unsigned)blocks, 32 * 16, 0, st>>>(a);
+  } else {
+    router_mma_kernel<NT, KMAX, 4><<<(unsigned)blocks, 32 * 4 * G, 0, st>>>(a);
+  }
+  return cudaGetLastError();
+}
+
+template <int KMAX>
+cudaError_t launch_router_mma_k(const Plan& p, RouterArgs a, cudaStream_t st) {
+  if (p.E <= 8) return launch_router_mma_t<1, KMAX>(p, a, st);
+  if (p.E <= 16) return launch_router_mma_t<2, KMAX>(p, a, st);
+  if (p.E <= 24) return launch_router_mma_t<3, KMAX>(p, a, st);
+  return launch_router_mma_t<4, KMAX>(p, a, st);
+}
+
+// bf16 layers with up to 32 experts and k <= 8 (expert choice: any k).
+bool router_uses_mma(const Plan& p) { return p.bf16 && p.E <= 32 && (p.ec || p.k <= 8) && p.d % 32 == 0; }
+
 // Router per layer shape:
 //  - bf16 with more than 32 experts: the tensor cores write the logits (K split
 //    for small batches, router_k_splits), then this file's kernel routes;
-//  - fp32 layers and bf16 layers with up to 32 experts: the SIMT router (dot
-//    products on the CUDA cores, one warp per token).
+//  - bf16 layers with up to 32 experts: router_mma_kernel (warp-level tensor-core
+//    MMAs on 16-token tiles, routing by lane quads);
+//  - fp32 layers (and bf16 with k > 8): the SIMT router (dot products on the CUDA
+//    cores, one warp per token).
 bool router_uses_tc(const Plan& p) { return p.bf16 && p.E >= kRouterTcMinE; }
 
 cudaError_t launch_router(const Plan& p, const void* x, const moe_weights* w, int32_t* idx, float* gate,
@@ -412,6 +659,8 @@ cudaError_t launch_router(const Plan& p, const void* x, const moe_weights* w, in
     a.part_stride = p.N * p.E;
     a.logits = split ? logits : nullptr;  // unsplit: the GEMM wrote the logits (bias included)
     err = launch_router_logits_in<__nv_bfloat16>(p, a, st);
+  } else if (router_uses_mma(p)) {
+    err = (p.ec || p.k <= 2) ? launch_router_mma_k<2>(p, a, st) : launch_router_mma_k<8>(p, a, st);
   } else {
     err = p.bf16 ? launch_router_simt<__nv_bfloat16>(p, a, st) : launch_router_simt<float>(p, a, st);
   }
