@@ -72,6 +72,11 @@ SMALL = [
     wl("bf16_k10_two_kernel", n_tokens=150, d_model=64, d_ff=64, n_experts=64, top_k=10, capacity_factor=1.25,
        gating="softmax_topk_renorm"),
     wl("bf16_E300_two_kernel", n_tokens=130, d_model=64, d_ff=64, n_experts=300, top_k=2, capacity_factor=0.0),
+    # the SIMT router: bf16 with k > 8 of at most 32 experts, fp32 with more than 64 experts
+    wl("bf16_E24_k10_simt", n_tokens=140, d_model=128, d_ff=64, n_experts=24, top_k=10, capacity_factor=1.0,
+       gating="softmax_topk_renorm"),
+    wl("f32_E72_k3", dtype="f32", n_tokens=90, d_model=64, d_ff=64, n_experts=72, top_k=3, capacity_factor=1.25,
+       gating="topk_softmax", has_bias=True),
 ]
 
 
@@ -138,6 +143,9 @@ def test_stage_calls_match_forward():
     row_token = torch.empty(R, dtype=torch.int32, device=dev)
     row_gate = torch.empty(R, dtype=torch.float32, device=dev)
     moe.permute(cfg, t["x"], idx, gate, xp, tok_rows, None, expert_off, row_token, row_gate, stats, ws)
+    torch.cuda.synchronize()
+    rows = int(expert_off[-1].item())
+    assert torch.equal(xp[:rows], t["x"][row_token[:rows].long()])  # permuted rows are exact copies
     yp = torch.empty(R, d, dtype=torch.float32, device=dev)
     ys = torch.empty(N, d, dtype=torch.float32, device=dev)
     moe.expert_ffn(cfg, xp, expert_off, row_gate, t["x"], layer.w, yp, ys, ws)
