@@ -300,16 +300,25 @@ def main():
     if dist:
         td.barrier()
     torch.cuda.synchronize(dev)
-    if True:
-        for _ in range(args.steps):
-            flush.zero_()
-            moe.forward_traced(layer.cfg, x, layer.w, out, ev, layer.stats, layer.ws)
-            ev[-1].synchronize()
-            times = [ev[i].elapsed_time(ev[i + 1]) for i in range(5)]
-            stage_ms += np.array(times)
-            step_ms.append(ev[0].elapsed_time(ev[5]))
-        torch.cuda.synchronize(dev)
+    # timed steps: one event before and one after each forward (events between the
+    # stages would stop each kernel's launch from overlapping the previous one's tail)
+    for _ in range(args.steps):
+        flush.zero_()
+        ev[0].record()
+        moe.forward(layer.cfg, x, layer.w, out, layer.stats, layer.ws)
+        ev[5].record()
+        ev[5].synchronize()
+        step_ms.append(ev[0].elapsed_time(ev[5]))
+    torch.cuda.synchronize(dev)
     total_ms = max_over_ranks(float(np.sum(step_ms)), dev)
+    # per-stage times from a traced pass (events between the stages; their sum exceeds ms_per_step)
+    n_traced = max(1, min(args.steps, 50))
+    for _ in range(n_traced):
+        flush.zero_()
+        moe.forward_traced(layer.cfg, x, layer.w, out, ev, layer.stats, layer.ws)
+        ev[-1].synchronize()
+        stage_ms += np.array([ev[i].elapsed_time(ev[i + 1]) for i in range(5)])
+    torch.cuda.synchronize(dev)
     if dist:
         td.barrier()
     code, word = moe.get_device_status(layer.cfg, layer.ws)
@@ -330,7 +339,7 @@ def main():
     touched = int((kept > 0).sum())
     alg = algorithmic(w, rows, touched)
     pk = peaks()
-    stage_avg = stage_ms / args.steps
+    stage_avg = stage_ms / n_traced
     # dominant kernel: the larger of the two grouped-GEMM launches
     gi = 2 if stage_avg[2] >= stage_avg[3] else 3
     flops = alg["up_flops"] if gi == 2 else alg["down_flops"]

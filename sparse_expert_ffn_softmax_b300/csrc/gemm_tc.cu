@@ -375,6 +375,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&done_bar, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
+  pdl_wait();  // expert offsets, operands: written by the previous kernels of the stream
+  pdl_launch_next();
   // tile prefix over all groups of both families (same in every CTA)
   const int G0 = P.fam[0].groups, G = G0 + P.fam[1].groups;
   if (warp == 0) {
@@ -750,9 +752,8 @@ cudaError_t launch_t(const CUtensorMap (&maps)[8], const Params& P, int64_t max_
   if (attr != cudaSuccess) return attr;
   const int64_t grid = max_tiles < num_sms() ? max_tiles : num_sms();
   if (grid <= 0) return cudaSuccess;
-  kern<<<(unsigned)grid, kThreads, C::kSmem, st>>>(maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6],
-                                                    maps[7], P);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3((unsigned)grid), dim3(kThreads), C::kSmem, st, maps[0], maps[1], maps[2], maps[3],
+                    maps[4], maps[5], maps[6], maps[7], P);
 }
 
 template <int EPI>

@@ -111,6 +111,8 @@ __global__ void __launch_bounds__(kWarps * 32) scatter_kernel(
   // writes the row metadata.
   const bool meta = blockIdx.y == 0;
   extern __shared__ uint32_t s_dyn[];
+  pdl_wait();
+  pdl_launch_next();
   uint32_t* msk = s_dyn;                                       // [E]
   int32_t* s_rows = reinterpret_cast<int32_t*>(s_dyn + E);     // [32][k]
   int32_t* s_pre = s_rows + kMaxTileTokens * k;                // [E]   (kFused)
@@ -406,6 +408,8 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(const float* __res
                                                               const int32_t* __restrict__ tok_off,
                                                               const float* __restrict__ ys, int64_t N, int64_t d,
                                                               int64_t k, TO* __restrict__ out) {
+  pdl_wait();
+  pdl_launch_next();
   using VO = Vec16<TO>;
   constexpr int VN = VO::n;  // outputs per lane chunk: 8 (bf16) or 4 (fp32)
   constexpr int NV = VN / 4; // float4 loads per row and chunk
@@ -506,10 +510,10 @@ cudaError_t launch_permute_t(const Plan& p, const void* x, const int32_t* idx, c
     fin.acc = stats_acc_at(ws_at<uint8_t>(ws, p.stat_acc), p.E);
     fin.alpha = p.cfg.aux_alpha;
     const size_t sc_smem = (size_t)p.E * 4 + (size_t)kMaxTileTokens * p.k * 4 + (size_t)(2 * p.E + 1) * 4;
-    scatter_kernel<T, true><<<dim3((unsigned)p.tiles + 1, (unsigned)slices), kWarps * 32, sc_smem, st>>>(
-        static_cast<const T*>(x), idx, gate, tile_counts, expert_off, p.N, p.d, p.k, p.E, p.tiles, p.tile, p.cap,
-        static_cast<T*>(xp), tok_rows, row_token, row_gate, stats, status, fin);
-    return cudaGetLastError();
+    return launch_pdl(scatter_kernel<T, true>, dim3((unsigned)p.tiles + 1, (unsigned)slices), dim3(kWarps * 32),
+                      sc_smem, st, static_cast<const T*>(x), idx, gate, (const int32_t*)tile_counts, expert_off, p.N,
+                      p.d, p.k, p.E, (int64_t)p.tiles, p.tile, p.cap, static_cast<T*>(xp), tok_rows, row_token,
+                      row_gate, stats, status, fin);
   }
   if (mode == kCountsFromIdx) {
     const size_t hist_smem = (size_t)kWarps * p.E * 4;
@@ -567,16 +571,16 @@ cudaError_t launch_combine(const Plan& p, const void* yp, const int32_t* tok_row
   const int64_t ku = p.ec ? 2 : p.k;
   if (p.bf16) {
     __nv_bfloat16* o = static_cast<__nv_bfloat16*>(out);
-    if (ku <= 1) combine_kernel<__nv_bfloat16, 1><<<grid, kWarps * 32, 0, st>>>(ypf, tok_rows, toff, ysf, p.N, p.d, p.k, o);
-    else if (ku <= 2) combine_kernel<__nv_bfloat16, 2><<<grid, kWarps * 32, 0, st>>>(ypf, tok_rows, toff, ysf, p.N, p.d, p.k, o);
-    else if (ku <= 4) combine_kernel<__nv_bfloat16, 4><<<grid, kWarps * 32, 0, st>>>(ypf, tok_rows, toff, ysf, p.N, p.d, p.k, o);
-    else combine_kernel<__nv_bfloat16, 8><<<grid, kWarps * 32, 0, st>>>(ypf, tok_rows, toff, ysf, p.N, p.d, p.k, o);
+    if (ku <= 1) launch_pdl(combine_kernel<__nv_bfloat16, 1>, grid, dim3(kWarps * 32), 0, st, ypf, (const int32_t*)tok_rows, toff, ysf, p.N, p.d, p.k, o);
+    else if (ku <= 2) launch_pdl(combine_kernel<__nv_bfloat16, 2>, grid, dim3(kWarps * 32), 0, st, ypf, (const int32_t*)tok_rows, toff, ysf, p.N, p.d, p.k, o);
+    else if (ku <= 4) launch_pdl(combine_kernel<__nv_bfloat16, 4>, grid, dim3(kWarps * 32), 0, st, ypf, (const int32_t*)tok_rows, toff, ysf, p.N, p.d, p.k, o);
+    else launch_pdl(combine_kernel<__nv_bfloat16, 8>, grid, dim3(kWarps * 32), 0, st, ypf, (const int32_t*)tok_rows, toff, ysf, p.N, p.d, p.k, o);
   } else {
     float* o = static_cast<float*>(out);
-    if (ku <= 1) combine_kernel<float, 1><<<grid, kWarps * 32, 0, st>>>(ypf, tok_rows, toff, ysf, p.N, p.d, p.k, o);
-    else if (ku <= 2) combine_kernel<float, 2><<<grid, kWarps * 32, 0, st>>>(ypf, tok_rows, toff, ysf, p.N, p.d, p.k, o);
-    else if (ku <= 4) combine_kernel<float, 4><<<grid, kWarps * 32, 0, st>>>(ypf, tok_rows, toff, ysf, p.N, p.d, p.k, o);
-    else combine_kernel<float, 8><<<grid, kWarps * 32, 0, st>>>(ypf, tok_rows, toff, ysf, p.N, p.d, p.k, o);
+    if (ku <= 1) launch_pdl(combine_kernel<float, 1>, grid, dim3(kWarps * 32), 0, st, ypf, (const int32_t*)tok_rows, toff, ysf, p.N, p.d, p.k, o);
+    else if (ku <= 2) launch_pdl(combine_kernel<float, 2>, grid, dim3(kWarps * 32), 0, st, ypf, (const int32_t*)tok_rows, toff, ysf, p.N, p.d, p.k, o);
+    else if (ku <= 4) launch_pdl(combine_kernel<float, 4>, grid, dim3(kWarps * 32), 0, st, ypf, (const int32_t*)tok_rows, toff, ysf, p.N, p.d, p.k, o);
+    else launch_pdl(combine_kernel<float, 8>, grid, dim3(kWarps * 32), 0, st, ypf, (const int32_t*)tok_rows, toff, ysf, p.N, p.d, p.k, o);
   }
   return cudaGetLastError();
 }

@@ -332,6 +332,8 @@ __global__ void __launch_bounds__(KS == 16 ? 512 : 256, KS == 16 ? 1 : 2) router
   constexpr int kMmaKSplit = KS;
   __shared__ float s_red[KS == 16 ? 1 : 2][KS][NT * 4][32];
   __shared__ int32_t s_cnt[2][32];  // per permute tile of the block (at most 2) and expert
+  pdl_wait();
+  pdl_launch_next();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int G = (int)(blockDim.x / (32 * kMmaKSplit));
   const int grp = warp / kMmaKSplit, ks = warp % kMmaKSplit;
@@ -596,11 +598,9 @@ cudaError_t launch_router_mma_t(const Plan& p, RouterArgs a, cudaStream_t st) {
   const int64_t TB = 16 * G;
   const int64_t blocks = ceil_div(p.N, TB);
   if (G == 1 && blocks < 148) {  // few groups: more warps split each group's K range
-    router_mma_kernel<NT, KMAX, 16><<<(unsigned)blocks, 32 * 16, 0, st>>>(a);
-  } else {
-    router_mma_kernel<NT, KMAX, 4><<<(unsigned)blocks, 32 * 4 * G, 0, st>>>(a);
+    return launch_pdl(router_mma_kernel<NT, KMAX, 16>, dim3((unsigned)blocks), dim3(32 * 16), 0, st, a);
   }
-  return cudaGetLastError();
+  return launch_pdl(router_mma_kernel<NT, KMAX, 4>, dim3((unsigned)blocks), dim3(32 * 4 * G), 0, st, a);
 }
 
 template <int KMAX>
