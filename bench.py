@@ -198,6 +198,19 @@ def algorithmic(w, rows, touched):
     )
 
 
+def gemm_roofline(flops: float, nbytes: float, seconds: float, pk: dict, traffic=None) -> dict:
+    """Roofline entry of a grouped GEMM launch: against whichever roof takes longer at its
+    peak -- the bf16 tensor peak for its FLOPs or the HBM bandwidth for its bytes (a decode
+    batch streams the expert weights and is bound by the second)."""
+    if nbytes / (pk["hbm"] * 1e9) > flops / (pk["bf16"] * 1e12):
+        achieved = nbytes / seconds / 1e9
+        return {"bound": "hbm", "achieved": achieved, "peak": pk["hbm"], "unit": "GB/s",
+                "frac": achieved / pk["hbm"], "traffic": traffic, "peak_source": f"{pk['source']} HBM copy"}
+    achieved = flops / seconds / 1e12
+    return {"bound": "tensor", "achieved": achieved, "peak": pk["bf16"], "unit": "TFLOP/s",
+            "frac": achieved / pk["bf16"], "traffic": traffic, "peak_source": f"{pk['source']} bf16 dense burst"}
+
+
 def launches_per_step(w):
     """Kernels the library launches per forward (the expert-choice bitmap memset not counted)."""
     ec = w.gating == "expert_choice"
@@ -346,16 +359,7 @@ def main():
     gbytes = alg["up_bytes"] if gi == 2 else alg["down_bytes"]
     dom_s = stage_avg[gi] / 1e3
     achieved_tflops = flops / dom_s / 1e12
-    # bound: whichever roof takes longer at its peak (decode batches stream the weights: HBM)
-    hbm_bound = gbytes / (pk["hbm"] * 1e9) > flops / (pk["bf16"] * 1e12)
-    if hbm_bound:
-        roof = {"bound": "hbm", "achieved": gbytes / dom_s / 1e9, "peak": pk["hbm"], "unit": "GB/s",
-                "frac": gbytes / dom_s / 1e9 / pk["hbm"], "traffic": measured_traffic(w.name, "up" if gi == 2 else "down"),
-                "peak_source": f"{pk['source']} HBM copy"}
-    else:
-        roof = {"bound": "tensor", "achieved": achieved_tflops, "peak": pk["bf16"], "unit": "TFLOP/s",
-                "frac": achieved_tflops / pk["bf16"], "traffic": measured_traffic(w.name, "up" if gi == 2 else "down"),
-                "peak_source": f"{pk['source']} bf16 dense burst"}
+    roof = gemm_roofline(flops, gbytes, dom_s, pk, measured_traffic(w.name, "up" if gi == 2 else "down"))
     value = job_tokens_per_s(w.n_tokens, args.steps, world, total_ms)
     e2e_value = job_tokens_per_s(w.n_tokens, args.steps, world, e2e_ms)
     b = 4 if w.dtype == "f32" else 2

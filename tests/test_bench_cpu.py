@@ -1,0 +1,49 @@
+"""bench.py's bookkeeping on the CPU: algorithmic work per forward and the choice of roof."""
+import importlib.util
+import os
+
+import pytest
+
+from sparse_expert_ffn_softmax_b300 import WORKLOADS
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def bench():
+    spec = importlib.util.spec_from_file_location("bench_under_test", os.path.join(ROOT, "bench.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod
+
+
+PEAKS = dict(hbm=6481.0, bf16=1749.0, bf16_sustained=1366.0, source="measured")
+
+
+def test_algorithmic_counts(bench):
+    w = WORKLOADS["small_bf16"]
+    rows = w.n_tokens * w.top_k
+    a = bench.algorithmic(w, rows, w.n_experts)
+    assert a["up_flops"] == 2 * rows * w.d_model * w.d_ff  # GELU: one projection
+    assert a["down_flops"] == a["up_flops"]
+    # up reads xp and W1 (+ bias-free byte count) and writes H, each once
+    assert a["up_bytes"] == rows * w.d_model * 2 + w.n_experts * w.d_ff * w.d_model * 2 + rows * w.d_ff * 2
+    sw = WORKLOADS["mixtral_prefill"]
+    b = bench.algorithmic(sw, sw.n_tokens * sw.top_k, sw.n_experts)
+    assert b["up_flops"] == 2 * 2 * sw.n_tokens * sw.top_k * sw.d_model * sw.d_ff  # SwiGLU: W1 and W3
+
+
+@pytest.mark.parametrize("name,bound", [("small_bf16", "tensor"), ("mixtral_prefill", "tensor"),
+                                        ("large_fine", "tensor"), ("mixtral_decode", "hbm"),
+                                        ("large_fine_decode", "hbm")])
+def test_roof_choice(bench, name, bound):
+    w = WORKLOADS[name]
+    a = bench.algorithmic(w, w.n_tokens * w.top_k, w.n_experts)
+    for flops, nbytes in ((a["up_flops"], a["up_bytes"]), (a["down_flops"], a["down_bytes"])):
+        r = bench.gemm_roofline(flops, nbytes, 1e-3, PEAKS)
+        assert r["bound"] == bound
+        assert r["frac"] == pytest.approx(r["achieved"] / r["peak"])
+        if bound == "hbm":
+            assert r["unit"] == "GB/s" and r["achieved"] == pytest.approx(nbytes / 1e-3 / 1e9)
+        else:
+            assert r["unit"] == "TFLOP/s" and r["achieved"] == pytest.approx(flops / 1e-3 / 1e12)
