@@ -143,6 +143,9 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     if (globaltimer() - t0 > kTimeoutNs) return false;
   }
 }
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
 __device__ __forceinline__ void tma_load_2d(const CUtensorMap* map, uint64_t* bar, void* dst, int32_t x,
                                             int32_t y) {
   asm volatile(
@@ -375,6 +378,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&done_bar, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
+  // Set-up that reads nothing earlier kernels wrote runs before the dependency wait, so
+  // it overlaps the previous kernel's tail: the tensor-map prefetch and the TMEM
+  // allocation (a previous CTA of this kernel cannot share the SM: its shared memory
+  // takes the SM's whole budget; the other kernels of the forward use no TMEM).
+  if (warp == 0 && lane == 0) {
+    prefetch_tensormap(&m0);
+    prefetch_tensormap(&m1);
+    prefetch_tensormap(&m2);
+    prefetch_tensormap(&m3);
+    prefetch_tensormap(&m4);
+    prefetch_tensormap(&m5);
+    prefetch_tensormap(&o0);
+    prefetch_tensormap(&o1);
+  }
+  if (warp == 1) tmem_alloc(&s_tmem_base, C::kTmemCols);
   pdl_wait();  // expert offsets, operands: written by the previous kernels of the stream
   pdl_launch_next();
   // tile prefix over all groups of both families (same in every CTA)
@@ -396,15 +414,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (lane == 0) s_start[G] = carry;
   }
-  __syncthreads();
-  const int total = s_start[G];
-  if ((int)blockIdx.x >= total) return;  // uniform across the CTA, before any TMEM is taken
-
-  if (warp == 1) tmem_alloc(&s_tmem_base, C::kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = s_tmem_base;
+  const int total = s_start[G];
+  if ((int)blockIdx.x >= total) {  // uniform across the CTA: nothing to do, give the TMEM back
+    if (warp == 1) tmem_dealloc(tmem_base, C::kTmemCols);
+    return;
+  }
   volatile int32_t* abort_flag = &s_abort;
 
   if (warp == 0) {
