@@ -20,11 +20,18 @@
 //
 // Tile 128 x BN x 64, K-major operands in 128-byte-swizzled shared memory.
 // Warp roles: warp 0 issues TMA loads into a STAGES-deep ring, warp 1 issues
-// tcgen05.mma (M=128, N=BN, K=16) into one of two TMEM accumulators, warps 2-9
+// tcgen05.mma (M=128, N=BN, K=16) into one of two TMEM accumulators, warps 2-13
 // drain the other accumulator with tcgen05.ld (warp w reads TMEM lanes
-// 32*(w%4)...), apply the epilogue (GELU + bias, SiLU x gate, or bias x row gate),
-// convert to bf16 and store. SwiGLU tiles load BN/2 rows of W1 and BN/2 rows of
-// W3 into one BN-row B tile, so one MMA fills both halves of the accumulator.
+// 32*(w%4)...), apply the epilogue (GELU + bias, SiLU x gate, or bias x row gate;
+// two columns per packed fp32x2 operation), and store through TMA. SwiGLU tiles
+// load BN/2 rows of W1 and BN/2 rows of W3 into one BN-row B tile, so one MMA
+// fills both halves of the accumulator.
+//
+// Pair form (down-projection of large batches): clusters of two CTAs compute
+// 256 x BN tiles with the M = 256 tcgen05.mma of a CTA pair. Each CTA stages its own
+// 128 rows of A and half of B; both halves' copies complete on the leader's
+// barrier, the leader issues the MMAs, its commits arrive at both CTAs, and each CTA
+// drains its own 128 accumulator rows, the peer signalling the leader when done.
 //
 // Every mbarrier wait is bounded by the global timer; on expiry the CTA records
 // MOE_ERR_TIMEOUT in the workspace error word, waits (bounded) for its own TMA
@@ -198,6 +205,94 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                : "memory");
 }
+
+// ---- CTA-pair forms (cluster of 2; the even CTA is the leader that issues the MMAs) ----
+// Tensor memory is allocated and freed collectively by one warp of each CTA of the
+// pair; an M = 256 MMA takes rows 0-127 of A from the leader's shared memory and
+// rows 128-255 from the peer's, B's first N/2 rows from the leader and the rest from
+// the peer (same shared-memory offsets in both), and writes accumulator rows 0-127
+// to the leader's tensor memory, rows 128-255 to the peer's.
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_id_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t nclusters_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+  return r;
+}
+// shared::cluster address of the same shared-memory offset in CTA `rank` of the cluster
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile(
+      "barrier.cluster.arrive.release.aligned;\n"
+      "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+// TMA load into this CTA's shared memory whose completion is counted on the
+// leader's mbarrier (`bar_cluster`: shared::cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(const CUtensorMap* map, uint32_t bar_cluster, void* dst, int32_t x,
+                                                 int32_t y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, "
+      "%4}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(y)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t* dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                               uint32_t accumulate) {
+  asm volatile(
+      "{\n"
+      ".reg .pred p;\n"
+      "setp.ne.b32 p, %4, 0;\n"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n"
+      "}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// arrive on the mbarrier at this offset in both CTAs of the pair once the MMAs
+// issued so far have completed
+__device__ __forceinline__ void umma_commit_pair(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_u32(bar)),
+      "h"((uint16_t)3)
+      : "memory");
+}
+
+template <bool PAIR>
+__device__ __forceinline__ void tmem_alloc_t(uint32_t* dst_smem, uint32_t ncols) {
+  if constexpr (PAIR) tmem_alloc_pair(dst_smem, ncols); else tmem_alloc(dst_smem, ncols);
+}
+template <bool PAIR>
+__device__ __forceinline__ void tmem_dealloc_t(uint32_t taddr, uint32_t ncols) {
+  if constexpr (PAIR) tmem_dealloc_pair(taddr, ncols); else tmem_dealloc(taddr, ncols);
+}
+template <bool PAIR>
+__device__ __forceinline__ void umma_commit_t(uint64_t* bar) {
+  if constexpr (PAIR) umma_commit_pair(bar); else umma_commit(bar);
+}
 // 32 lanes x 32 consecutive fp32 columns: thread i of the warp gets lane (base lane + i).
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(
@@ -283,10 +378,35 @@ __device__ __forceinline__ float gelu_as7126(float u) {
   return fmaf(-fabsf(u), hq, fmaxf(u, 0.f));
 }
 
-template <int BN>
+// gelu_as7126 on two values at once with the packed fp32x2 multiply / FMA, each of
+// whose halves rounds exactly as its scalar form, so the results are bit-identical
+// to two scalar calls. The polynomial's coefficients enter negated (exact under
+// round-to-nearest), so it yields -q/2 and the last step is |u| (-q/2) + max(u, 0).
+__device__ __forceinline__ float2 gelu2_as7126(float2 u) {
+  constexpr float kS = 0.8493218002880191f;
+  constexpr float kP = 0.2727374808792225f;
+  constexpr float kN1 = -0.5f * 0.254829592f, kN2 = -0.5f * -0.284496736f, kN3 = -0.5f * 1.421413741f,
+                  kN4 = -0.5f * -1.453152027f, kN5 = -0.5f * 1.061405429f;
+  const float2 au = make_float2(fabsf(u.x), fabsf(u.y));
+  const float2 s = __fmul2_rn(au, make_float2(kS, kS));
+  const float2 den = __ffma2_rn(make_float2(kP, kP), s, make_float2(1.f, 1.f));
+  const float2 t = make_float2(rcp_ftz(den.x), rcp_ftz(den.y));
+  float2 pn = __ffma2_rn(make_float2(kN5, kN5), t, make_float2(kN4, kN4));
+  pn = __ffma2_rn(pn, t, make_float2(kN3, kN3));
+  pn = __ffma2_rn(pn, t, make_float2(kN2, kN2));
+  pn = __ffma2_rn(pn, t, make_float2(kN1, kN1));
+  const float2 ss = __fmul2_rn(s, s);
+  const float2 e = make_float2(ex2_ftz(-ss.x), ex2_ftz(-ss.y));
+  const float2 hqn = __fmul2_rn(__fmul2_rn(pn, t), e);  // -q/2
+  return __ffma2_rn(au, hqn, make_float2(fmaxf(u.x, 0.f), fmaxf(u.y, 0.f)));
+}
+
+// PAIR: the tile is 256 x BN on a CTA pair; each CTA stages its 128 rows of A and
+// half (BN / 2 rows) of B.
+template <int BN, bool PAIR = false>
 struct Cfg {
   static constexpr int kABytes = BM * BK * 2;
-  static constexpr int kBBytes = BN * BK * 2;
+  static constexpr int kBBytes = (PAIR ? BN / 2 : BN) * BK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kStages = (192 * 1024) / kStageBytes > 8 ? 8 : (192 * 1024) / kStageBytes;
   static constexpr int kTmemCols = 2 * BN;
@@ -298,8 +418,11 @@ struct TileInfo {
   int fam, g, mt, nt, m, a_row0;
 };
 
+// Tile `tile` of the prefix s_start. PAIR: tiles are 256-row pair tiles and the CTA
+// of rank `half` in the pair takes their 128-row half `half`.
+template <bool PAIR = false>
 __device__ __forceinline__ TileInfo decode_tile(int tile, const int32_t* s_start, int G, int G0,
-                                                const Family* fams, const int32_t* off) {
+                                                const Family* fams, const int32_t* off, int half = 0) {
   int lo = 0, hi = G;  // last group whose start <= tile
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
@@ -317,10 +440,11 @@ __device__ __forceinline__ TileInfo decode_tile(int tile, const int32_t* s_start
     row0 = 0;
     ti.m = F.m_fixed;
   }
-  const int m_tiles = (ti.m + BM - 1) / BM;
+  const int m_tiles = PAIR ? (ti.m + 2 * BM - 1) / (2 * BM) : (ti.m + BM - 1) / BM;
   const int local = tile - s_start[lo];
   ti.nt = local / m_tiles;
   ti.mt = local - ti.nt * m_tiles;
+  if (PAIR) ti.mt = 2 * ti.mt + half;
   ti.a_row0 = row0 + ti.mt * BM;
   return ti;
 }
@@ -338,17 +462,18 @@ __device__ __forceinline__ const CUtensorMap* pick_map(int i, const CUtensorMap&
   }
 }
 
-template <int BN, int EPI>
+template <int BN, int EPI, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap m0, const __grid_constant__ CUtensorMap m1,
                         const __grid_constant__ CUtensorMap m2, const __grid_constant__ CUtensorMap m3,
                         const __grid_constant__ CUtensorMap m4, const __grid_constant__ CUtensorMap m5,
                         const __grid_constant__ CUtensorMap o0, const __grid_constant__ CUtensorMap o1,
                         const __grid_constant__ Params P) {
-  using C = Cfg<BN>;
+  static_assert(!PAIR || EPI == kLinear, "CTA pairs serve the down-projection (one B map, linear epilogue)");
+  using C = Cfg<BN, PAIR>;
   constexpr int kStages = C::kStages;
   constexpr int kOutCols = EPI == kSwiglu ? BN / 2 : BN;
-  constexpr uint32_t kIdesc = idesc_bf16(BM, BN);
+  constexpr uint32_t kIdesc = idesc_bf16(PAIR ? 2 * BM : BM, BN);
 
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[kStages], empty_bar[kStages], tfull_bar[2], tempty_bar[2], done_bar;
@@ -358,6 +483,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ int32_t s_abort;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // PAIR: rank 0 (leader) issues the MMAs and owns the full / accumulator-empty barriers
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+  const int walk0 = PAIR ? (int)cluster_id_x() : (int)blockIdx.x;
+  const int walk_step = PAIR ? (int)nclusters_x() : (int)gridDim.x;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   uint8_t* sA = smem;
   uint8_t* sB = smem + kStages * C::kABytes;
@@ -373,7 +502,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull_bar[a], 1);
-      mbar_init(&tempty_bar[a], kEpiWarps);
+      mbar_init(&tempty_bar[a], PAIR ? 2 * kEpiWarps : kEpiWarps);
     }
     mbar_init(&done_bar, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -392,7 +521,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tensormap(&o0);
     prefetch_tensormap(&o1);
   }
-  if (warp == 1) tmem_alloc(&s_tmem_base, C::kTmemCols);
+  if (warp == 1) tmem_alloc_t<PAIR>(&s_tmem_base, C::kTmemCols);
   pdl_wait();  // expert offsets, operands: written by the previous kernels of the stream
   pdl_launch_next();
   // tile prefix over all groups of both families (same in every CTA)
@@ -406,7 +535,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const Family& F = g < G0 ? P.fam[0] : P.fam[1];
         const int gl = g < G0 ? g : g - G0;
         const int m = F.m_from_off ? off[gl + 1] - off[gl] : F.m_fixed;
-        tiles = ((m + BM - 1) / BM) * F.n_tiles;
+        tiles = (PAIR ? (m + 2 * BM - 1) / (2 * BM) : (m + BM - 1) / BM) * F.n_tiles;
       }
       const int inc = warp_inclusive_scan(tiles);
       if (g < G) s_start[g] = carry + inc - tiles;
@@ -416,11 +545,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  // PAIR: both CTAs' barriers are initialised before either CTA signals the other's
+  if (PAIR) cluster_sync_all();
   tc_fence_after();
   const uint32_t tmem_base = s_tmem_base;
   const int total = s_start[G];
-  if ((int)blockIdx.x >= total) {  // uniform across the CTA: nothing to do, give the TMEM back
-    if (warp == 1) tmem_dealloc(tmem_base, C::kTmemCols);
+  if (walk0 >= total) {  // uniform across the CTA (and the pair): nothing to do, give the TMEM back
+    if (warp == 1) tmem_dealloc_t<PAIR>(tmem_base, C::kTmemCols);
     return;
   }
   volatile int32_t* abort_flag = &s_abort;
@@ -434,8 +565,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int s = 0; s < kStages; ++s) last_parity[s] = -1;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-        const TileInfo ti = decode_tile(tile, s_start, G, G0, s_fam, off);
+      for (int tile = walk0; tile < total && ok; tile += walk_step) {
+        const TileInfo ti = decode_tile<PAIR>(tile, s_start, G, G0, s_fam, off, (int)rank);
         const Family& F = s_fam[ti.fam];
         const CUtensorMap* ma = pick_map(F.a_map, m0, m1, m2, m3, m4, m5);
         const CUtensorMap* mb = pick_map(F.b_map, m0, m1, m2, m3, m4, m5);
@@ -446,11 +577,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
+          const int kseg = kb / F.kseg_blocks;
+          const int kin = k0 + kb - kseg * F.kseg_blocks;
+          if (PAIR) {
+            // both CTAs' copies complete on the leader's full barrier, which expects
+            // the bytes of the two halves; B: the leader stages rows [0, BN/2) of the
+            // tile, the peer rows [BN/2, BN)
+            const uint32_t fb = mapa_shared(smem_u32(&full_bar[stage]), 0u);
+            if (rank == 0) {
+              mbar_arrive_expect_tx(&full_bar[stage], 2 * C::kStageBytes);
+              last_parity[stage] = (int32_t)phase;
+            }
+            tma_load_2d_pair(ma, fb, sA + stage * C::kABytes, (k0 + kb) * BK, ti.a_row0);
+            const int by = ti.g * F.b_rows_group + kseg * F.b_rows_kseg + ti.nt * BN + (int)rank * (BN / 2);
+            tma_load_2d_pair(mb, fb, sB + stage * C::kBBytes, kin * BK, by);
+            if (++stage == kStages) {
+              stage = 0;
+              phase ^= 1u;
+            }
+            continue;
+          }
           mbar_arrive_expect_tx(&full_bar[stage], C::kStageBytes);
           last_parity[stage] = (int32_t)phase;
           tma_load_2d(ma, &full_bar[stage], sA + stage * C::kABytes, (k0 + kb) * BK, ti.a_row0);
-          const int kseg = kb / F.kseg_blocks;
-          const int kin = k0 + kb - kseg * F.kseg_blocks;
           if (EPI == kSwiglu) {
             const int by = ti.g * F.b_rows_group + kseg * F.b_rows_kseg + ti.nt * (BN / 2);
             tma_load_2d(mb, &full_bar[stage], sB + stage * C::kBBytes, kin * BK, by);
@@ -483,8 +632,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-        const TileInfo ti = decode_tile(tile, s_start, G, G0, s_fam, off);
+      for (int tile = walk0; tile < total && ok && (!PAIR || rank == 0); tile += walk_step) {
+        const TileInfo ti = decode_tile<PAIR>(tile, s_start, G, G0, s_fam, off, (int)rank);
         const int kblocks = s_fam[ti.fam].k_blocks;
         if (!mbar_wait<false>(&tempty_bar[acc], acc_phase ^ 1u, abort_flag)) {
           ok = false;
@@ -502,17 +651,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t b_addr = smem_u32(sB + stage * C::kBBytes);
 #pragma unroll
           for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-            umma_bf16(d_tmem, sw128_desc(a_addr + kk * UMMA_K * 2), sw128_desc(b_addr + kk * UMMA_K * 2), kIdesc,
-                      (kb | kk) != 0 ? 1u : 0u);
+            if constexpr (PAIR)
+              umma_bf16_pair(d_tmem, sw128_desc(a_addr + kk * UMMA_K * 2), sw128_desc(b_addr + kk * UMMA_K * 2),
+                             kIdesc, (kb | kk) != 0 ? 1u : 0u);
+            else
+              umma_bf16(d_tmem, sw128_desc(a_addr + kk * UMMA_K * 2), sw128_desc(b_addr + kk * UMMA_K * 2), kIdesc,
+                        (kb | kk) != 0 ? 1u : 0u);
           }
-          umma_commit(&empty_bar[stage]);
+          umma_commit_t<PAIR>(&empty_bar[stage]);
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        umma_commit(&tfull_bar[acc]);
+        umma_commit_t<PAIR>(&tfull_bar[acc]);
         if (++acc == 2) {
           acc = 0;
           acc_phase ^= 1u;
@@ -522,8 +675,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         record_error(P.status, kErrTimeout, 202, (int32_t)blockIdx.x, 0);
         s_abort = 1;
       }
-      // every MMA this thread issued has finished before TMEM is released
-      umma_commit(&done_bar);
+      // every MMA this thread issued has finished before TMEM is released (PAIR: the
+      // leader's commit also tells the peer, whose shared and tensor memory they use)
+      if (!PAIR || rank == 0) umma_commit_t<PAIR>(&done_bar);
       const unsigned long long t0 = globaltimer();
       while (!mbar_try_wait<true>(&done_bar, 0u) && globaltimer() - t0 < kTimeoutNs) {
       }
@@ -538,8 +692,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool store_pending = false;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-      const TileInfo ti = decode_tile(tile, s_start, G, G0, s_fam, off);
+    for (int tile = walk0; tile < total; tile += walk_step) {
+      const TileInfo ti = decode_tile<PAIR>(tile, s_start, G, G0, s_fam, off, (int)rank);
       const Family& F = s_fam[ti.fam];
       int got = 0;
       if (lane == 0) got = mbar_wait<true>(&tfull_bar[acc], acc_phase, abort_flag) ? 1 : 0;
@@ -576,10 +730,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (EPI == kSwiglu) {
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const float a0 = __uint_as_float(v[2 * i]), a1 = __uint_as_float(v[2 * i + 1]);
-            const float h0 = a0 * rcp_ftz(1.f + ex2_ftz(-1.4426950408889634f * a0)) * __uint_as_float(u[2 * i]);
-            const float h1 =
-                a1 * rcp_ftz(1.f + ex2_ftz(-1.4426950408889634f * a1)) * __uint_as_float(u[2 * i + 1]);
+            // SiLU(a) * u = a / (1 + 2^(-a log2 e)) * u, two columns per packed op
+            const float2 a = make_float2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+            const float2 m = __fmul2_rn(a, make_float2(-1.4426950408889634f, -1.4426950408889634f));
+            const float2 den = __fadd2_rn(make_float2(ex2_ftz(m.x), ex2_ftz(m.y)), make_float2(1.f, 1.f));
+            const float2 h = __fmul2_rn(__fmul2_rn(a, make_float2(rcp_ftz(den.x), rcp_ftz(den.y))),
+                                        make_float2(__uint_as_float(u[2 * i]), __uint_as_float(u[2 * i + 1])));
+            const float h0 = h.x, h1 = h.y;
             const __nv_bfloat162 hb = __floats2bfloat162_rn(h0, h1);
             pk[i] = *reinterpret_cast<const uint32_t*>(&hb);
           }
@@ -614,21 +771,25 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             float a0 = __uint_as_float(v[2 * i]), a1 = __uint_as_float(v[2 * i + 1]);
+            if (EPI == kGelu) {
+              float2 a = make_float2(a0, a1);
+              if (one_bias) {
+                const uint32_t bw = (&braw[i >> 2].x)[i & 3];  // bf16x2: low half = column 2i
+                a = __fadd2_rn(a, make_float2(__uint_as_float(bw << 16), __uint_as_float(bw & 0xFFFF0000u)));
+              }
+              const float2 g = gelu2_as7126(a);
+              const __nv_bfloat162 hb = __floats2bfloat162_rn(g.x, g.y);
+              pk[i] = *reinterpret_cast<const uint32_t*>(&hb);
+              continue;
+            }
+            float2 a = make_float2(a0, a1);
             if (one_bias) {
               const uint32_t bw = (&braw[i >> 2].x)[i & 3];  // bf16x2: low half = column 2i
-              a0 += __uint_as_float(bw << 16);
-              a1 += __uint_as_float(bw & 0xFFFF0000u);
+              a = __fadd2_rn(a, make_float2(__uint_as_float(bw << 16), __uint_as_float(bw & 0xFFFF0000u)));
             }
-            if (EPI == kGelu) {
-              const __nv_bfloat162 hb = __floats2bfloat162_rn(gelu_as7126(a0), gelu_as7126(a1));
-              pk[i] = *reinterpret_cast<const uint32_t*>(&hb);
-            } else if (EPI == kLinear) {
-              v[2 * i] = __float_as_uint(a0 * gate);
-              v[2 * i + 1] = __float_as_uint(a1 * gate);
-            } else {
-              v[2 * i] = __float_as_uint(a0);
-              v[2 * i + 1] = __float_as_uint(a1);
-            }
+            if (EPI == kLinear) a = __fmul2_rn(a, make_float2(gate, gate));
+            v[2 * i] = __float_as_uint(a.x);
+            v[2 * i + 1] = __float_as_uint(a.y);
           }
         }
         if (use_tma) {
@@ -691,7 +852,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty_bar[acc]);
+      if (lane == 0) {
+        if (!PAIR || rank == 0)
+          mbar_arrive(&tempty_bar[acc]);
+        else  // the leader's MMAs wait for both halves of the accumulator to be drained
+          mbar_arrive_remote(mapa_shared(smem_u32(&tempty_bar[acc]), 0u));
+      }
       if (++acc == 2) {
         acc = 0;
         acc_phase ^= 1u;
@@ -702,9 +868,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncwarp();
   tc_fence_before();
   __syncthreads();
+  // PAIR: neither CTA leaves while the other may still signal its barriers
+  if (PAIR) cluster_sync_all();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, C::kTmemCols);
+    tmem_dealloc_t<PAIR>(tmem_base, C::kTmemCols);
   }
 }
 
@@ -765,13 +933,52 @@ int num_sms() {
 template <int BN, int EPI>
 cudaError_t launch_t(const CUtensorMap (&maps)[8], const Params& P, int64_t max_tiles, cudaStream_t st) {
   using C = Cfg<BN>;
-  auto kern = grouped_gemm_kernel<BN, EPI>;
+  auto kern = grouped_gemm_kernel<BN, EPI, false>;
   static cudaError_t attr = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
   if (attr != cudaSuccess) return attr;
   const int64_t grid = max_tiles < num_sms() ? max_tiles : num_sms();
   if (grid <= 0) return cudaSuccess;
   return launch_pdl(kern, dim3((unsigned)grid), dim3(kThreads), C::kSmem, st, maps[0], maps[1], maps[2], maps[3],
                     maps[4], maps[5], maps[6], maps[7], P);
+}
+
+// CTA-pair form: clusters of two CTAs, one cluster per pair tile up to the number of
+// clusters the GPU holds at once (persistent), launched with the same dependent-launch
+// attribute as the single-CTA form.
+template <int BN, int EPI>
+cudaError_t launch_pair_t(const CUtensorMap (&maps)[8], const Params& P, int64_t max_pair_tiles, cudaStream_t st) {
+  using C = Cfg<BN, true>;
+  auto kern = grouped_gemm_kernel<BN, EPI, true>;
+  static cudaError_t attr = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
+  if (attr != cudaSuccess) return attr;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = C::kSmem;
+  cfg.stream = st;
+  cudaLaunchAttribute at[2];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = 2;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 2;
+  static int resident = [&]() {
+    cudaLaunchConfig_t q = cfg;
+    q.gridDim = dim3((unsigned)num_sms());
+    q.numAttrs = 1;  // cluster shape only
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &q) != cudaSuccess || n <= 0) {
+      (void)cudaGetLastError();
+      n = num_sms() / 2;
+    }
+    return n;
+  }();
+  const int64_t clusters = max_pair_tiles < resident ? max_pair_tiles : resident;
+  if (clusters <= 0) return cudaSuccess;
+  cfg.gridDim = dim3((unsigned)(2 * clusters));
+  return cudaLaunchKernelEx(&cfg, kern, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6], maps[7], P);
 }
 
 template <int EPI>
@@ -830,6 +1037,17 @@ cudaError_t launch_router_logits_tc(const Plan& p, const void* x, const void* w_
   P.expert_off = nullptr;
   P.status = status;
   return launch_bn<kLogits>(bn, maps, P, ceil_div(p.N, BM) * f0.n_tiles * splits, st);
+}
+
+// The down-projection runs on CTA pairs (256-row tiles, half of B per CTA) with
+// 256-wide tiles once the routed experts average at least four 128-row tiles each;
+// smaller batches (decode) keep 128-row tiles, whose padding is half as large. The
+// up-projection stays on single CTAs: its short K leaves it bound by the epilogue,
+// which pairs do not shorten, while an expert's odd last 128-row tile costs a whole
+// pair tile.
+bool use_pair_tiles(const Plan& p, int bn) {
+  const int64_t R = p.max_rows > 0 ? p.max_rows : 1;
+  return bn == 256 && R >= (int64_t)4 * tc::BM * p.E;
 }
 
 // part: bit 0 = up-projections (routed + shared), bit 1 = down-projections.
@@ -899,11 +1117,14 @@ cudaError_t launch_ffn_bf16(const Plan& p, const void* xp, const int32_t* expert
   if (part & 2) {
     const int bn = pick_bn(false, p.d, 0);
     if (!bn) return cudaErrorInvalidValue;
+    const bool pair = use_pair_tiles(p, bn);
+    const int brows = pair ? bn / 2 : bn;
     CUtensorMap maps[8];
     if (!make_map(&maps[0], h, R, p.F, BM)) return cudaErrorInvalidValue;
     for (int i = 1; i < 8; ++i) maps[i] = maps[0];
-    bool ok = make_map(&maps[2], w->w2, p.E * p.d, p.F, bn);
-    if (p.S > 0) ok = ok && make_map(&maps[1], hs, p.N, p.S * p.Fs, BM) && make_map(&maps[3], w->ws2, p.S * p.d, p.Fs, bn);
+    bool ok = make_map(&maps[2], w->w2, p.E * p.d, p.F, brows);
+    if (p.S > 0)
+      ok = ok && make_map(&maps[1], hs, p.N, p.S * p.Fs, BM) && make_map(&maps[3], w->ws2, p.S * p.d, p.Fs, brows);
     ok = ok && make_out_map_f32(&maps[6], yp, R, p.d);
     if (p.S > 0) ok = ok && make_out_map_f32(&maps[7], ys, p.N, p.d);
     if (!ok) return cudaErrorInvalidValue;
@@ -944,8 +1165,14 @@ cudaError_t launch_ffn_bf16(const Plan& p, const void* xp, const int32_t* expert
     }
     P.expert_off = expert_off;
     P.status = status;
-    const int64_t max_tiles = (R / BM + p.E) * f0.n_tiles + (p.S > 0 ? ceil_div(p.N, BM) * P.fam[1].n_tiles : 0);
-    cudaError_t err = launch_bn<kLinear>(bn, maps, P, max_tiles, st);
+    cudaError_t err;
+    if (pair) {
+      const int64_t max_pairs = (R / (2 * BM) + p.E) * f0.n_tiles + (p.S > 0 ? ceil_div(p.N, 2 * BM) * P.fam[1].n_tiles : 0);
+      err = launch_pair_t<256, kLinear>(maps, P, max_pairs, st);
+    } else {
+      const int64_t max_tiles = (R / BM + p.E) * f0.n_tiles + (p.S > 0 ? ceil_div(p.N, BM) * P.fam[1].n_tiles : 0);
+      err = launch_bn<kLinear>(bn, maps, P, max_tiles, st);
+    }
     if (err != cudaSuccess) return err;
   }
   return cudaSuccess;

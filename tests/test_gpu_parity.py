@@ -77,6 +77,16 @@ SMALL = [
        gating="softmax_topk_renorm"),
     wl("f32_E72_k3", dtype="f32", n_tokens=90, d_model=64, d_ff=64, n_experts=72, top_k=3, capacity_factor=1.25,
        gating="topk_softmax", has_bias=True),
+    # 256-wide down-projection tiles with at least four 128-row tiles per expert: the
+    # down-projection runs on CTA pairs (256-row tiles, each CTA staging half of B),
+    # odd tile counts leaving the second CTA's half past the expert's rows; the shared
+    # experts' K-concatenated down-projection on pairs too
+    wl("bf16_pair_gelu_shared_bias", n_tokens=1100, d_model=256, d_ff=512, n_experts=4, top_k=2,
+       capacity_factor=1.25, has_bias=True, n_shared=1, d_ff_shared=256),
+    wl("bf16_pair_swiglu_ec", n_tokens=1030, d_model=256, d_ff=256, n_experts=4, top_k=2, capacity_factor=1.0,
+       gating="expert_choice", act="swiglu", n_shared=2, d_ff_shared=128),
+    wl("bf16_pair_skewed", n_tokens=1200, d_model=256, d_ff=256, n_experts=2, top_k=1, capacity_factor=0.0,
+       gating="softmax_topk_renorm", logit_bias_max=3.0),
 ]
 
 
