@@ -356,49 +356,36 @@ __device__ __forceinline__ float rcp_ftz(float x) {
 }
 
 // GELU(u) = u * Phi(u) = 0.5 u (1 + erf(u / sqrt 2)), with erf from Abramowitz &
-// Stegun, Handbook of Mathematical Functions, formula 7.1.26 (after Hastings):
-// erf(z) = 1 - q(z), q(z) = (a1 t + ... + a5 t^5) exp(-z^2), t = 1 / (1 + p z),
-// z >= 0, |error| <= 1.5e-7 -- far below the bf16 rounding of the stored result.
-// Substituting z = s / sqrt(log2 e) with s = |u| sqrt(log2(e) / 2) gives
-// exp(-z^2) = 2^(-s^2) and t = 1 / (1 + p' s), p' = p / sqrt(log2 e); the
-// polynomial coefficients carry the factor 1/2 of Phi. Since Phi(-|u|) = q/2,
-// GELU(u) = max(u, 0) - |u| q / 2 for either sign of u (no select).
-__device__ __forceinline__ float gelu_as7126(float u) {
-  constexpr float kS = 0.8493218002880191f;  // sqrt(log2(e) / 2)
-  constexpr float kP = 0.2727374808792225f;  // 0.3275911 / sqrt(log2 e)
-  constexpr float kA1 = 0.5f * 0.254829592f, kA2 = 0.5f * -0.284496736f, kA3 = 0.5f * 1.421413741f,
-                  kA4 = 0.5f * -1.453152027f, kA5 = 0.5f * 1.061405429f;
-  const float s = fabsf(u) * kS;
-  const float t = rcp_ftz(fmaf(kP, s, 1.f));
-  float poly = fmaf(kA5, t, kA4);
-  poly = fmaf(poly, t, kA3);
-  poly = fmaf(poly, t, kA2);
-  poly = fmaf(poly, t, kA1);
-  const float hq = (poly * t) * ex2_ftz(-s * s);  // q / 2
-  return fmaf(-fabsf(u), hq, fmaxf(u, 0.f));
-}
-
-// gelu_as7126 on two values at once with the packed fp32x2 multiply / FMA, each of
-// whose halves rounds exactly as its scalar form, so the results are bit-identical
-// to two scalar calls. The polynomial's coefficients enter negated (exact under
-// round-to-nearest), so it yields -q/2 and the last step is |u| (-q/2) + max(u, 0).
-__device__ __forceinline__ float2 gelu2_as7126(float2 u) {
-  constexpr float kS = 0.8493218002880191f;
-  constexpr float kP = 0.2727374808792225f;
-  constexpr float kN1 = -0.5f * 0.254829592f, kN2 = -0.5f * -0.284496736f, kN3 = -0.5f * 1.421413741f,
-                  kN4 = -0.5f * -1.453152027f, kN5 = -0.5f * 1.061405429f;
-  const float2 au = make_float2(fabsf(u.x), fabsf(u.y));
-  const float2 s = __fmul2_rn(au, make_float2(kS, kS));
-  const float2 den = __ffma2_rn(make_float2(kP, kP), s, make_float2(1.f, 1.f));
-  const float2 t = make_float2(rcp_ftz(den.x), rcp_ftz(den.y));
-  float2 pn = __ffma2_rn(make_float2(kN5, kN5), t, make_float2(kN4, kN4));
-  pn = __ffma2_rn(pn, t, make_float2(kN3, kN3));
-  pn = __ffma2_rn(pn, t, make_float2(kN2, kN2));
-  pn = __ffma2_rn(pn, t, make_float2(kN1, kN1));
-  const float2 ss = __fmul2_rn(s, s);
-  const float2 e = make_float2(ex2_ftz(-ss.x), ex2_ftz(-ss.y));
-  const float2 hqn = __fmul2_rn(__fmul2_rn(pn, t), e);  // -q/2
-  return __ffma2_rn(au, hqn, make_float2(fmaxf(u.x, 0.f), fmaxf(u.y, 0.f)));
+// Stegun, Handbook of Mathematical Functions, formula 7.1.28 (after Hastings):
+// erf(z) = 1 - 1 / (1 + a1 z + ... + a6 z^6)^16, z >= 0, |error| <= 3e-7 -- far
+// below the bf16 rounding of the stored result. With z = |u| / sqrt 2 and the
+// factor 1/2 of Phi taken into the polynomial as 2^(1/16):
+//   Phi(-|u|) = 1 / q(|u|)^16,  q(y) = c0 + c1 y + ... + c6 y^6,  c_i = 2^(1/16) a_i 2^(-i/2), a0 = 1,
+// and GELU(u) = max(u, 0) - |u| Phi(-|u|) for either sign of u (no select): six
+// FMAs, four squarings and one reciprocal per value (q^16 overflows to infinity
+// for |u| > ~20, where the reciprocal's zero is the exact limit). Two values per
+// packed fp32x2 multiply / FMA.
+__device__ __forceinline__ float2 gelu2_as7128(float2 u) {
+  constexpr double kR = 1.0442737824274138;  // 2^(1/16)
+  constexpr double kH = 0.7071067811865476;  // 2^(-1/2)
+  constexpr float kC0 = (float)kR, kC1 = (float)(kR * 0.0705230784 * kH),
+                  kC2 = (float)(kR * 0.0422820123 * kH * kH), kC3 = (float)(kR * 0.0092705272 * kH * kH * kH),
+                  kC4 = (float)(kR * 0.0001520143 * kH * kH * kH * kH),
+                  kC5 = (float)(kR * 0.0002765672 * kH * kH * kH * kH * kH),
+                  kC6 = (float)(kR * 0.0000430638 * kH * kH * kH * kH * kH * kH);
+  const float2 y = make_float2(fabsf(u.x), fabsf(u.y));
+  float2 q = __ffma2_rn(make_float2(kC6, kC6), y, make_float2(kC5, kC5));
+  q = __ffma2_rn(q, y, make_float2(kC4, kC4));
+  q = __ffma2_rn(q, y, make_float2(kC3, kC3));
+  q = __ffma2_rn(q, y, make_float2(kC2, kC2));
+  q = __ffma2_rn(q, y, make_float2(kC1, kC1));
+  q = __ffma2_rn(q, y, make_float2(kC0, kC0));
+  q = __fmul2_rn(q, q);  // q^2
+  q = __fmul2_rn(q, q);  // q^4
+  q = __fmul2_rn(q, q);  // q^8
+  q = __fmul2_rn(q, q);  // q^16
+  const float2 nphi = make_float2(rcp_ftz(-q.x), rcp_ftz(-q.y));  // -Phi(-|u|)
+  return __ffma2_rn(y, nphi, make_float2(fmaxf(u.x, 0.f), fmaxf(u.y, 0.f)));
 }
 
 // PAIR: the tile is 256 x BN on a CTA pair; each CTA stages its 128 rows of A and
@@ -777,7 +764,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t bw = (&braw[i >> 2].x)[i & 3];  // bf16x2: low half = column 2i
                 a = __fadd2_rn(a, make_float2(__uint_as_float(bw << 16), __uint_as_float(bw & 0xFFFF0000u)));
               }
-              const float2 g = gelu2_as7126(a);
+              const float2 g = gelu2_as7128(a);
               const __nv_bfloat162 hb = __floats2bfloat162_rn(g.x, g.y);
               pk[i] = *reinterpret_cast<const uint32_t*>(&hb);
               continue;
