@@ -405,6 +405,27 @@ struct TileInfo {
   int fam, g, mt, nt, m, a_row0;
 };
 
+// The work of one CTA (or CTA pair): tiles b, b + W, b + 2W, ... When `split`, the
+// last wave's tiles (fewer than half the CTAs) are cut instead into two halves of
+// BN / 2 output columns, half h of tile nwave * W + j going to CTA 2j + h, so the
+// last wave ends after about half a tile's time.
+struct Walk {
+  int b, W, total, nwave, split;
+  __device__ __forceinline__ bool item(int it, int& tile, int& half) const {
+    half = -1;
+    if (!split || it < nwave) {
+      tile = b + it * W;
+      return tile < total;
+    }
+    if (it == nwave && b < 2 * (total - nwave * W)) {
+      tile = nwave * W + (b >> 1);
+      half = b & 1;
+      return true;
+    }
+    return false;
+  }
+};
+
 // Tile `tile` of the prefix s_start. PAIR: tiles are 256-row pair tiles and the CTA
 // of rank `half` in the pair takes their 128-row half `half`.
 template <bool PAIR = false>
@@ -461,6 +482,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int kStages = C::kStages;
   constexpr int kOutCols = EPI == kSwiglu ? BN / 2 : BN;
   constexpr uint32_t kIdesc = idesc_bf16(PAIR ? 2 * BM : BM, BN);
+  // half tiles (N = BN / 2) for the last wave: one-B-map, whole-width epilogues only
+  constexpr bool kCanSplit = !PAIR && (EPI == kGelu || EPI == kLinear);
+  constexpr uint32_t kIdescHalf = idesc_bf16(BM, BN / 2);
 
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[kStages], empty_bar[kStages], tfull_bar[2], tempty_bar[2], done_bar;
@@ -537,7 +561,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = s_tmem_base;
   const int total = s_start[G];
-  if (walk0 >= total) {  // uniform across the CTA (and the pair): nothing to do, give the TMEM back
+  Walk walk;
+  walk.b = walk0;
+  walk.W = walk_step;
+  walk.total = total;
+  walk.nwave = total / walk_step;
+  walk.split = kCanSplit && total % walk_step != 0 && 2 * (total % walk_step) <= walk_step;
+  int first_tile, first_half;
+  if (!walk.item(0, first_tile, first_half)) {  // uniform across the CTA (and the pair): nothing to do
     if (warp == 1) tmem_dealloc_t<PAIR>(tmem_base, C::kTmemCols);
     return;
   }
@@ -552,7 +583,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int s = 0; s < kStages; ++s) last_parity[s] = -1;
       bool ok = true;
-      for (int tile = walk0; tile < total && ok; tile += walk_step) {
+      for (int it = 0, tile, half; ok && walk.item(it, tile, half); ++it) {
         const TileInfo ti = decode_tile<PAIR>(tile, s_start, G, G0, s_fam, off, (int)rank);
         const Family& F = s_fam[ti.fam];
         const CUtensorMap* ma = pick_map(F.a_map, m0, m1, m2, m3, m4, m5);
@@ -584,6 +615,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             continue;
           }
+          // a half tile stages the whole B tile too (one BN-row copy: two half-height
+          // copies per stage measured slower than the bytes they save)
           mbar_arrive_expect_tx(&full_bar[stage], C::kStageBytes);
           last_parity[stage] = (int32_t)phase;
           tma_load_2d(ma, &full_bar[stage], sA + stage * C::kABytes, (k0 + kb) * BK, ti.a_row0);
@@ -619,9 +652,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
-      for (int tile = walk0; tile < total && ok && (!PAIR || rank == 0); tile += walk_step) {
+      for (int it = 0, tile, half; ok && (!PAIR || rank == 0) && walk.item(it, tile, half); ++it) {
         const TileInfo ti = decode_tile<PAIR>(tile, s_start, G, G0, s_fam, off, (int)rank);
         const int kblocks = s_fam[ti.fam].k_blocks;
+        // a half tile multiplies by B's rows [half * BN/2, (half + 1) * BN/2) into accumulator columns [0, BN/2)
+        const uint32_t idesc = half < 0 ? kIdesc : kIdescHalf;
+        const uint32_t b_off = half < 0 ? 0u : (uint32_t)half * (BN / 2) * BK * 2;
         if (!mbar_wait<false>(&tempty_bar[acc], acc_phase ^ 1u, abort_flag)) {
           ok = false;
           break;
@@ -635,14 +671,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after();
           const uint32_t a_addr = smem_u32(sA + stage * C::kABytes);
-          const uint32_t b_addr = smem_u32(sB + stage * C::kBBytes);
+          const uint32_t b_addr = smem_u32(sB + stage * C::kBBytes) + b_off;
 #pragma unroll
           for (int kk = 0; kk < BK / UMMA_K; ++kk) {
             if constexpr (PAIR)
               umma_bf16_pair(d_tmem, sw128_desc(a_addr + kk * UMMA_K * 2), sw128_desc(b_addr + kk * UMMA_K * 2),
                              kIdesc, (kb | kk) != 0 ? 1u : 0u);
             else
-              umma_bf16(d_tmem, sw128_desc(a_addr + kk * UMMA_K * 2), sw128_desc(b_addr + kk * UMMA_K * 2), kIdesc,
+              umma_bf16(d_tmem, sw128_desc(a_addr + kk * UMMA_K * 2), sw128_desc(b_addr + kk * UMMA_K * 2), idesc,
                         (kb | kk) != 0 ? 1u : 0u);
           }
           umma_commit_t<PAIR>(&empty_bar[stage]);
@@ -679,9 +715,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool store_pending = false;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int tile = walk0; tile < total; tile += walk_step) {
+    for (int it = 0, tile, half; walk.item(it, tile, half); ++it) {
       const TileInfo ti = decode_tile<PAIR>(tile, s_start, G, G0, s_fam, off, (int)rank);
       const Family& F = s_fam[ti.fam];
+      // output columns of this CTA's share of the tile: all, or one half (accumulator columns 0..)
+      const int out_cols = half < 0 ? kOutCols : BN / 2;
+      const int col_shift = half < 0 ? 0 : half * (BN / 2);
       int got = 0;
       if (lane == 0) got = mbar_wait<true>(&tfull_bar[acc], acc_phase, abort_flag) ? 1 : 0;
       got = __shfl_sync(kFull, got, 0);
@@ -701,11 +740,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t tbase = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(q * 32) << 16);
       // H tiles (GELU / SwiGLU) are stored as bf16 for the next GEMM; gate-scaled
       // expert outputs (linear epilogue) stay fp32 until the combine's single rounding.
-      const int64_t out_off = grow * F.ld_out + (int64_t)ti.g * F.out_col_group + (int64_t)ti.nt * kOutCols;
-      const int32_t ox0 = (int32_t)((int64_t)ti.g * F.out_col_group + (int64_t)ti.nt * kOutCols);
+      const int64_t out_off =
+          grow * F.ld_out + (int64_t)ti.g * F.out_col_group + (int64_t)ti.nt * kOutCols + col_shift;
+      const int32_t ox0 = (int32_t)((int64_t)ti.g * F.out_col_group + (int64_t)ti.nt * kOutCols + col_shift);
       const int32_t oy = ti.a_row0 + q * 32;
       const CUtensorMap* omap = ti.fam == 0 ? &o0 : &o1;
-      const int64_t bcol0 = (int64_t)ti.nt * kOutCols;
+      const int64_t bcol0 = (int64_t)ti.nt * kOutCols + col_shift;
       const __nv_bfloat16* bias = F.bias ? F.bias + (int64_t)ti.g * F.bias_group : nullptr;
       float gate = 1.f;
       if (EPI == kLinear && F.row_gate && valid) gate = F.row_gate[grow];
@@ -830,7 +870,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       // chunks c = part*32, part*32 + 32*kEpiParts, ...
       uint32_t va[32], ua[32];
-      for (int c = part * 32; c < kOutCols; c += 32 * kEpiParts) {
+      for (int c = part * 32; c < out_cols; c += 32 * kEpiParts) {
         tmem_ld32(tbase + (uint32_t)c, va);
         if (EPI == kSwiglu) tmem_ld32(tbase + (uint32_t)(BN / 2 + c), ua);
         tmem_ld_wait(va);

@@ -87,6 +87,13 @@ SMALL = [
        gating="expert_choice", act="swiglu", n_shared=2, d_ff_shared=128),
     wl("bf16_pair_skewed", n_tokens=1200, d_model=256, d_ff=256, n_experts=2, top_k=1, capacity_factor=0.0,
        gating="softmax_topk_renorm", logit_bias_max=3.0),
+    # more tiles than CTAs with a last wave at most half full: its tiles are cut into
+    # two halves of the tile's columns on two CTAs (183 tiles: up 256 -> 128-column and
+    # down 64 -> 32-column halves; 192 tiles: up 64 -> 32, down 256 -> 128 on single CTAs)
+    wl("bf16_tail_split", n_tokens=11392, d_model=64, d_ff=256, n_experts=8, top_k=2, capacity_factor=0.0,
+       has_bias=True),
+    wl("bf16_tail_split_down256", n_tokens=10000, d_model=256, d_ff=64, n_experts=64, top_k=2,
+       capacity_factor=0.0, gating="softmax_topk_renorm"),
 ]
 
 
