@@ -16,7 +16,8 @@
 //                             accumulator)
 // A group's rows come from the device-side expert offsets, so no host sync is
 // needed; every CTA builds the same tile prefix over the groups and walks tiles
-// blockIdx.x, blockIdx.x + gridDim.x, ... (persistent, one CTA per SM).
+// blockIdx.x, blockIdx.x + gridDim.x, ... (persistent, one CTA per SM); a last wave
+// that would keep at most half the CTAs busy is cut into half-width tiles instead.
 //
 // Tile 128 x BN x 64, K-major operands in 128-byte-swizzled shared memory.
 // Warp roles: warp 0 issues TMA loads into a STAGES-deep ring, warp 1 issues
