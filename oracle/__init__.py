@@ -46,7 +46,7 @@ class OracleConfig(ctypes.Structure):
         ("n_experts", ctypes.c_int64), ("n_shared", ctypes.c_int64), ("d_ff_shared", ctypes.c_int64),
         ("top_k", ctypes.c_int64), ("capacity_factor", ctypes.c_double), ("gating", ctypes.c_int32),
         ("act", ctypes.c_int32), ("has_bias", ctypes.c_int32), ("dtype", ctypes.c_int32),
-        ("aux_alpha", ctypes.c_double), ("mimic_bf16", ctypes.c_int32), ("pad_", ctypes.c_int32),
+        ("aux_alpha", ctypes.c_double), ("mimic_bf16", ctypes.c_int32), ("passthrough", ctypes.c_int32),
     ]
 
 
@@ -73,6 +73,8 @@ class Oracle:
         lib.oracle_gates.argtypes = [_P, _P, _P, _P]
         lib.oracle_assign.argtypes = [_P, _P, _I64, _P, _P, _P, _P]
         lib.oracle_assign.restype = _I64
+        lib.oracle_assign_shard.argtypes = [_P, _P, _I64, _P, _P, _P, _P, _P]
+        lib.oracle_assign_shard.restype = _I64
         lib.oracle_expert_choice.argtypes = [_P, _P, _I64, _P]
         lib.oracle_stats.argtypes = [_P, _P, _P, _P, _P, _P]
         lib.oracle_expert_apply.argtypes = [_P, _P, ctypes.c_int32, _I64, _P, _P]
@@ -97,7 +99,8 @@ class Oracle:
                  n_shared=w.n_shared, d_ff_shared=w.d_ff_shared, top_k=w.top_k,
                  capacity_factor=w.capacity_factor, gating=GATING[w.gating], act=ACT[w.act],
                  has_bias=int(bool(w.has_bias)), dtype=0 if w.dtype == "f32" else 1,
-                 aux_alpha=w.aux_alpha, mimic_bf16=int(mimic_bf16))
+                 aux_alpha=w.aux_alpha, mimic_bf16=int(mimic_bf16),
+                 passthrough=int(bool(getattr(w, "drop_passthrough", False))))
         g.update(over)
         return OracleConfig(**g)
 
@@ -152,6 +155,21 @@ class Oracle:
         kept = np.empty(E, np.int32)
         dropped = self.lib.oracle_assign(ctypes.byref(cfg), self._ptr(idx), cap, self._ptr(row_of),
                                          self._ptr(off), self._ptr(counts), self._ptr(kept))
+        return dict(row_of=row_of, expert_off=off, counts=counts, kept=kept, dropped=int(dropped))
+
+    def assign_shard(self, cfg, idx: np.ndarray, cap: int, base: np.ndarray) -> Dict[str, np.ndarray]:
+        """oracle_assign for one contiguous token shard whose experts already hold
+        ``base[e]`` assignments from earlier tokens of the batch."""
+        idx = np.ascontiguousarray(idx, np.int32)
+        base = np.ascontiguousarray(base, np.int32)
+        E = cfg.n_experts
+        row_of = np.empty(idx.shape, np.int32)
+        off = np.empty(E + 1, np.int32)
+        counts = np.empty(E, np.int32)
+        kept = np.empty(E, np.int32)
+        dropped = self.lib.oracle_assign_shard(ctypes.byref(cfg), self._ptr(idx), cap, self._ptr(base),
+                                               self._ptr(row_of), self._ptr(off), self._ptr(counts),
+                                               self._ptr(kept))
         return dict(row_of=row_of, expert_off=off, counts=counts, kept=kept, dropped=int(dropped))
 
     def expert_choice(self, cfg, keys: np.ndarray, cap: int) -> np.ndarray:

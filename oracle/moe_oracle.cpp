@@ -59,7 +59,8 @@ struct OracleConfig {
   double aux_alpha;
   int32_t mimic_bf16;      // round the hidden activations and the final output to
                            // bf16, the two places a bf16 pipeline must store bf16
-  int32_t pad_;
+  int32_t passthrough;     // a token with no kept expert gets its input added (see
+                           // oracle_combine_tokens)
 };
 
 struct OracleWeights {
@@ -275,6 +276,39 @@ int64_t oracle_assign(const OracleConfig* c, const int32_t* idx, int64_t cap, in
 }
 
 // ---------------------------------------------------------------------------
+// The same capacity rule for one contiguous shard of a batch's tokens: base[e]
+// assignments to expert e come from the tokens before the shard, so the shard's
+// (t, j) has rank base[e] + (its rank among the shard's assignments to e) in the
+// whole batch's token order, and is kept when that rank is below C. Rows number
+// the shard's kept pairs expert by expert, in token order within an expert.
+// [AIG] "Expert capacity" and MoE code (nonzero()[:capacity] over the batch).
+// With base = 0 this is oracle_assign. Returns the shard's dropped count.
+int64_t oracle_assign_shard(const OracleConfig* c, const int32_t* idx, int64_t cap, const int32_t* base,
+                            int32_t* row_of, int32_t* expert_off, int32_t* counts, int32_t* kept) {
+  const int64_t N = c->n_tokens, E = c->n_experts, k = c->top_k;
+  std::vector<int64_t> rank(static_cast<size_t>(N * k));
+  for (int64_t e = 0; e < E; ++e) counts[e] = 0;
+  for (int64_t t = 0; t < N; ++t)
+    for (int64_t j = 0; j < k; ++j) rank[t * k + j] = counts[idx[t * k + j]]++;
+  int64_t dropped = 0;
+  expert_off[0] = 0;
+  for (int64_t e = 0; e < E; ++e) {
+    const int64_t left = std::max<int64_t>(cap - base[e], 0);
+    kept[e] = static_cast<int32_t>(std::min<int64_t>(counts[e], left));
+    dropped += counts[e] - kept[e];
+    expert_off[e + 1] = expert_off[e] + kept[e];
+  }
+  for (int64_t t = 0; t < N; ++t)
+    for (int64_t j = 0; j < k; ++j) {
+      int32_t e = idx[t * k + j];
+      int64_t r = rank[t * k + j];
+      const int64_t global_rank = PLANT(12) ? r : base[e] + r;
+      row_of[t * k + j] = global_rank < cap ? static_cast<int32_t>(expert_off[e] + r) : -1;
+    }
+  return dropped;
+}
+
+// ---------------------------------------------------------------------------
 // Expert choice: every expert takes the C tokens with the largest key
 // (its softmax-over-experts probability), ties to the lower token index, and
 // lists them in ascending token order. [VAN] ExpertChoiceRouter (each expert
@@ -387,7 +421,10 @@ void oracle_expert_apply(const OracleConfig* c, const OracleWeights* w, int32_t 
 // [AIG] y = sum g_i E_i(x) and its MoE code (out[index] += w * expert(x));
 // [VAN] HybridMoE and [STP] SharedExpertMoE add the shared experts with weight 1.
 // A dropped slot adds nothing ([AIG]: dropped tokens pass through the residual,
-// which is outside this layer). Token-choice inputs: idx/gate [N,k], row_of
+// which is outside this layer). With passthrough set, a token left with no kept
+// expert (all its slots dropped; in expert choice, picked by no expert) adds its
+// own input after the shared experts: [VAN] CapacityManagedMoE, "Handle dropped
+// tokens (pass through residual)". Token-choice inputs: idx/gate [N,k], row_of
 // [N,k] (-1 = dropped). Expert-choice inputs: sel [E,C], gate_ec [E,C].
 void oracle_combine_tokens(const OracleConfig* c, const void* x, const OracleWeights* w,
                            const int32_t* idx, const double* gate, const int32_t* row_of,
@@ -405,9 +442,11 @@ void oracle_combine_tokens(const OracleConfig* c, const void* x, const OracleWei
       for (int64_t i = 0; i < d; ++i) sh[i] += y[i];
     }
     for (int64_t i = 0; i < d; ++i) acc[i] = sh[i];
+    int64_t terms = 0;
     auto add_term = [&](int64_t e, double g) {
       oracle_expert_apply(c, w, 0, e, xr.data(), y.data());
       for (int64_t i = 0; i < d; ++i) acc[i] += g * y[i];
+      ++terms;
     };
     if (c->gating == 3) {
       for (int64_t e = 0; e < E; ++e)
@@ -417,6 +456,13 @@ void oracle_combine_tokens(const OracleConfig* c, const void* x, const OracleWei
       for (int64_t j = 0; j < k; ++j)
         if (row_of[t * k + j] >= 0) add_term(idx[t * k + j], gate[t * k + j]);
     }
+    bool pass = c->passthrough && terms == 0;
+    if (PLANT(11) && c->passthrough && c->gating != 3) {  // any dropped slot passes the token through
+      pass = false;
+      for (int64_t j = 0; j < k; ++j) pass = pass || row_of[t * k + j] < 0;
+    }
+    if (pass)
+      for (int64_t i = 0; i < d; ++i) acc[i] += xr[i];
     for (int64_t i = 0; i < d; ++i) out[o * d + i] = store_round(acc[i], c);
   }
 }

@@ -389,7 +389,94 @@ def pin_page_entropy(o):
     assert round(math.log(8), 3) == g["maximum"]
 
 
+def pin_passthrough(o):
+    """Dropped-token pass-through: a token with no kept expert outputs its own input
+    (plus the shared experts) exactly; a token with at least one kept expert is not
+    affected. Logits are set by hand so the drop pattern is known."""
+    N, E, k = 6, 3, 2
+    L = np.zeros((N, E), np.float32)
+    L[:, 0] = 5.0                 # every token's first choice: expert 0
+    L[:3, 1] = 1.0                # tokens 0-2 then expert 1, tokens 3-5 expert 2
+    L[3:, 2] = 1.0
+    for shared in (0, 1):
+        w = wl(n_tokens=N, d_model=8, d_ff=12, n_experts=E, top_k=k, capacity_factor=0.5,
+               n_shared=shared, d_ff_shared=8)
+        t = rand_layer(w, 21)
+        cfg_off = o.config(w)
+        cfg_on = o.config(w, passthrough=1)
+        assert o.capacity(cfg_off) == 2
+        ow = o.weights(t)
+        r = o.route(cfg_off, None, None, logits=L)
+        # expert 0 keeps tokens 0, 1; expert 1 keeps 0, 1 (drops 2); expert 2 keeps 3, 4 (drops 5)
+        kept_any = (r["row_of"] >= 0).any(axis=1)
+        assert kept_any.tolist() == [True, True, False, True, True, False]
+        off = o.outputs(cfg_off, t["x"], ow, r)
+        on = o.outputs(cfg_on, t["x"], ow, r)
+        x64 = t["x"].astype(np.float64)
+        np.testing.assert_array_equal(on[kept_any], off[kept_any])
+        np.testing.assert_array_equal(on[~kept_any], off[~kept_any] + x64[~kept_any])
+        if not shared:
+            np.testing.assert_array_equal(off[~kept_any], 0.0)
+            np.testing.assert_array_equal(on[~kept_any], x64[~kept_any])
+    # expert choice: a token picked by no expert passes through
+    w = wl(n_tokens=8, d_model=8, d_ff=12, n_experts=2, top_k=1, gating="expert_choice", capacity_factor=0.5)
+    t = rand_layer(w, 22)
+    Lec = np.zeros((8, 2), np.float32)
+    Lec[:, 0] = np.arange(8, dtype=np.float32)   # expert 0 prefers late tokens, expert 1 early ones
+    r = o.route(o.config(w), None, None, logits=Lec)
+    picked = np.zeros(8, bool)
+    picked[r["sel"].ravel()] = True
+    assert picked.sum() < 8
+    on = o.outputs(o.config(w, passthrough=1), t["x"], o.weights(t), r)
+    np.testing.assert_array_equal(on[~picked], t["x"].astype(np.float64)[~picked])
+
+
+def pin_assign_shard(o):
+    """Capacity over a batch cut into contiguous shards: each shard assigns its tokens
+    with the earlier shards' per-expert counts as rank base, and the kept pairs and
+    their ranks equal the unsharded assignment; base = 0 is the unsharded rule."""
+    rs = np.random.RandomState(23)
+    for N, E, k, cf, cuts in [(60, 4, 2, 1.0, (20, 45)), (96, 8, 3, 0.75, (32, 64)), (50, 5, 1, 1.25, (1, 49)),
+                              (40, 6, 2, 0.0, (17,))]:
+        L = (rs.standard_normal((N, E)) + np.linspace(0, 2, E)).astype(np.float32)
+        idx = o.topk(L, k)
+        cfg = o.config(wl(n_tokens=N, n_experts=E, top_k=k, capacity_factor=cf))
+        C = o.capacity(cfg)
+        full = o.assign(cfg, idx, C)
+        zero = o.assign_shard(cfg, idx, C, np.zeros(E, np.int32))
+        for key in ("row_of", "expert_off", "counts", "kept", "dropped"):
+            assert np.array_equal(np.asarray(zero[key]), np.asarray(full[key])), key
+        # global (expert, rank) of every kept pair, unsharded
+        ref = {}
+        for tt, jj in zip(*np.nonzero(full["row_of"] >= 0)):
+            e = int(idx[tt, jj])
+            ref[(int(tt), int(jj))] = (e, int(full["row_of"][tt, jj] - full["expert_off"][e]))
+        bounds = (0,) + tuple(cuts) + (N,)
+        base = np.zeros(E, np.int32)
+        got, kept, dropped = {}, np.zeros(E, np.int64), 0
+        for a, b in zip(bounds[:-1], bounds[1:]):
+            cfg_s = o.config(wl(n_tokens=b - a, n_experts=E, top_k=k, capacity_factor=cf))
+            sh = o.assign_shard(cfg_s, np.ascontiguousarray(idx[a:b]), C, base)
+            _check_shard_rows(sh, E)
+            for tt, jj in zip(*np.nonzero(sh["row_of"] >= 0)):
+                e = int(idx[a + tt, jj])
+                got[(int(a + tt), int(jj))] = (e, int(base[e] + sh["row_of"][tt, jj] - sh["expert_off"][e]))
+            kept += sh["kept"]
+            dropped += sh["dropped"]
+            base = base + sh["counts"]
+        assert got == ref
+        assert np.array_equal(kept, full["kept"]) and dropped == full["dropped"]
+        assert np.array_equal(base, full["counts"])
+
+
+def _check_shard_rows(sh, E):
+    """A shard's rows are a bijection onto [0, rows), expert-contiguous."""
+    rows = sh["row_of"][sh["row_of"] >= 0]
+    assert np.array_equal(np.sort(rows), np.arange(int(sh["expert_off"][-1])))
+    assert np.array_equal(np.diff(sh["expert_off"]), sh["kept"])
+
+
 ALL_PINS = [pin_capacity, pin_router_logits, pin_softmax, pin_topk, pin_gates, pin_assign, pin_zero_router,
             pin_uniform_usage, pin_stats_formula, pin_single_expert_is_dense_ffn, pin_activation_zero,
             pin_brute_force, pin_dense_softmax_mixture, pin_expert_choice, pin_bf16_inputs_and_mimic,
-            pin_page_entropy]
+            pin_page_entropy, pin_passthrough, pin_assign_shard]

@@ -4,7 +4,8 @@ The plants (sites marked PLANT(n) in oracle/moe_oracle.cpp) are the kinds of
 error the pins are meant to catch: a dropped bias term, a wrong tie-break, a
 transposed operand, a capacity formula without k, a wrong GELU or SiLU, missing
 renormalisation, reversed dropping order, a missing factor in the aux loss and
-an unsquared z-loss. Only the oracle is planted, on the CPU.
+an unsquared z-loss, a pass-through of tokens that kept an expert, and a shard
+that ignores the earlier shards' counts. Only the oracle is planted, on the CPU.
 """
 import os
 
@@ -24,6 +25,8 @@ PLANTS = {
     8: "dropping keeps the last C tokens",
     9: "aux loss without the factor E",
     10: "z-loss not squared",
+    11: "pass-through for a token with any dropped slot",
+    12: "shard ranks without the earlier shards' counts",
 }
 
 
