@@ -48,7 +48,7 @@
 extern "C" {
 #endif
 
-#define MOE_ABI_VERSION 1
+#define MOE_ABI_VERSION 2
 
 #if defined(__GNUC__)
 #define MOE_API __attribute__((visibility("default")))
@@ -85,7 +85,27 @@ typedef enum moe_act { MOE_ACT_GELU = 0, MOE_ACT_SWIGLU = 1 } moe_act;
 
 typedef enum moe_dtype { MOE_DT_F32 = 0, MOE_DT_BF16 = 1 } moe_dtype;
 
-/* Layer description (plain data, 80 bytes). */
+/* moe_config.flags bits.
+ * MOE_FLAG_DROP_PASSTHROUGH: a token left with no kept (token, expert) row -- every
+ *   one of its k choices dropped over capacity (token choice), or picked by no expert
+ *   (expert choice) -- gets its own input x added to its output, so it passes through
+ *   the layer unchanged apart from the shared experts. [VAN] CapacityManagedMoE,
+ *   "Handle dropped tokens (pass through residual)"; [AIG] "Expert capacity": tokens
+ *   above the limit "pass through unchanged". Off: such a token's routed part is 0 and
+ *   the residual connection is the caller's. */
+#define MOE_FLAG_DROP_PASSTHROUGH 1
+/* MOE_FLAG_GATHER_ROWS (bf16 layers, moe_forward / moe_forward_overlap): the routed
+ *   up-projection loads its A rows straight from x by the permute's row -> token map
+ *   (TMA tile::gather4, four rows per copy) instead of from an expert-contiguous copy,
+ *   so the permute writes only row metadata and the workspace has no xp region
+ *   (max_rows * d * 2 bytes less: 1.9 GB for 16384 tokens, d = 7168, top-8). It costs
+ *   up-projection time: the GEMM re-reads each row tile once per output column tile,
+ *   and each re-read is 32 gathers instead of one tile copy (measured on B300: the
+ *   8192-token d = 512 layer's up-projection 46 -> 133 us, the 16384-token d = 7168
+ *   layer's 8.7 -> 22.2 ms). [AIE] "Gather/scatter outputs from experts". */
+#define MOE_FLAG_GATHER_ROWS 2
+
+/* Layer description (plain data, 96 bytes). */
 typedef struct moe_config {
   int64_t n_tokens;      /* N: tokens (B*T flattened)                                 */
   int64_t d_model;       /* d                                                         */
@@ -102,6 +122,11 @@ typedef struct moe_config {
   int32_t dtype;         /* moe_dtype of x, weights, biases, outputs                  */
   int32_t has_bias;      /* GELU experts: b1/b2 (and bs1/bs2) present                 */
   float aux_alpha;       /* alpha of the auxiliary loss ([AIG]: ~0.01)                */
+  int32_t flags;         /* MOE_FLAG_* bits                                           */
+  int32_t reserved;      /* 0                                                         */
+  int64_t n_tokens_total; /* token-sharded batch: tokens of the whole batch over all
+                            shards (capacity, statistics and kernel shapes follow it);
+                            0 or n_tokens: this call holds the whole batch             */
 } moe_config;
 
 /* Weights, nn.Linear [out, in] layout, all device pointers of cfg->dtype except
@@ -157,12 +182,16 @@ typedef struct moe_workspace_layout {
   size_t expert_off;  /* int32 [E+1]                                            */
   size_t row_token;   /* int32 [max_rows]                                       */
   size_t row_gate;    /* fp32 [max_rows]                                        */
-  size_t xp;          /* dtype [max_rows, d] permuted tokens                    */
+  size_t xp;          /* dtype [max_rows, d] permuted tokens (empty with
+                         MOE_FLAG_GATHER_ROWS)                                   */
   size_t h;           /* dtype [max_rows, F] routed hidden activations          */
   size_t hs;          /* dtype [N, S*Fs] shared hidden activations              */
   size_t yp;          /* fp32 [max_rows, d] gate-scaled expert outputs          */
   size_t ys;          /* fp32 [N, d] sum of shared expert outputs               */
   size_t stats;       /* moe_stats_bytes(E) used when the caller passes none    */
+  size_t stat_acc;    /* router statistic partial sums, moe_stat_acc_bytes(E):
+                         uint64 P_sum[E] (fixed point 2^-40), uint64 lse_sum and
+                         lse2_sum (2^-32, 2^-24), int32 counts[E] (before dropping) */
   size_t scratch;     /* per-kernel partial sums and tile counts                */
   int64_t max_rows;   /* token choice N*k; expert choice E*C                    */
   int64_t capacity;   /* C (token choice without a limit: N)                    */
@@ -177,6 +206,10 @@ MOE_API const char* moe_status_string(moe_status s);
 /* Bytes of the device statistics buffer for E routed experts. */
 MOE_API size_t moe_stats_bytes(int64_t n_experts);
 
+/* Bytes of the router's statistic partial sums for E routed experts (the
+ * moe_workspace_layout.stat_acc region; see moe_permute_shard). */
+MOE_API size_t moe_stat_acc_bytes(int64_t n_experts);
+
 /* Validates cfg (no CUDA call) and returns the workspace size in *bytes. */
 MOE_API moe_status moe_workspace_size(const moe_config* cfg, size_t* bytes);
 
@@ -189,7 +222,9 @@ MOE_API moe_status moe_workspace_init(const moe_config* cfg, void* ws, size_t ws
 
 /* Router, gates and balancing statistics (hot-path steps: router GEMM, softmax,
  * log-sum-exp, top-k, gates, statistics). [STP] "Key Equations"; [AIG] formula and
- * MoE code; [VAN] TokenChoiceRouter / ExpertChoiceRouter.
+ * MoE code; [VAN] TokenChoiceRouter / ExpertChoiceRouter. With a sharded cfg
+ * (n_tokens_total > n_tokens) the statistics stay as partial sums in the workspace
+ * for the shards' exchange (see moe_permute_shard) and stats is not written.
  *  x      [N, d] dtype
  *  idx    token choice: [N, k] int32 expert ids, rank order (largest logit first).
  *         expert choice: [E, C] int32 token ids, ascending within each expert.
@@ -217,6 +252,34 @@ MOE_API moe_status moe_permute(const moe_config* cfg, const void* x, const int32
                        int32_t* tok_rows, int32_t* tok_off, int32_t* expert_off, int32_t* row_token,
                        float* row_gate, void* stats, void* ws, size_t ws_bytes, void* stream);
 
+/* Capacity, dropping and permutation of one shard of a token-sharded batch.
+ * [AIG] "Expert capacity" and MoE code: every expert keeps the first C of its
+ * assignments in token order over the WHOLE batch, so a shard holding tokens
+ * [t0, t0 + N) keeps (t, j) exactly when (assignments to e in earlier shards) +
+ * (rank of (t, j) among this shard's assignments to e) < C, with C from the whole
+ * batch (cfg->n_tokens_total). Token choice only (expert choice ranks every token of
+ * the batch for every expert; sharding it would need a candidate exchange).
+ * The sharded layer, shard r of n_shards holding a contiguous token range in rank order:
+ *   1. moe_route with the sharded cfg: top-k and gates of the shard's tokens; the
+ *      statistic partial sums (moe_workspace_layout.stat_acc: P_sum, lse sums,
+ *      counts before dropping) stay in the workspace, nothing is finalised;
+ *   2. the caller exchanges them (e.g. NCCL): all-gather the int32 counts[E] of every
+ *      shard into shard_counts [n_shards][E] (rank order), and all-reduce (sum) the
+ *      stat_acc region in place: the E + 2 uint64 words as 64-bit integers (fixed
+ *      point, so the sum is exact and independent of the order) and counts[E] as int32;
+ *   3. moe_permute_shard (this call): per-expert rank base from shard_counts, this
+ *      shard's rows, and the router statistics of the whole batch from the exchanged
+ *      sums (f, P, aux, z over n_tokens_total; counts are the batch's); dropped,
+ *      rows and kept in stats are this shard's;
+ *   4. moe_expert_ffn and moe_combine on the shard's rows, as for a whole batch.
+ * The result for each token equals that of the unsharded batch.
+ *  shard_counts  [n_shards][E] int32 device; shard_rank in [0, n_shards).
+ *  Other arguments as moe_permute (tok_rows [N, k], no tok_off). */
+MOE_API moe_status moe_permute_shard(const moe_config* cfg, const void* x, const int32_t* idx, const float* gate,
+                                     const int32_t* shard_counts, int32_t n_shards, int32_t shard_rank, void* xp,
+                                     int32_t* tok_rows, int32_t* expert_off, int32_t* row_token, float* row_gate,
+                                     void* stats, void* ws, size_t ws_bytes, void* stream);
+
 /* Grouped expert FFNs over the expert-contiguous rows, and the shared experts
  * over all tokens ([VAN] SwiGLUExpert / StandardExpert / HybridMoE;
  * [VAN] "Efficient Batched MoE": one grouped computation instead of a loop).
@@ -233,17 +296,35 @@ MOE_API moe_status moe_expert_ffn(const moe_config* cfg, const void* xp, const i
 /* Combine into token order ([AIG] out[index] += w * expert(x); [VAN] HybridMoE):
  * out[t] = ys[t] + sum of yp over the token's rows, in fixed order (token choice:
  * j = 0..k-1 skipping dropped; expert choice: ascending expert id), fp32
- * accumulation and one rounding. Tokens with no kept row get ys[t] (or 0).
+ * accumulation and one rounding. Tokens with no kept row get ys[t] (or 0), plus
+ * x[t] when cfg->flags has MOE_FLAG_DROP_PASSTHROUGH.
  *  yp [max_rows, d] fp32 and ys [N, d] fp32 (may be NULL) as written by moe_expert_ffn;
- *  tok_rows / tok_off as written by moe_permute. out [N, d] dtype. */
+ *  tok_rows / tok_off as written by moe_permute. x [N, d] dtype: the layer input,
+ *  required with MOE_FLAG_DROP_PASSTHROUGH, else ignored (may be NULL).
+ *  out [N, d] dtype. */
 MOE_API moe_status moe_combine(const moe_config* cfg, const void* yp, const int32_t* tok_rows, const int32_t* tok_off,
-                       const void* ys, void* out, void* stream);
+                       const void* ys, const void* x, void* out, void* stream);
 
 /* The whole layer: moe_route -> moe_permute -> moe_expert_ffn -> moe_combine with
  * every intermediate in ws (see moe_workspace_layout_of). out [N, d] dtype.
- * stats: moe_stats buffer or NULL (then written inside ws). No host sync. */
+ * stats: moe_stats buffer or NULL (then written inside ws). No host sync.
+ * A sharded cfg (n_tokens_total > n_tokens) is rejected: see moe_permute_shard. */
 MOE_API moe_status moe_forward(const moe_config* cfg, const void* x, const moe_weights* w, void* out, void* stats,
                        void* ws, size_t ws_bytes, void* stream);
+
+/* moe_forward with the shared experts on a second stream: their up- and
+ * down-projection launches run on side_stream, forked from `stream` by ev_fork and
+ * joined back by ev_join before the combine, so they can overlap the routing and the
+ * permute, which they do not depend on ("Mixture of Experts (MoE)"
+ * (learn.starphix.com), "Communication Optimization": compute the shared experts
+ * while the routed tokens are dispatched). side_ctas > 0 caps the side launches' CTAs
+ * (one per SM), leaving the other SMs to the main stream; 0 = no cap.
+ *  side_stream: a cudaStream_t other than `stream`; ev_fork, ev_join: caller-created
+ *  cudaEvent_t (timing may be disabled), recorded by this call. Same results as
+ *  moe_forward. fp32 layers and layers without shared experts run as moe_forward. */
+MOE_API moe_status moe_forward_overlap(const moe_config* cfg, const void* x, const moe_weights* w, void* out,
+                                       void* stats, void* ws, size_t ws_bytes, void* stream, void* side_stream,
+                                       void* ev_fork, void* ev_join, int32_t side_ctas);
 
 /* moe_forward that also records caller-created CUDA events (cudaEvent_t) on
  * `stream`: events[0] before the first kernel and events[i] after the i-th

@@ -39,6 +39,9 @@
 // copies and MMAs in flight, frees its TMEM and exits.
 #include <cuda.h>
 
+#include <cstdlib>
+
+#include "act.cuh"
 #include "common.cuh"
 #include "internal.h"
 
@@ -79,13 +82,16 @@ struct Family {
   const float* bias_f32;  // kLogits: fp32 per-column bias, or null
   int64_t n_valid;        // kLogits: columns < n_valid are stored
   int32_t tma_out;        // bf16 outputs: store full 32-row blocks through the family's output tensor map
-  int32_t pad2;
+  int32_t gather_n;       // gather_rows: rows of the gathered matrix (bounds of the row ids)
+  const int32_t* gather_rows;  // non-null: A row r of a group is row gather_rows[r] of the a_map matrix,
+                               // loaded with tile::gather4 (a_map has one-row boxes)
 };
 
 struct Params {
   Family fam[2];
   const int32_t* expert_off;
   int32_t* status;
+  unsigned long long wait_ns;  // bound on each pipeline wait (teardown drains keep kTimeoutNs)
 };
 
 // ---- PTX wrappers -----------------------------------------------------------
@@ -138,9 +144,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   }
   return ok != 0;
 }
-// Bounded wait: false after kTimeoutNs or once another role has aborted.
+// Bounded wait: false after limit_ns or once another role has aborted.
 template <bool kSleep>
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int32_t* abort_flag) {
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int32_t* abort_flag,
+                                          unsigned long long limit_ns) {
   if (mbar_try_wait<kSleep>(bar, parity)) return true;
   const unsigned long long t0 = globaltimer();
   while (true) {
@@ -148,7 +155,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     for (int i = 0; i < (kSleep ? 1 : 64); ++i)
       if (mbar_try_wait<kSleep>(bar, parity)) return true;
     if (*abort_flag) return false;
-    if (globaltimer() - t0 > kTimeoutNs) return false;
+    if (globaltimer() - t0 > limit_ns) return false;
   }
 }
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
@@ -160,6 +167,18 @@ __device__ __forceinline__ void tma_load_2d(const CUtensorMap* map, uint64_t* ba
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(
           smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y)
+      : "memory");
+}
+// Four rows of a 2-D tensor map with one-row boxes (rows r0..r3, columns x .. x + box - 1)
+// into four consecutive box rows of shared memory at dst (completion counted on bar).
+// The 128-byte swizzle follows the shared-memory address, so four groups of rows
+// written at 512-byte steps land exactly as one 128-row box would.
+__device__ __forceinline__ void tma_gather4(const CUtensorMap* map, uint64_t* bar, void* dst, int32_t x, int32_t r0,
+                                            int32_t r1, int32_t r2, int32_t r3) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%3, "
+      "%4, %5, %6, %7}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3)
       : "memory");
 }
 // Bulk tensor store smem -> global (bulk-group completion).
@@ -343,50 +362,6 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
 // Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major, M x N.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
-}
-
-__device__ __forceinline__ float ex2_ftz(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-__device__ __forceinline__ float rcp_ftz(float x) {
-  float y;
-  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
-// GELU(u) = u * Phi(u) = 0.5 u (1 + erf(u / sqrt 2)), with erf from Abramowitz &
-// Stegun, Handbook of Mathematical Functions, formula 7.1.28 (after Hastings):
-// erf(z) = 1 - 1 / (1 + a1 z + ... + a6 z^6)^16, z >= 0, |error| <= 3e-7 -- far
-// below the bf16 rounding of the stored result. With z = |u| / sqrt 2 and the
-// factor 1/2 of Phi taken into the polynomial as 2^(1/16):
-//   Phi(-|u|) = 1 / q(|u|)^16,  q(y) = c0 + c1 y + ... + c6 y^6,  c_i = 2^(1/16) a_i 2^(-i/2), a0 = 1,
-// and GELU(u) = max(u, 0) - |u| Phi(-|u|) for either sign of u (no select): six
-// FMAs, four squarings and one reciprocal per value (q^16 overflows to infinity
-// for |u| > ~20, where the reciprocal's zero is the exact limit). Two values per
-// packed fp32x2 multiply / FMA.
-__device__ __forceinline__ float2 gelu2_as7128(float2 u) {
-  constexpr double kR = 1.0442737824274138;  // 2^(1/16)
-  constexpr double kH = 0.7071067811865476;  // 2^(-1/2)
-  constexpr float kC0 = (float)kR, kC1 = (float)(kR * 0.0705230784 * kH),
-                  kC2 = (float)(kR * 0.0422820123 * kH * kH), kC3 = (float)(kR * 0.0092705272 * kH * kH * kH),
-                  kC4 = (float)(kR * 0.0001520143 * kH * kH * kH * kH),
-                  kC5 = (float)(kR * 0.0002765672 * kH * kH * kH * kH * kH),
-                  kC6 = (float)(kR * 0.0000430638 * kH * kH * kH * kH * kH * kH);
-  const float2 y = make_float2(fabsf(u.x), fabsf(u.y));
-  float2 q = __ffma2_rn(make_float2(kC6, kC6), y, make_float2(kC5, kC5));
-  q = __ffma2_rn(q, y, make_float2(kC4, kC4));
-  q = __ffma2_rn(q, y, make_float2(kC3, kC3));
-  q = __ffma2_rn(q, y, make_float2(kC2, kC2));
-  q = __ffma2_rn(q, y, make_float2(kC1, kC1));
-  q = __ffma2_rn(q, y, make_float2(kC0, kC0));
-  q = __fmul2_rn(q, q);  // q^2
-  q = __fmul2_rn(q, q);  // q^4
-  q = __fmul2_rn(q, q);  // q^8
-  q = __fmul2_rn(q, q);  // q^16
-  const float2 nphi = make_float2(rcp_ftz(-q.x), rcp_ftz(-q.y));  // -Phi(-|u|)
-  return __ffma2_rn(y, nphi, make_float2(fmaxf(u.x, 0.f), fmaxf(u.y, 0.f)));
 }
 
 // PAIR: the tile is 256 x BN on a CTA pair; each CTA stages its 128 rows of A and
@@ -576,28 +551,50 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int32_t* abort_flag = &s_abort;
 
   if (warp == 0) {
-    if (lane == 0) {
-      // ---------------- TMA producer ----------------
-      int stage = 0;
-      uint32_t phase = 0;
-      int32_t last_parity[kStages];
+    // ---------------- TMA producer ----------------
+    // Lane 0 waits for free stages and issues the copies; for a gathering family the
+    // 32 lanes issue one tile::gather4 each (4 of the tile's 128 A rows, row ids held in
+    // registers for the tile), after lane 0 has set the stage's expected bytes.
+    int stage = 0;
+    uint32_t phase = 0;
+    int32_t last_parity[kStages];
 #pragma unroll
-      for (int s = 0; s < kStages; ++s) last_parity[s] = -1;
-      bool ok = true;
-      for (int it = 0, tile, half; ok && walk.item(it, tile, half); ++it) {
-        const TileInfo ti = decode_tile<PAIR>(tile, s_start, G, G0, s_fam, off, (int)rank);
-        const Family& F = s_fam[ti.fam];
-        const CUtensorMap* ma = pick_map(F.a_map, m0, m1, m2, m3, m4, m5);
-        const CUtensorMap* mb = pick_map(F.b_map, m0, m1, m2, m3, m4, m5);
-        const CUtensorMap* mb3 = pick_map(F.b3_map, m0, m1, m2, m3, m4, m5);
-        const int k0 = ti.g * F.k_group;  // split-K groups start further along K
-        for (int kb = 0; kb < F.k_blocks; ++kb) {
-          if (!mbar_wait<false>(&empty_bar[stage], phase ^ 1u, abort_flag)) {
-            ok = false;
-            break;
+    for (int s = 0; s < kStages; ++s) last_parity[s] = -1;
+    bool ok = true;
+    for (int it = 0, tile, half; ok && walk.item(it, tile, half); ++it) {
+      const TileInfo ti = decode_tile<PAIR>(tile, s_start, G, G0, s_fam, off, (int)rank);
+      const Family& F = s_fam[ti.fam];
+      const CUtensorMap* ma = pick_map(F.a_map, m0, m1, m2, m3, m4, m5);
+      const CUtensorMap* mb = pick_map(F.b_map, m0, m1, m2, m3, m4, m5);
+      const CUtensorMap* mb3 = pick_map(F.b3_map, m0, m1, m2, m3, m4, m5);
+      const int k0 = ti.g * F.k_group;  // split-K groups start further along K
+      const bool gather = !PAIR && F.gather_rows != nullptr;
+      int32_t gr[4] = {0, 0, 0, 0};
+      if (gather) {
+        // rows past the group's end repeat its first row (their results are not stored)
+        const int row0 = ti.a_row0 - ti.mt * BM;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int r = lane * 4 + i;
+          const int src = ti.mt * BM + r < ti.m ? ti.a_row0 + r : row0;
+          int32_t id = F.gather_rows[src];
+          if (id < 0 || id >= F.gather_n) {
+            record_error(P.status, kErrIndex, 204, src, id);
+            id = 0;
           }
-          const int kseg = kb / F.kseg_blocks;
-          const int kin = k0 + kb - kseg * F.kseg_blocks;
+          gr[i] = id;
+        }
+      }
+      for (int kb = 0; kb < F.k_blocks; ++kb) {
+        int w_ok = 1;
+        if (lane == 0) w_ok = mbar_wait<false>(&empty_bar[stage], phase ^ 1u, abort_flag, P.wait_ns) ? 1 : 0;
+        if (!__shfl_sync(kFull, w_ok, 0)) {
+          ok = false;
+          break;
+        }
+        const int kseg = kb / F.kseg_blocks;
+        const int kin = k0 + kb - kseg * F.kseg_blocks;
+        if (lane == 0) {
           if (PAIR) {
             // both CTAs' copies complete on the leader's full barrier, which expects
             // the bytes of the two halves; B: the leader stages rows [0, BN/2) of the
@@ -610,42 +607,44 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_2d_pair(ma, fb, sA + stage * C::kABytes, (k0 + kb) * BK, ti.a_row0);
             const int by = ti.g * F.b_rows_group + kseg * F.b_rows_kseg + ti.nt * BN + (int)rank * (BN / 2);
             tma_load_2d_pair(mb, fb, sB + stage * C::kBBytes, kin * BK, by);
-            if (++stage == kStages) {
-              stage = 0;
-              phase ^= 1u;
-            }
-            continue;
-          }
-          // a half tile stages the whole B tile too (one BN-row copy: two half-height
-          // copies per stage measured slower than the bytes they save)
-          mbar_arrive_expect_tx(&full_bar[stage], C::kStageBytes);
-          last_parity[stage] = (int32_t)phase;
-          tma_load_2d(ma, &full_bar[stage], sA + stage * C::kABytes, (k0 + kb) * BK, ti.a_row0);
-          if (EPI == kSwiglu) {
-            const int by = ti.g * F.b_rows_group + kseg * F.b_rows_kseg + ti.nt * (BN / 2);
-            tma_load_2d(mb, &full_bar[stage], sB + stage * C::kBBytes, kin * BK, by);
-            tma_load_2d(mb3, &full_bar[stage], sB + stage * C::kBBytes + (BN / 2) * BK * 2, kin * BK, by);
           } else {
-            const int by = ti.g * F.b_rows_group + kseg * F.b_rows_kseg + ti.nt * BN;
-            tma_load_2d(mb, &full_bar[stage], sB + stage * C::kBBytes, kin * BK, by);
-          }
-          if (++stage == kStages) {
-            stage = 0;
-            phase ^= 1u;
+            // a half tile stages the whole B tile too (one BN-row copy: two half-height
+            // copies per stage measured slower than the bytes they save)
+            mbar_arrive_expect_tx(&full_bar[stage], C::kStageBytes);
+            last_parity[stage] = (int32_t)phase;
+            if (!gather) tma_load_2d(ma, &full_bar[stage], sA + stage * C::kABytes, (k0 + kb) * BK, ti.a_row0);
+            if (EPI == kSwiglu) {
+              const int by = ti.g * F.b_rows_group + kseg * F.b_rows_kseg + ti.nt * (BN / 2);
+              tma_load_2d(mb, &full_bar[stage], sB + stage * C::kBBytes, kin * BK, by);
+              tma_load_2d(mb3, &full_bar[stage], sB + stage * C::kBBytes + (BN / 2) * BK * 2, kin * BK, by);
+            } else {
+              const int by = ti.g * F.b_rows_group + kseg * F.b_rows_kseg + ti.nt * BN;
+              tma_load_2d(mb, &full_bar[stage], sB + stage * C::kBBytes, kin * BK, by);
+            }
           }
         }
+        if (gather) {
+          __syncwarp();  // the stage's expected bytes are set before any gathered row lands
+          tma_gather4(ma, &full_bar[stage], sA + stage * C::kABytes + lane * (4 * BK * 2), (k0 + kb) * BK, gr[0],
+                      gr[1], gr[2], gr[3]);
+        }
+        if (++stage == kStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
       }
-      if (!ok) {
-        record_error(P.status, kErrTimeout, 201, (int32_t)blockIdx.x, 0);
-        s_abort = 1;
-        // let our own copies land before the CTA's shared memory goes away
-        for (int s = 0; s < kStages; ++s)
-          if (last_parity[s] >= 0) {
-            const unsigned long long t0 = globaltimer();
-            while (!mbar_try_wait<true>(&full_bar[s], (uint32_t)last_parity[s]) && globaltimer() - t0 < kTimeoutNs) {
-            }
+    }
+    if (!ok && lane == 0) {
+      record_error(P.status, kErrTimeout, 201, (int32_t)blockIdx.x, 0);
+      s_abort = 1;
+      // let our own copies land before the CTA's shared memory goes away (every lane's
+      // gathers of a stage complete on the same barrier as lane 0's copies)
+      for (int s = 0; s < kStages; ++s)
+        if (last_parity[s] >= 0) {
+          const unsigned long long t0 = globaltimer();
+          while (!mbar_try_wait<true>(&full_bar[s], (uint32_t)last_parity[s]) && globaltimer() - t0 < kTimeoutNs) {
           }
-      }
+        }
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -659,14 +658,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         // a half tile multiplies by B's rows [half * BN/2, (half + 1) * BN/2) into accumulator columns [0, BN/2)
         const uint32_t idesc = half < 0 ? kIdesc : kIdescHalf;
         const uint32_t b_off = half < 0 ? 0u : (uint32_t)half * (BN / 2) * BK * 2;
-        if (!mbar_wait<false>(&tempty_bar[acc], acc_phase ^ 1u, abort_flag)) {
+        if (!mbar_wait<false>(&tempty_bar[acc], acc_phase ^ 1u, abort_flag, P.wait_ns)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
         for (int kb = 0; kb < kblocks; ++kb) {
-          if (!mbar_wait<false>(&full_bar[stage], phase, abort_flag)) {
+          if (!mbar_wait<false>(&full_bar[stage], phase, abort_flag, P.wait_ns)) {
             ok = false;
             break;
           }
@@ -723,7 +722,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int out_cols = half < 0 ? kOutCols : BN / 2;
       const int col_shift = half < 0 ? 0 : half * (BN / 2);
       int got = 0;
-      if (lane == 0) got = mbar_wait<true>(&tfull_bar[acc], acc_phase, abort_flag) ? 1 : 0;
+      if (lane == 0) got = mbar_wait<true>(&tfull_bar[acc], acc_phase, abort_flag, P.wait_ns) ? 1 : 0;
       got = __shfl_sync(kFull, got, 0);
       if (!got) {
         if (lane == 0) {
@@ -758,14 +757,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (EPI == kSwiglu) {
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            // SiLU(a) * u = a / (1 + 2^(-a log2 e)) * u, two columns per packed op
-            const float2 a = make_float2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
-            const float2 m = __fmul2_rn(a, make_float2(-1.4426950408889634f, -1.4426950408889634f));
-            const float2 den = __fadd2_rn(make_float2(ex2_ftz(m.x), ex2_ftz(m.y)), make_float2(1.f, 1.f));
-            const float2 h = __fmul2_rn(__fmul2_rn(a, make_float2(rcp_ftz(den.x), rcp_ftz(den.y))),
-                                        make_float2(__uint_as_float(u[2 * i]), __uint_as_float(u[2 * i + 1])));
-            const float h0 = h.x, h1 = h.y;
-            const __nv_bfloat162 hb = __floats2bfloat162_rn(h0, h1);
+            // SiLU(a) * u, two columns per packed op
+            const float2 h = act::silu_mul2(make_float2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])),
+                                            make_float2(__uint_as_float(u[2 * i]), __uint_as_float(u[2 * i + 1])));
+            const __nv_bfloat162 hb = __floats2bfloat162_rn(h.x, h.y);
             pk[i] = *reinterpret_cast<const uint32_t*>(&hb);
           }
         } else {
@@ -805,7 +800,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t bw = (&braw[i >> 2].x)[i & 3];  // bf16x2: low half = column 2i
                 a = __fadd2_rn(a, make_float2(__uint_as_float(bw << 16), __uint_as_float(bw & 0xFFFF0000u)));
               }
-              const float2 g = gelu2_as7128(a);
+              const float2 g = act::gelu2_as7128(a);
               const __nv_bfloat162 hb = __floats2bfloat162_rn(g.x, g.y);
               pk[i] = *reinterpret_cast<const uint32_t*>(&hb);
               continue;
@@ -951,6 +946,19 @@ bool make_out_map_f32(CUtensorMap* m, const void* ptr, int64_t rows, int64_t col
   return make_map_ex(m, ptr, rows, cols, 16, 32, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
+// Bound on each pipeline wait of the single-CTA grouped GEMM: 2 s, or the value of
+// the environment variable MOE_GEMM_WAIT_LIMIT_NS when it is set (read at every
+// launch; lets a test make the waits run out and check that the kernel reports
+// MOE_ERR_TIMEOUT and tears down cleanly). The teardown's waits for copies and MMAs
+// in flight, and every wait of the CTA-pair form, keep the 2 s bound.
+unsigned long long wait_limit_ns() {
+  const char* v = std::getenv("MOE_GEMM_WAIT_LIMIT_NS");
+  if (!v || !*v) return kTimeoutNs;
+  char* end = nullptr;
+  const unsigned long long n = std::strtoull(v, &end, 10);
+  return (end && *end == 0 && n > 0 && n <= kTimeoutNs) ? n : kTimeoutNs;
+}
+
 int num_sms() {
   int dev = 0, n = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 148;
@@ -958,13 +966,16 @@ int num_sms() {
   return n;
 }
 
+// grid_cap > 0: at most this many CTAs (the rest of the SMs stay free for other work).
 template <int BN, int EPI>
-cudaError_t launch_t(const CUtensorMap (&maps)[8], const Params& P, int64_t max_tiles, cudaStream_t st) {
+cudaError_t launch_t(const CUtensorMap (&maps)[8], const Params& P, int64_t max_tiles, cudaStream_t st,
+                     int64_t grid_cap = 0) {
   using C = Cfg<BN>;
   auto kern = grouped_gemm_kernel<BN, EPI, false>;
   static cudaError_t attr = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
   if (attr != cudaSuccess) return attr;
-  const int64_t grid = max_tiles < num_sms() ? max_tiles : num_sms();
+  int64_t grid = max_tiles < num_sms() ? max_tiles : num_sms();
+  if (grid_cap > 0 && grid > grid_cap) grid = grid_cap;
   if (grid <= 0) return cudaSuccess;
   return launch_pdl(kern, dim3((unsigned)grid), dim3(kThreads), C::kSmem, st, maps[0], maps[1], maps[2], maps[3],
                     maps[4], maps[5], maps[6], maps[7], P);
@@ -974,7 +985,8 @@ cudaError_t launch_t(const CUtensorMap (&maps)[8], const Params& P, int64_t max_
 // clusters the GPU holds at once (persistent), launched with the same dependent-launch
 // attribute as the single-CTA form.
 template <int BN, int EPI>
-cudaError_t launch_pair_t(const CUtensorMap (&maps)[8], const Params& P, int64_t max_pair_tiles, cudaStream_t st) {
+cudaError_t launch_pair_t(const CUtensorMap (&maps)[8], const Params& P, int64_t max_pair_tiles, cudaStream_t st,
+                          int64_t grid_cap = 0) {
   using C = Cfg<BN, true>;
   auto kern = grouped_gemm_kernel<BN, EPI, true>;
   static cudaError_t attr = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
@@ -1003,18 +1015,20 @@ cudaError_t launch_pair_t(const CUtensorMap (&maps)[8], const Params& P, int64_t
     }
     return n;
   }();
-  const int64_t clusters = max_pair_tiles < resident ? max_pair_tiles : resident;
+  int64_t clusters = max_pair_tiles < resident ? max_pair_tiles : resident;
+  if (grid_cap > 0 && 2 * clusters > grid_cap) clusters = grid_cap / 2 > 0 ? grid_cap / 2 : 1;
   if (clusters <= 0) return cudaSuccess;
   cfg.gridDim = dim3((unsigned)(2 * clusters));
   return cudaLaunchKernelEx(&cfg, kern, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6], maps[7], P);
 }
 
 template <int EPI>
-cudaError_t launch_bn(int bn, const CUtensorMap (&maps)[8], const Params& P, int64_t max_tiles, cudaStream_t st) {
+cudaError_t launch_bn(int bn, const CUtensorMap (&maps)[8], const Params& P, int64_t max_tiles, cudaStream_t st,
+                      int64_t grid_cap = 0) {
   switch (bn) {
-    case 256: return launch_t<256, EPI>(maps, P, max_tiles, st);
-    case 128: return launch_t<128, EPI>(maps, P, max_tiles, st);
-    default: return launch_t<64, EPI>(maps, P, max_tiles, st);
+    case 256: return launch_t<256, EPI>(maps, P, max_tiles, st, grid_cap);
+    case 128: return launch_t<128, EPI>(maps, P, max_tiles, st, grid_cap);
+    default: return launch_t<64, EPI>(maps, P, max_tiles, st, grid_cap);
   }
 }
 
@@ -1064,24 +1078,30 @@ cudaError_t launch_router_logits_tc(const Plan& p, const void* x, const void* w_
   f0.n_valid = p.E;
   P.expert_off = nullptr;
   P.status = status;
+  P.wait_ns = wait_limit_ns();
   return launch_bn<kLogits>(bn, maps, P, ceil_div(p.N, BM) * f0.n_tiles * splits, st);
 }
 
 // The down-projection runs on CTA pairs (256-row tiles, half of B per CTA) with
-// 256-wide tiles once the routed experts average at least four 128-row tiles each;
-// smaller batches (decode) keep 128-row tiles, whose padding is half as large. The
-// up-projection stays on single CTAs: its short K leaves it bound by the epilogue,
-// which pairs do not shorten, while an expert's odd last 128-row tile costs a whole
-// pair tile.
+// 256-wide tiles once the routed experts average at least eight 128-row tiles each;
+// smaller batches keep 128-row tiles, whose ragged last tile wastes half as much: an
+// expert's odd last 128-row tile costs a whole pair tile, which at four tiles per expert
+// (the 16384-token, 256-expert layer) is ~22 % of the tiles against ~11 % (measured
+// there: 4.08-4.12 ms on pairs, 3.99 ms on single CTAs). The up-projection stays on
+// single CTAs: its epilogue, which pairs do not shorten, bounds it at short K.
 bool use_pair_tiles(const Plan& p, int bn) {
   const int64_t R = p.max_rows > 0 ? p.max_rows : 1;
-  return bn == 256 && R >= (int64_t)4 * tc::BM * p.E;
+  return bn == 256 && R >= (int64_t)8 * tc::BM * p.E;
 }
 
 // part: bit 0 = up-projections (routed + shared), bit 1 = down-projections.
+// gather_rows non-null: the routed up-projection reads its A rows straight from x
+// (row r of the expert-contiguous order is x[gather_rows[r]]) with tile::gather4, and
+// xp is not used.
 cudaError_t launch_ffn_bf16(const Plan& p, const void* xp, const int32_t* expert_off, const float* row_gate,
                             const void* x, const moe_weights* w, void* h, void* hs, void* yp, void* ys,
-                            int32_t* status, cudaStream_t st, int part) {
+                            int32_t* status, cudaStream_t st, int part, const int32_t* gather_rows, int families,
+                            int64_t grid_cap) {
   using namespace tc;
   const int64_t R = p.max_rows > 0 ? p.max_rows : 1;
   if (part & 1) {
@@ -1090,7 +1110,12 @@ cudaError_t launch_ffn_bf16(const Plan& p, const void* xp, const int32_t* expert
     const int oc = p.swiglu ? bn / 2 : bn;
     const int brows = p.swiglu ? bn / 2 : bn;
     CUtensorMap maps[8];
-    if (!make_map(&maps[0], xp, R, p.d, BM)) return cudaErrorInvalidValue;
+    // (a launch of the shared experts alone never reads the routed A map: any valid map)
+    const bool ok_a = !(families & kRoutedFamily) ? make_map(&maps[0], x, p.N, p.d, BM)
+                      : gather_rows ? make_map_ex(&maps[0], x, p.N, p.d, BK, 1, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                                                  CU_TENSOR_MAP_SWIZZLE_128B)
+                                    : make_map(&maps[0], xp, R, p.d, BM);
+    if (!ok_a) return cudaErrorInvalidValue;
     for (int i = 1; i < 8; ++i) maps[i] = maps[0];  // unused slots hold a valid map
     bool ok = make_map(&maps[2], w->w1, p.E * p.F, p.d, brows);
     if (p.swiglu) ok = ok && make_map(&maps[3], w->w3, p.E * p.F, p.d, brows);
@@ -1118,6 +1143,8 @@ cudaError_t launch_ffn_bf16(const Plan& p, const void* xp, const int32_t* expert
     f0.bias = static_cast<const __nv_bfloat16*>(p.bias ? w->b1 : nullptr);
     f0.bias_group = p.F;
     f0.bias_nsum = p.bias ? 1 : 0;
+    f0.gather_rows = gather_rows;
+    f0.gather_n = (int32_t)p.N;
     if (p.S > 0) {
       Family& f1 = P.fam[1];
       f1.groups = (int32_t)p.S;
@@ -1137,9 +1164,13 @@ cudaError_t launch_ffn_bf16(const Plan& p, const void* xp, const int32_t* expert
     }
     P.expert_off = expert_off;
     P.status = status;
-    const int64_t max_tiles = (R / BM + p.E) * f0.n_tiles + (p.S > 0 ? p.S * ceil_div(p.N, BM) * P.fam[1].n_tiles : 0);
-    cudaError_t err = p.swiglu ? launch_bn<kSwiglu>(bn, maps, P, max_tiles, st)
-                               : launch_bn<kGelu>(bn, maps, P, max_tiles, st);
+    P.wait_ns = wait_limit_ns();
+    if (!(families & kRoutedFamily)) f0.groups = 0;
+    if (!(families & kSharedFamily)) P.fam[1].groups = 0;
+    const int64_t max_tiles = (f0.groups ? (R / BM + p.E) * f0.n_tiles : 0) +
+                              (P.fam[1].groups ? p.S * ceil_div(p.N, BM) * P.fam[1].n_tiles : 0);
+    cudaError_t err = p.swiglu ? launch_bn<kSwiglu>(bn, maps, P, max_tiles, st, grid_cap)
+                               : launch_bn<kGelu>(bn, maps, P, max_tiles, st, grid_cap);
     if (err != cudaSuccess) return err;
   }
   if (part & 2) {
@@ -1193,13 +1224,18 @@ cudaError_t launch_ffn_bf16(const Plan& p, const void* xp, const int32_t* expert
     }
     P.expert_off = expert_off;
     P.status = status;
+    P.wait_ns = pair ? kTimeoutNs : wait_limit_ns();  // the pair form keeps the full bound
+    if (!(families & kRoutedFamily)) f0.groups = 0;
+    if (!(families & kSharedFamily)) P.fam[1].groups = 0;
     cudaError_t err;
     if (pair) {
-      const int64_t max_pairs = (R / (2 * BM) + p.E) * f0.n_tiles + (p.S > 0 ? ceil_div(p.N, 2 * BM) * P.fam[1].n_tiles : 0);
-      err = launch_pair_t<256, kLinear>(maps, P, max_pairs, st);
+      const int64_t max_pairs = (f0.groups ? (R / (2 * BM) + p.E) * f0.n_tiles : 0) +
+                                (P.fam[1].groups ? ceil_div(p.N, 2 * BM) * P.fam[1].n_tiles : 0);
+      err = launch_pair_t<256, kLinear>(maps, P, max_pairs, st, grid_cap);
     } else {
-      const int64_t max_tiles = (R / BM + p.E) * f0.n_tiles + (p.S > 0 ? ceil_div(p.N, BM) * P.fam[1].n_tiles : 0);
-      err = launch_bn<kLinear>(bn, maps, P, max_tiles, st);
+      const int64_t max_tiles = (f0.groups ? (R / BM + p.E) * f0.n_tiles : 0) +
+                                (P.fam[1].groups ? ceil_div(p.N, BM) * P.fam[1].n_tiles : 0);
+      err = launch_bn<kLinear>(bn, maps, P, max_tiles, st, grid_cap);
     }
     if (err != cudaSuccess) return err;
   }

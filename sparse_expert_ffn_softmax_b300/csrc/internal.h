@@ -15,6 +15,10 @@ constexpr int kMaxTileTokens = 32;  // a tile is ranked by one warp, one token p
 struct Plan {
   moe_config cfg;
   int64_t N, d, F, E, S, Fs, k;
+  int64_t Ntot;       // tokens of the whole batch (N unless the batch is sharded over calls)
+  bool sharded;       // Ntot > N: this call holds one contiguous token shard of the batch
+  bool passthrough;   // MOE_FLAG_DROP_PASSTHROUGH
+  bool gather;        // MOE_FLAG_GATHER_ROWS (bf16): the up-projection gathers its rows from x
   bool bf16, swiglu, ec, bias;
   int64_t cap;       // C
   int64_t max_rows;  // rows reserved for xp / h / yp
@@ -28,6 +32,7 @@ struct Plan {
   size_t ec_bits;                     // [N][words]
   int64_t rsplit;                     // bf16 router GEMM split along K into this many groups (1: none)
   size_t logits_part;                 // [rsplit][N][E] fp32 partial logits when rsplit > 1
+  size_t rank_base;                   // int32 [E]: assignments to each expert in earlier shards
 };
 
 // K groups of the bf16 logits GEMM (layers with more than 32 experts) for a batch
@@ -55,6 +60,8 @@ inline T* ws_at(void* ws, size_t off) {
 cudaError_t launch_router(const Plan& p, const void* x, const moe_weights* w, int32_t* idx, float* gate,
                           float* logits, float* probs, void* stats, void* ws, cudaStream_t st,
                           int32_t* tile_counts, bool finalize);
+// Router statistics from the workspace's accumulators (which it then zeroes).
+cudaError_t launch_router_stats_finalize(const Plan& p, void* ws, void* stats, cudaStream_t st);
 // True when the router writes the logits to memory before a second kernel reads
 // them (bf16 layers that the fused tensor-core router does not cover).
 bool router_uses_tc(const Plan& p);
@@ -70,11 +77,18 @@ enum PermuteMode { kCountsFromIdx = 0, kCountsFromRouter = 1, kFusedOffsets = 2 
 bool permute_fuses_offsets(const Plan& p);
 cudaError_t launch_ec_select(const Plan& p, const float* probs, int32_t* idx, float* gate, void* ws,
                              cudaStream_t st);
+// xp null: only the row metadata is written (the up-projection gathers the rows from x).
+// shard_counts (token-sharded batch, kCountsFromIdx only): [n_shards][E] assignment
+// counts of every shard before dropping; the ranks of this shard's assignments start
+// after those of shards 0 .. shard_rank - 1.
 cudaError_t launch_permute(const Plan& p, const void* x, const int32_t* idx, const float* gate, void* xp,
                            int32_t* tok_rows, int32_t* tok_off, int32_t* expert_off, int32_t* row_token,
-                           float* row_gate, void* stats, void* ws, cudaStream_t st, PermuteMode mode);
+                           float* row_gate, void* stats, void* ws, cudaStream_t st, PermuteMode mode,
+                           const int32_t* shard_counts = nullptr, int32_t n_shards = 0, int32_t shard_rank = 0);
+// x: the layer input, read for tokens with no kept row when p.passthrough (else unused).
+// pdl false: an ordinary launch (after a cross-stream event wait).
 cudaError_t launch_combine(const Plan& p, const void* yp, const int32_t* tok_rows, const int32_t* tok_off,
-                           const void* ys, void* out, cudaStream_t st);
+                           const void* ys, const void* x, void* out, cudaStream_t st, bool pdl = true);
 
 // ffn_simt.cu (fp32 layers)
 cudaError_t launch_ffn_f32(const Plan& p, const void* xp, const int32_t* expert_off, const float* row_gate,
@@ -82,9 +96,15 @@ cudaError_t launch_ffn_f32(const Plan& p, const void* xp, const int32_t* expert_
                            int32_t* status, cudaStream_t st, int part);
 
 // gemm_tc.cu (bf16 layers, tcgen05)
+// gather_rows non-null: the routed up-projection gathers its rows from x by these row
+// ids (tile::gather4) instead of reading xp. families: kRoutedFamily | kSharedFamily
+// (the routed experts' and the shared experts' tiles of each launch); grid_cap > 0
+// limits the CTAs of each launch (the rest of the SMs stay free for other streams).
+constexpr int kRoutedFamily = 1, kSharedFamily = 2;
 cudaError_t launch_ffn_bf16(const Plan& p, const void* xp, const int32_t* expert_off, const float* row_gate,
                             const void* x, const moe_weights* w, void* h, void* hs, void* yp, void* ys,
-                            int32_t* status, cudaStream_t st, int part);
+                            int32_t* status, cudaStream_t st, int part, const int32_t* gather_rows = nullptr,
+                            int families = kRoutedFamily | kSharedFamily, int64_t grid_cap = 0);
 bool tc_gemm_available();
 // Router logits x W_r^T on the tensor cores (bf16 layers), fp32: splits = 1 writes
 // logits + logit_bias [N, E]; splits > 1 writes [splits][N][E] partial sums over

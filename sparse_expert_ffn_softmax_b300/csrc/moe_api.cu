@@ -39,8 +39,15 @@ moe_status make_plan(const moe_config* c, Plan* p) {
   if (c->gating < 0 || c->gating > 3 || c->act < 0 || c->act > 1 || c->dtype < 0 || c->dtype > 1)
     return MOE_ERR_INVALID_ARG;
   if (!std::isfinite(c->capacity_factor) || !std::isfinite(c->aux_alpha)) return MOE_ERR_INVALID_ARG;
+  if (c->n_tokens_total != 0 && c->n_tokens_total < c->n_tokens) return MOE_ERR_INVALID_ARG;
+  if ((c->flags & ~(int32_t)(MOE_FLAG_DROP_PASSTHROUGH | MOE_FLAG_GATHER_ROWS)) != 0 || c->reserved != 0)
+    return MOE_ERR_INVALID_ARG;
+  p->Ntot = c->n_tokens_total > p->N ? c->n_tokens_total : p->N;
+  p->sharded = p->Ntot > p->N;
+  p->passthrough = (c->flags & MOE_FLAG_DROP_PASSTHROUGH) != 0;
   if (p->k > p->E || p->k > 32 || p->E > 512 || p->S > 64) return MOE_ERR_UNSUPPORTED;
   p->bf16 = c->dtype == MOE_DT_BF16;
+  p->gather = p->bf16 && (c->flags & MOE_FLAG_GATHER_ROWS) != 0;
   p->swiglu = c->act == MOE_ACT_SWIGLU;
   p->ec = c->gating == MOE_GATE_EXPERT_CHOICE;
   p->bias = c->has_bias != 0;
@@ -52,24 +59,30 @@ moe_status make_plan(const moe_config* c, Plan* p) {
   }
   if (p->N * p->k >= (int64_t)1 << 31) return MOE_ERR_UNSUPPORTED;
   if (p->ec && p->N > ((int64_t)1 << 20)) return MOE_ERR_UNSUPPORTED;
-  // capacity: token choice C = ceil(N*k*cf/E) (cf <= 0: no limit); expert choice
-  // C = min(N, ceil(N*k*cf/E)) with cf <= 0 read as 1.
+  // expert choice ranks every token of the batch for every expert: a shard cannot
+  // select without the other shards' candidates
+  if (p->ec && p->sharded) return MOE_ERR_UNSUPPORTED;
+  if (p->Ntot * p->k >= (int64_t)1 << 31) return MOE_ERR_UNSUPPORTED;
+  // capacity of the whole batch: token choice C = ceil(N*k*cf/E) (cf <= 0: no limit);
+  // expert choice C = min(N, ceil(N*k*cf/E)) with cf <= 0 read as 1.
   const double cf = (double)c->capacity_factor;
   if (p->ec) {
     const double cfe = cf > 0 ? cf : 1.0;
     int64_t cap = (int64_t)std::ceil((double)p->N * (double)p->k * cfe / (double)p->E);
     p->cap = cap < p->N ? cap : p->N;
   } else if (cf <= 0) {
-    p->cap = p->N;
+    p->cap = p->Ntot;
   } else {
-    int64_t cap = (int64_t)std::ceil((double)p->N * (double)p->k * cf / (double)p->E);
-    p->cap = cap < p->N ? cap : p->N;
+    int64_t cap = (int64_t)std::ceil((double)p->Ntot * (double)p->k * cf / (double)p->E);
+    p->cap = cap < p->Ntot ? cap : p->Ntot;
   }
   if (p->cap < 0) p->cap = 0;
   p->max_rows = p->ec ? p->E * p->cap : p->N * p->k;
   if (p->max_rows >= (int64_t)1 << 31) return MOE_ERR_UNSUPPORTED;
-  // smaller tiles for smaller batches, so routing and permuting still spread over the SMs
-  p->tile = p->N >= 16384 ? 32 : (p->N >= 4096 ? 16 : 8);
+  // smaller tiles for smaller batches, so routing and permuting still spread over the SMs.
+  // A shard takes the whole batch's choices (tile, K split of the router), so its per-token
+  // arithmetic and its statistic partials are those of the unsharded batch.
+  p->tile = p->Ntot >= 16384 ? 32 : (p->Ntot >= 4096 ? 16 : 8);
   p->tiles = ceil_div(p->N, p->tile);
   p->words = ceil_div(p->E, 32);
 
@@ -92,18 +105,22 @@ moe_status make_plan(const moe_config* c, Plan* p) {
   L.expert_off = take((size_t)(p->E + 1) * 4);
   L.row_token = take((size_t)p->max_rows * 4);
   L.row_gate = take((size_t)p->max_rows * 4);
-  L.xp = take((size_t)p->max_rows * (size_t)p->d * b);
+  // with MOE_FLAG_GATHER_ROWS the up-projection gathers its rows straight from x and
+  // the forward writes no xp
+  L.xp = take(p->gather ? 0 : (size_t)p->max_rows * (size_t)p->d * b);
   L.h = take((size_t)p->max_rows * (size_t)p->F * b);
   L.hs = take((size_t)p->N * (size_t)(p->S * p->Fs) * b);
   L.yp = take((size_t)p->max_rows * (size_t)p->d * 4);  // fp32 for every layer dtype
   L.ys = take(p->S > 0 ? (size_t)p->N * (size_t)p->d * 4 : 0);
   L.stats = take(moe_stats_bytes(p->E));
-  L.scratch = o;
   p->stat_acc = take(stats_acc_bytes(p->E));  // zeroed by moe_workspace_init, reset by each finaliser
+  L.stat_acc = p->stat_acc;
+  L.scratch = o;
+  p->rank_base = take((size_t)p->E * 4);
   p->tile_counts = take((size_t)(p->E * p->tiles) * 4);
   p->tile_base = take((size_t)(p->E * (p->tiles + 1)) * 4);
   p->ec_bits = take((size_t)(p->N * p->words) * 4);
-  p->rsplit = p->bf16 ? router_k_splits(p->N, p->d, p->E) : 1;
+  p->rsplit = p->bf16 ? router_k_splits(p->Ntot, p->d, p->E) : 1;
   p->logits_part = take(p->rsplit > 1 ? (size_t)(p->rsplit * p->N * p->E) * 4 : 0);
   L.total_bytes = o;
   L.max_rows = p->max_rows;
@@ -167,11 +184,12 @@ moe_status do_route(const Plan& p, const void* x, const moe_weights* w, int32_t*
 }
 
 moe_status do_ffn(const Plan& p, const void* xp, const int32_t* expert_off, const float* row_gate, const void* x,
-                  const moe_weights* w, void* yp, void* ys, void* ws, cudaStream_t st, int part) {
+                  const moe_weights* w, void* yp, void* ys, void* ws, cudaStream_t st, int part,
+                  const int32_t* gather_rows = nullptr, int families = kRoutedFamily | kSharedFamily) {
   void* h = ws_at<uint8_t>(ws, p.L.h);
   void* hs = ws_at<uint8_t>(ws, p.L.hs);
   cudaError_t e = p.bf16 ? launch_ffn_bf16(p, xp, expert_off, row_gate, x, w, h, hs, yp, ys, status_ptr(p, ws), st,
-                                           part)
+                                           part, gather_rows, families)
                          : launch_ffn_f32(p, xp, expert_off, row_gate, x, w, h, hs, yp, ys, status_ptr(p, ws), st,
                                           part);
   return cuda_status(e);
@@ -198,6 +216,8 @@ const char* moe_status_string(moe_status s) {
   }
   return "unknown status";
 }
+
+size_t moe_stat_acc_bytes(int64_t n_experts) { return stats_acc_bytes(n_experts < 0 ? 0 : n_experts); }
 
 size_t moe_stats_bytes(int64_t n_experts) {
   if (n_experts < 0) n_experts = 0;
@@ -244,6 +264,12 @@ moe_status moe_route(const moe_config* cfg, const void* x, const moe_weights* w,
   if (p.N == 0) return MOE_OK;
   if (!ok_ptr(x) || !ok_ptr(idx) || !ok_ptr(gate)) return MOE_ERR_INVALID_ARG;
   cudaGetLastError();
+  if (p.sharded) {
+    // one shard of a batch: the statistic partial sums stay in the workspace
+    // (stat_acc) for the exchange; moe_permute_shard finalises them
+    return cuda_status(launch_router(p, x, w, idx, gate, logits, probs, nullptr, ws, (cudaStream_t)stream,
+                                     nullptr, false));
+  }
   return do_route(p, x, w, idx, gate, logits, probs, stats, ws, (cudaStream_t)stream);
 }
 
@@ -256,6 +282,7 @@ moe_status moe_permute(const moe_config* cfg, const void* x, const int32_t* idx,
   if ((s = check_ws(p, ws, ws_bytes)) != MOE_OK) return s;
   if (!ok_opt(stats) || !ok_ptr(expert_off)) return MOE_ERR_INVALID_ARG;
   if (p.ec && !ok_ptr(tok_off)) return MOE_ERR_INVALID_ARG;
+  if (p.sharded) return MOE_ERR_INVALID_ARG;  // a shard needs the other shards' counts: moe_permute_shard
   if (p.N == 0) {
     cudaGetLastError();
     return cuda_status(cudaMemsetAsync(expert_off, 0, (size_t)(p.E + 1) * 4, (cudaStream_t)stream));
@@ -266,6 +293,34 @@ moe_status moe_permute(const moe_config* cfg, const void* x, const int32_t* idx,
   cudaGetLastError();
   return cuda_status(launch_permute(p, x, idx, gate, xp, tok_rows, tok_off, expert_off, row_token, row_gate, stats,
                                     ws, (cudaStream_t)stream, kCountsFromIdx));
+}
+
+moe_status moe_permute_shard(const moe_config* cfg, const void* x, const int32_t* idx, const float* gate,
+                             const int32_t* shard_counts, int32_t n_shards, int32_t shard_rank, void* xp,
+                             int32_t* tok_rows, int32_t* expert_off, int32_t* row_token, float* row_gate, void* stats,
+                             void* ws, size_t ws_bytes, void* stream) {
+  Plan p;
+  moe_status s = make_plan(cfg, &p);
+  if (s != MOE_OK) return s;
+  if ((s = check_ws(p, ws, ws_bytes)) != MOE_OK) return s;
+  if (p.ec) return MOE_ERR_UNSUPPORTED;
+  if (n_shards < 1 || shard_rank < 0 || shard_rank >= n_shards) return MOE_ERR_INVALID_ARG;
+  if (!ok_ptr(shard_counts) || !ok_opt(stats) || !ok_ptr(expert_off)) return MOE_ERR_INVALID_ARG;
+  if (p.N > 0 && (!ok_ptr(x) || !ok_ptr(idx) || !ok_ptr(gate) || !ok_ptr(xp) || !ok_ptr(tok_rows) ||
+                  !ok_ptr(row_token) || !ok_ptr(row_gate)))
+    return MOE_ERR_INVALID_ARG;
+  cudaGetLastError();
+  cudaStream_t st = (cudaStream_t)stream;
+  // the statistics are always finalised (into the workspace's copy when stats is NULL):
+  // finalising also zeroes the partial sums for the next call
+  void* st_buf = stats_or_ws(p, stats, ws);
+  if (p.N == 0) {
+    // an empty shard still finalises the exchanged statistics
+    if (cudaMemsetAsync(expert_off, 0, (size_t)(p.E + 1) * 4, st) != cudaSuccess) return MOE_ERR_CUDA;
+    return cuda_status(launch_router_stats_finalize(p, ws, st_buf, st));
+  }
+  return cuda_status(launch_permute(p, x, idx, gate, xp, tok_rows, nullptr, expert_off, row_token, row_gate, st_buf,
+                                    ws, st, kCountsFromIdx, shard_counts, n_shards, shard_rank));
 }
 
 moe_status moe_expert_ffn(const moe_config* cfg, const void* xp, const int32_t* expert_off, const float* row_gate,
@@ -285,30 +340,30 @@ moe_status moe_expert_ffn(const moe_config* cfg, const void* xp, const int32_t* 
 }
 
 moe_status moe_combine(const moe_config* cfg, const void* yp, const int32_t* tok_rows, const int32_t* tok_off,
-                       const void* ys, void* out, void* stream) {
+                       const void* ys, const void* x, void* out, void* stream) {
   Plan p;
   moe_status s = make_plan(cfg, &p);
   if (s != MOE_OK) return s;
   if (p.N == 0) return MOE_OK;
-  if (!ok_ptr(yp) || !ok_ptr(tok_rows) || !ok_ptr(out) || !ok_opt(ys)) return MOE_ERR_INVALID_ARG;
+  if (!ok_ptr(yp) || !ok_ptr(tok_rows) || !ok_ptr(out) || !ok_opt(ys) || !ok_opt(x)) return MOE_ERR_INVALID_ARG;
   if (p.ec && !ok_ptr(tok_off)) return MOE_ERR_INVALID_ARG;
+  if (p.passthrough && !x) return MOE_ERR_INVALID_ARG;
   cudaGetLastError();
-  return cuda_status(launch_combine(p, yp, tok_rows, tok_off, ys, out, (cudaStream_t)stream));
+  return cuda_status(launch_combine(p, yp, tok_rows, tok_off, ys, x, out, (cudaStream_t)stream));
 }
 
-moe_status moe_forward_traced(const moe_config* cfg, const void* x, const moe_weights* w, void* out, void* stats,
-                              void* ws, size_t ws_bytes, void* stream, void* const* events, int32_t n_events) {
-  Plan p;
-  moe_status s = make_plan(cfg, &p);
-  if (s != MOE_OK) return s;
-  if ((s = check_ws(p, ws, ws_bytes)) != MOE_OK) return s;
-  if ((s = check_weights(p, w, true, true)) != MOE_OK) return s;
-  if (!ok_opt(stats) || (n_events > 0 && !events)) return MOE_ERR_INVALID_ARG;
-  if (p.N == 0) return MOE_OK;
-  if (!ok_ptr(x) || !ok_ptr(out)) return MOE_ERR_INVALID_ARG;
-  if (p.bf16 && !tc_gemm_available()) return MOE_ERR_CUDA;
-  cudaStream_t st = (cudaStream_t)stream;
-  cudaGetLastError();
+namespace {
+
+// Shared experts on a second stream (see moe_forward_overlap): their up- and
+// down-projection launches, forked from `st` and joined back before the combine.
+struct SideStream {
+  cudaStream_t st;
+  cudaEvent_t fork, join;
+  int64_t ctas;
+};
+
+moe_status forward_impl(const Plan& p, const void* x, const moe_weights* w, void* out, void* stats, void* ws,
+                        cudaStream_t st, void* const* events, int32_t n_events, const SideStream* side) {
   int ev = 0;
   auto mark = [&]() -> bool {
     if (ev < n_events && ev < 6) {
@@ -325,10 +380,27 @@ moe_status moe_forward_traced(const moe_config* cfg, const void* x, const moe_we
   int32_t* expert_off = ws_at<int32_t>(ws, L.expert_off);
   int32_t* row_token = ws_at<int32_t>(ws, L.row_token);
   float* row_gate = ws_at<float>(ws, L.row_gate);
-  void* xp = ws_at<uint8_t>(ws, L.xp);
+  // MOE_FLAG_GATHER_ROWS: the up-projection gathers its rows from x by row_token (no xp copy)
+  void* xp = p.gather ? nullptr : ws_at<uint8_t>(ws, L.xp);
+  const int32_t* gather_rows = p.gather ? row_token : nullptr;
   void* yp = ws_at<uint8_t>(ws, L.yp);
   void* ys = p.S > 0 ? ws_at<uint8_t>(ws, L.ys) : nullptr;
   void* st_buf = stats_or_ws(p, stats, ws);
+  moe_status s;
+  // the main stream's GEMM launches: every family, or the routed experts only when the
+  // shared experts run on the side stream
+  const int fams = side ? kRoutedFamily : (kRoutedFamily | kSharedFamily);
+  if (side) {
+    void* h = ws_at<uint8_t>(ws, p.L.h);
+    void* hs = ws_at<uint8_t>(ws, p.L.hs);
+    if (cudaEventRecord(side->fork, st) != cudaSuccess || cudaStreamWaitEvent(side->st, side->fork, 0) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    for (int part = 1; part <= 2; ++part)
+      if (launch_ffn_bf16(p, xp, expert_off, row_gate, x, w, h, hs, yp, ys, status_ptr(p, ws), side->st, part,
+                          nullptr, kSharedFamily, side->ctas) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (cudaEventRecord(side->join, side->st) != cudaSuccess) return MOE_ERR_CUDA;
+  }
   if (!mark()) return MOE_ERR_CUDA;
   int32_t* fused_counts = p.ec ? nullptr : ws_at<int32_t>(ws, p.tile_counts);
   const bool fused_offsets = permute_fuses_offsets(p);
@@ -341,18 +413,62 @@ moe_status moe_forward_traced(const moe_config* cfg, const void* x, const moe_we
                      mode) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (!mark()) return MOE_ERR_CUDA;
-  if ((s = do_ffn(p, xp, expert_off, row_gate, x, w, yp, ys, ws, st, 1)) != MOE_OK) return s;
+  if ((s = do_ffn(p, xp, expert_off, row_gate, x, w, yp, ys, ws, st, 1, gather_rows, fams)) != MOE_OK) return s;
   if (!mark()) return MOE_ERR_CUDA;
-  if ((s = do_ffn(p, xp, expert_off, row_gate, x, w, yp, ys, ws, st, 2)) != MOE_OK) return s;
+  if ((s = do_ffn(p, xp, expert_off, row_gate, x, w, yp, ys, ws, st, 2, gather_rows, fams)) != MOE_OK) return s;
   if (!mark()) return MOE_ERR_CUDA;
-  if (launch_combine(p, yp, tok_rows, tok_off, ys, out, st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (side && cudaStreamWaitEvent(st, side->join, 0) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_combine(p, yp, tok_rows, tok_off, ys, x, out, st, side == nullptr) != cudaSuccess) return MOE_ERR_CUDA;
   if (!mark()) return MOE_ERR_CUDA;
   return MOE_OK;
+}
+
+moe_status forward_checks(const Plan& p, const void* x, const moe_weights* w, void* out, void* stats, void* ws,
+                          size_t ws_bytes) {
+  moe_status s;
+  if (p.sharded) return MOE_ERR_INVALID_ARG;  // a shard exchanges counts between route and permute
+  if ((s = check_ws(p, ws, ws_bytes)) != MOE_OK) return s;
+  if ((s = check_weights(p, w, true, true)) != MOE_OK) return s;
+  if (!ok_opt(stats)) return MOE_ERR_INVALID_ARG;
+  if (p.N == 0) return MOE_OK;
+  if (!ok_ptr(x) || !ok_ptr(out)) return MOE_ERR_INVALID_ARG;
+  if (p.bf16 && !tc_gemm_available()) return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+}  // namespace
+
+moe_status moe_forward_traced(const moe_config* cfg, const void* x, const moe_weights* w, void* out, void* stats,
+                              void* ws, size_t ws_bytes, void* stream, void* const* events, int32_t n_events) {
+  Plan p;
+  moe_status s = make_plan(cfg, &p);
+  if (s != MOE_OK) return s;
+  if ((s = forward_checks(p, x, w, out, stats, ws, ws_bytes)) != MOE_OK) return s;
+  if (n_events > 0 && !events) return MOE_ERR_INVALID_ARG;
+  if (p.N == 0) return MOE_OK;
+  cudaGetLastError();
+  return forward_impl(p, x, w, out, stats, ws, (cudaStream_t)stream, events, n_events, nullptr);
 }
 
 moe_status moe_forward(const moe_config* cfg, const void* x, const moe_weights* w, void* out, void* stats, void* ws,
                        size_t ws_bytes, void* stream) {
   return moe_forward_traced(cfg, x, w, out, stats, ws, ws_bytes, stream, nullptr, 0);
+}
+
+moe_status moe_forward_overlap(const moe_config* cfg, const void* x, const moe_weights* w, void* out, void* stats,
+                               void* ws, size_t ws_bytes, void* stream, void* side_stream, void* ev_fork,
+                               void* ev_join, int32_t side_ctas) {
+  Plan p;
+  moe_status s = make_plan(cfg, &p);
+  if (s != MOE_OK) return s;
+  if ((s = forward_checks(p, x, w, out, stats, ws, ws_bytes)) != MOE_OK) return s;
+  if (!side_stream || side_stream == stream || !ev_fork || !ev_join || side_ctas < 0) return MOE_ERR_INVALID_ARG;
+  if (p.N == 0) return MOE_OK;
+  cudaGetLastError();
+  if (!p.bf16 || p.S == 0)  // nothing to overlap (fp32 layers run their shared experts in line)
+    return forward_impl(p, x, w, out, stats, ws, (cudaStream_t)stream, nullptr, 0, nullptr);
+  SideStream side{(cudaStream_t)side_stream, (cudaEvent_t)ev_fork, (cudaEvent_t)ev_join, side_ctas};
+  return forward_impl(p, x, w, out, stats, ws, (cudaStream_t)stream, nullptr, 0, &side);
 }
 
 moe_status moe_get_device_status(const moe_config* cfg, void* ws, size_t ws_bytes, void* stream,

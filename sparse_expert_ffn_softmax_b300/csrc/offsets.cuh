@@ -54,10 +54,20 @@ __device__ inline void scan_expert_tiles(const int32_t* counts, int32_t* base, i
   if (lane == 0) base[T] = carry;
 }
 
+// Capacity left to this shard by expert e: C minus the assignments to e in earlier
+// shards (rank_base null: the whole batch, C).
+__device__ __forceinline__ int64_t cap_left(int64_t cap, const int32_t* rank_base, int64_t e) {
+  if (!rank_base) return cap;
+  const int64_t c = cap - (int64_t)rank_base[e];
+  return c > 0 ? c : 0;
+}
+
 // Whole block: offsets over E <= 512 experts from the totals tile_base[e][T],
-// and (stats non-null) kept counts and dropping statistics.
+// and (stats non-null) kept counts and dropping statistics. rank_base (nullable):
+// per-expert assignments in earlier shards of a token-sharded batch.
 __device__ inline void offsets_from_totals(const int32_t* tile_base, int64_t E, int64_t T, int64_t cap, int64_t N,
-                                           int64_t k, int32_t* expert_off, void* stats) {
+                                           int64_t k, int32_t* expert_off, void* stats,
+                                           const int32_t* rank_base = nullptr) {
   __shared__ int s_warp[33];
   const int per = (int)ceil_div(E, (int64_t)blockDim.x);  // <= 2 for blockDim >= 256
   const int64_t e0 = (int64_t)threadIdx.x * per;
@@ -66,7 +76,8 @@ __device__ inline void offsets_from_totals(const int32_t* tile_base, int64_t E, 
     const int64_t ee = e0 + i;
     if (ee < E) {
       const int cnt = *((volatile const int32_t*)(tile_base + ee * (T + 1) + T));
-      kept[i] = (int)(cnt < cap ? cnt : cap);
+      const int64_t cl = cap_left(cap, rank_base, ee);
+      kept[i] = (int)(cnt < cl ? cnt : cl);
       ksum += kept[i];
       dsum += cnt - kept[i];
     }

@@ -73,16 +73,34 @@ struct RouterStatsArgs {  // finalise the router statistics from these accumulat
 // for another): kept_e = min(count_e, C), expert_off = exclusive prefix of kept,
 // the dropping statistics and, when given the router partials, the router
 // statistics.
+// n_stats: tokens the router statistics average over (the whole batch when sharded);
+// rank_base: per-expert assignments in earlier shards, or null.
 __global__ void __launch_bounds__(kWarps * 32) scan_offsets_kernel(
     const int32_t* __restrict__ tile_counts, int64_t E, int64_t T, int64_t cap, int64_t N, int64_t k,
     int32_t* __restrict__ tile_base, int32_t* __restrict__ expert_off, void* stats, int32_t* ticket,
-    RouterStatsArgs rs) {
+    RouterStatsArgs rs, int64_t n_stats, const int32_t* __restrict__ rank_base) {
   const int warp = threadIdx.x >> 5;
   const int64_t e = (int64_t)blockIdx.x * kWarps + warp;
   if (e < E) scan_expert_tiles(tile_counts + e * T, tile_base + e * (T + 1), T);
   if (!last_block_ticket(ticket)) return;
-  offsets_from_totals(tile_base, E, T, cap, N, k, expert_off, stats);
-  if (stats && rs.acc.p) finalize_router_stats(rs.acc, N, E, k, cap, 0, rs.alpha, stats);
+  offsets_from_totals(tile_base, E, T, cap, N, k, expert_off, stats, rank_base);
+  if (stats && rs.acc.p) finalize_router_stats(rs.acc, n_stats, E, k, cap, 0, rs.alpha, stats);
+}
+
+// Token-sharded batch: base[e] = assignments to expert e in shards 0 .. rank - 1,
+// from every shard's counts [n_shards][E] (the ranks of this shard's assignments
+// to e start there, in token order across the whole batch).
+__global__ void shard_base_kernel(const int32_t* __restrict__ shard_counts, int32_t n_shards, int32_t rank,
+                                  int64_t E, int32_t* __restrict__ base, int32_t* status) {
+  const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= E) return;
+  int64_t b = 0;
+  for (int32_t r = 0; r < rank && r < n_shards; ++r) b += shard_counts[(int64_t)r * E + e];
+  if (b < 0 || b > 0x7fffffff) {
+    record_error(status, kErrIndex, 105, (int32_t)e, rank);
+    b = 0;
+  }
+  base[e] = (int32_t)b;
 }
 
 // One block per tile of 8-32 tokens. Warp 0 ranks the tile's (token, choice)
@@ -99,13 +117,15 @@ __global__ void __launch_bounds__(kWarps * 32) scan_offsets_kernel(
 // one extra block (blockIdx.x == T) turns the router's accumulators into the
 // router statistics.
 // Otherwise tile_base [E][T+1] and expert_off come from scan_offsets_kernel.
+// rank_base (token-sharded batch, else null): assignments to each expert in earlier
+// shards; (t, j) is kept when rank_base[e] + its rank in this shard < C.
 template <typename DT, bool kFused>
 __global__ void __launch_bounds__(kWarps * 32) scatter_kernel(
     const DT* __restrict__ x, const int32_t* __restrict__ idx, const float* __restrict__ gate,
     const int32_t* __restrict__ counts_or_base, int32_t* __restrict__ expert_off, int64_t N, int64_t d, int64_t k,
     int64_t E, int64_t T, int64_t TT, int64_t cap, DT* __restrict__ xp, int32_t* __restrict__ tok_rows,
     int32_t* __restrict__ row_token, float* __restrict__ row_gate, void* stats, int32_t* status,
-    RouterStatsArgs rs) {
+    RouterStatsArgs rs, const int32_t* __restrict__ rank_base) {
   // blockIdx.y selects a slice of the row's 16-byte chunks: small batches copy
   // their rows with more blocks. Every slice ranks the tile (cheap); slice 0
   // writes the row metadata.
@@ -149,7 +169,8 @@ __global__ void __launch_bounds__(kWarps * 32) scatter_kernel(
     for (int i = 0; i < per && i < 2; ++i)
       if (e0 + i < E) {
         const int tot = s_off[e0 + i];
-        kept[i] = (int)(tot < cap ? tot : cap);
+        const int64_t cl = cap_left(cap, rank_base, e0 + i);
+        kept[i] = (int)(tot < cl ? tot : cl);
         ksum += kept[i];
         dsum += tot - kept[i];
       }
@@ -207,8 +228,8 @@ __global__ void __launch_bounds__(kWarps * 32) scatter_kernel(
         const int32_t e = idx[t * k + j];
         if (e >= 0 && e < E) {
           const int64_t before = kFused ? s_pre[e] : counts_or_base[(int64_t)e * (T + 1) + tile];
-          const int64_t r = before + __popc(msk[e] & lt);
-          if (r < cap) {
+          const int64_t r = before + __popc(msk[e] & lt);  // rank among this shard's assignments to e
+          if (r < cap_left(cap, rank_base, e)) {
             row = (kFused ? s_off[e] : expert_off[e]) + (int32_t)r;
             if (meta) {
               row_token[row] = (int32_t)t;
@@ -224,6 +245,7 @@ __global__ void __launch_bounds__(kWarps * 32) scatter_kernel(
     }
   }
   __syncthreads();
+  if (xp == nullptr) return;  // metadata only: the up-projection gathers the rows from x
   const int64_t nchunk = d / VT::n;
   const int64_t cs = ceil_div(nchunk, (int64_t)gridDim.y);
   const int64_t cbeg = (int64_t)blockIdx.y * cs, cend = cbeg + cs < nchunk ? cbeg + cs : nchunk;
@@ -402,12 +424,15 @@ __global__ void __launch_bounds__(kWarps * 32) copy_rows_csr_kernel(const T* __r
 // accumulation, one rounding to the output type. A lane owns 16 output bytes.
 // The first KU rows of a token are loaded together (all loads in flight before
 // the first add); rows past KU follow one at a time. Same order of additions.
+// x non-null (dropped-token pass-through): a token with no kept row gets x[t]
+// added after ys[t].
 template <typename TO, int KU>
 __global__ void __launch_bounds__(kWarps * 32) combine_kernel(const float* __restrict__ yp,
                                                               const int32_t* __restrict__ tok_rows,
                                                               const int32_t* __restrict__ tok_off,
                                                               const float* __restrict__ ys, int64_t N, int64_t d,
-                                                              int64_t k, TO* __restrict__ out) {
+                                                              int64_t k, TO* __restrict__ out,
+                                                              const TO* __restrict__ x) {
   pdl_wait();
   pdl_launch_next();
   using VO = Vec16<TO>;
@@ -428,6 +453,9 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(const float* __res
       n = k;
     }
     const int32_t my_row = lane < n ? tok_rows[beg + lane] : -1;
+    // no kept row among the first 32 (token choice: all k; expert choice: the list is
+    // non-empty exactly when it has a row, and every listed row is kept)
+    const bool pass = x != nullptr && !__any_sync(kFull, my_row >= 0) && (tok_off == nullptr || n == 0);
     for (int64_t c0 = cbeg; c0 < cend; c0 += 32) {
       const int64_t c = c0 + lane;
       const bool act = c < cend;
@@ -471,6 +499,12 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(const float* __res
           }
         }
       }
+      if (pass && act) {
+        float xv[VN];
+        VO::unpack(__ldg(reinterpret_cast<const uint4*>(x) + t * nchunk + c), xv);
+#pragma unroll
+        for (int i = 0; i < VN; ++i) acc[i] += xv[i];
+      }
       if (act) reinterpret_cast<uint4*>(out)[t * nchunk + c] = VO::pack(acc);
     }
   }
@@ -479,8 +513,16 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(const float* __res
 template <typename T>
 cudaError_t launch_permute_t(const Plan& p, const void* x, const int32_t* idx, const float* gate, void* xp,
                              int32_t* tok_rows, int32_t* tok_off, int32_t* expert_off, int32_t* row_token,
-                             float* row_gate, void* stats, void* ws, cudaStream_t st, PermuteMode mode) {
+                             float* row_gate, void* stats, void* ws, cudaStream_t st, PermuteMode mode,
+                             const int32_t* shard_counts, int32_t n_shards, int32_t shard_rank) {
   int32_t* status = status_ptr(p, ws);
+  int32_t* rank_base = nullptr;
+  if (shard_counts) {
+    if (p.ec || mode != kCountsFromIdx) return cudaErrorInvalidValue;
+    rank_base = ws_at<int32_t>(ws, p.rank_base);
+    shard_base_kernel<<<(unsigned)ceil_div(p.E, 256), 256, 0, st>>>(shard_counts, n_shards, shard_rank, p.E,
+                                                                    rank_base, status);
+  }
   if (p.ec) {
     uint32_t* bits = ws_at<uint32_t>(ws, p.ec_bits);
     cudaError_t err = cudaMemsetAsync(bits, 0, (size_t)(p.N * p.words) * 4, st);
@@ -492,9 +534,11 @@ cudaError_t launch_permute_t(const Plan& p, const void* x, const int32_t* idx, c
     ec_tok_scan_kernel<<<1, 1024, 0, st>>>(bits, p.N, p.E, p.words, p.cap, tok_off, stats);
     ec_fill_kernel<<<(unsigned)ceil_div(p.N, kWarps), kWarps * 32, 0, st>>>(bits, idx, tok_off, p.N, p.words, p.cap,
                                                                             tok_rows);
-    const int64_t blocks = ceil_div(p.N, kWarps) < 148 * 16 ? ceil_div(p.N, kWarps) : 148 * 16;
-    copy_rows_csr_kernel<T><<<(unsigned)blocks, kWarps * 32, 0, st>>>(static_cast<const T*>(x), tok_rows, tok_off,
-                                                                      p.N, p.d, static_cast<T*>(xp));
+    if (xp) {
+      const int64_t blocks = ceil_div(p.N, kWarps) < 148 * 16 ? ceil_div(p.N, kWarps) : 148 * 16;
+      copy_rows_csr_kernel<T><<<(unsigned)blocks, kWarps * 32, 0, st>>>(static_cast<const T*>(x), tok_rows, tok_off,
+                                                                        p.N, p.d, static_cast<T*>(xp));
+    }
     return cudaGetLastError();
   }
   int32_t* tile_counts = ws_at<int32_t>(ws, p.tile_counts);
@@ -504,7 +548,7 @@ cudaError_t launch_permute_t(const Plan& p, const void* x, const int32_t* idx, c
   int64_t slices = ceil_div(2 * 148, p.tiles);
   const int64_t max_slices = ceil_div(nchunk, 32);
   if (slices > max_slices) slices = max_slices;
-  if (slices < 1) slices = 1;
+  if (slices < 1 || xp == nullptr) slices = 1;  // (metadata only: one block per tile)
   if (mode == kFusedOffsets) {
     RouterStatsArgs fin{};
     fin.acc = stats_acc_at(ws_at<uint8_t>(ws, p.stat_acc), p.E);
@@ -513,7 +557,7 @@ cudaError_t launch_permute_t(const Plan& p, const void* x, const int32_t* idx, c
     return launch_pdl(scatter_kernel<T, true>, dim3((unsigned)p.tiles + 1, (unsigned)slices), dim3(kWarps * 32),
                       sc_smem, st, static_cast<const T*>(x), idx, gate, (const int32_t*)tile_counts, expert_off, p.N,
                       p.d, p.k, p.E, (int64_t)p.tiles, p.tile, p.cap, static_cast<T*>(xp), tok_rows, row_token,
-                      row_gate, stats, status, fin);
+                      row_gate, stats, status, fin, (const int32_t*)nullptr);
   }
   if (mode == kCountsFromIdx) {
     const size_t hist_smem = (size_t)kWarps * p.E * 4;
@@ -525,12 +569,17 @@ cudaError_t launch_permute_t(const Plan& p, const void* x, const int32_t* idx, c
     rs.acc = stats_acc_at(ws_at<uint8_t>(ws, p.stat_acc), p.E);
     rs.alpha = p.cfg.aux_alpha;
   }
+  // the router statistics of a sharded batch come from the exchanged partial sums
+  if (shard_counts && stats) {
+    rs.acc = stats_acc_at(ws_at<uint8_t>(ws, p.stat_acc), p.E);
+    rs.alpha = p.cfg.aux_alpha;
+  }
   scan_offsets_kernel<<<(unsigned)ceil_div(p.E, kWarps), kWarps * 32, 0, st>>>(
-      tile_counts, p.E, p.tiles, p.cap, p.N, p.k, tile_base, expert_off, stats, status + 5, rs);
+      tile_counts, p.E, p.tiles, p.cap, p.N, p.k, tile_base, expert_off, stats, status + 5, rs, p.Ntot, rank_base);
   const size_t sc_smem = (size_t)p.E * 4 + (size_t)kMaxTileTokens * p.k * 4;
   scatter_kernel<T, false><<<dim3((unsigned)p.tiles, (unsigned)slices), kWarps * 32, sc_smem, st>>>(
       static_cast<const T*>(x), idx, gate, tile_base, expert_off, p.N, p.d, p.k, p.E, p.tiles, p.tile, p.cap,
-      static_cast<T*>(xp), tok_rows, row_token, row_gate, stats, status, RouterStatsArgs{});
+      static_cast<T*>(xp), tok_rows, row_token, row_gate, stats, status, RouterStatsArgs{}, rank_base);
   return cudaGetLastError();
 }
 
@@ -545,18 +594,27 @@ cudaError_t launch_ec_select(const Plan& p, const float* probs, int32_t* idx, fl
 
 cudaError_t launch_permute(const Plan& p, const void* x, const int32_t* idx, const float* gate, void* xp,
                            int32_t* tok_rows, int32_t* tok_off, int32_t* expert_off, int32_t* row_token,
-                           float* row_gate, void* stats, void* ws, cudaStream_t st, PermuteMode mode) {
+                           float* row_gate, void* stats, void* ws, cudaStream_t st, PermuteMode mode,
+                           const int32_t* shard_counts, int32_t n_shards, int32_t shard_rank) {
   if (p.bf16)
     return launch_permute_t<__nv_bfloat16>(p, x, idx, gate, xp, tok_rows, tok_off, expert_off, row_token, row_gate,
-                                           stats, ws, st, mode);
+                                           stats, ws, st, mode, shard_counts, n_shards, shard_rank);
   return launch_permute_t<float>(p, x, idx, gate, xp, tok_rows, tok_off, expert_off, row_token, row_gate, stats, ws,
-                                 st, mode);
+                                 st, mode, shard_counts, n_shards, shard_rank);
 }
 
 bool permute_fuses_offsets(const Plan& p) { return !p.ec && p.E * p.tiles <= 8192; }
 
+template <typename... KArgs, typename... Args>
+cudaError_t launch_maybe_pdl(bool pdl, void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                             Args... args) {
+  if (pdl) return launch_pdl(kern, grid, block, smem, st, args...);
+  kern<<<grid, block, smem, st>>>(args...);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_combine(const Plan& p, const void* yp, const int32_t* tok_rows, const int32_t* tok_off,
-                           const void* ys, void* out, cudaStream_t st) {
+                           const void* ys, const void* x, void* out, cudaStream_t st, bool pdl) {
   const int64_t blocks = ceil_div(p.N, kWarps) < 148 * 16 ? ceil_div(p.N, kWarps) : 148 * 16;
   const int64_t nchunk = p.d / (p.bf16 ? 8 : 4);
   int64_t slices = ceil_div(4 * 148, blocks);  // small batches: split rows so ~4 blocks per SM combine
@@ -569,18 +627,20 @@ cudaError_t launch_combine(const Plan& p, const void* yp, const int32_t* tok_row
   const float* ypf = static_cast<const float*>(yp);
   // rows loaded together: top-k's k (expert choice: a token has up to E rows, 2 on average for cf 1)
   const int64_t ku = p.ec ? 2 : p.k;
+  const __nv_bfloat16* xb = p.passthrough ? static_cast<const __nv_bfloat16*>(x) : nullptr;
+  const float* xf = p.passthrough ? static_cast<const float*>(x) : nullptr;
   if (p.bf16) {
     __nv_bfloat16* o = static_cast<__nv_bfloat16*>(out);
-    if (ku <= 1) launch_pdl(combine_kernel<__nv_bfloat16, 1>, grid, dim3(kWarps * 32), 0, st, ypf, (const int32_t*)tok_rows, toff, ysf, p.N, p.d, p.k, o);
-    else if (ku <= 2) launch_pdl(combine_kernel<__nv_bfloat16, 2>, grid, dim3(kWarps * 32), 0, st, ypf, (const int32_t*)tok_rows, toff, ysf, p.N, p.d, p.k, o);
-    else if (ku <= 4) launch_pdl(combine_kernel<__nv_bfloat16, 4>, grid, dim3(kWarps * 32), 0, st, ypf, (const int32_t*)tok_rows, toff, ysf, p.N, p.d, p.k, o);
-    else launch_pdl(combine_kernel<__nv_bfloat16, 8>, grid, dim3(kWarps * 32), 0, st, ypf, (const int32_t*)tok_rows, toff, ysf, p.N, p.d, p.k, o);
+    if (ku <= 1) launch_maybe_pdl(pdl, combine_kernel<__nv_bfloat16, 1>, grid, dim3(kWarps * 32), 0, st, ypf, (const int32_t*)tok_rows, toff, ysf, p.N, p.d, p.k, o, xb);
+    else if (ku <= 2) launch_maybe_pdl(pdl, combine_kernel<__nv_bfloat16, 2>, grid, dim3(kWarps * 32), 0, st, ypf, (const int32_t*)tok_rows, toff, ysf, p.N, p.d, p.k, o, xb);
+    else if (ku <= 4) launch_maybe_pdl(pdl, combine_kernel<__nv_bfloat16, 4>, grid, dim3(kWarps * 32), 0, st, ypf, (const int32_t*)tok_rows, toff, ysf, p.N, p.d, p.k, o, xb);
+    else launch_maybe_pdl(pdl, combine_kernel<__nv_bfloat16, 8>, grid, dim3(kWarps * 32), 0, st, ypf, (const int32_t*)tok_rows, toff, ysf, p.N, p.d, p.k, o, xb);
   } else {
     float* o = static_cast<float*>(out);
-    if (ku <= 1) launch_pdl(combine_kernel<float, 1>, grid, dim3(kWarps * 32), 0, st, ypf, (const int32_t*)tok_rows, toff, ysf, p.N, p.d, p.k, o);
-    else if (ku <= 2) launch_pdl(combine_kernel<float, 2>, grid, dim3(kWarps * 32), 0, st, ypf, (const int32_t*)tok_rows, toff, ysf, p.N, p.d, p.k, o);
-    else if (ku <= 4) launch_pdl(combine_kernel<float, 4>, grid, dim3(kWarps * 32), 0, st, ypf, (const int32_t*)tok_rows, toff, ysf, p.N, p.d, p.k, o);
-    else launch_pdl(combine_kernel<float, 8>, grid, dim3(kWarps * 32), 0, st, ypf, (const int32_t*)tok_rows, toff, ysf, p.N, p.d, p.k, o);
+    if (ku <= 1) launch_maybe_pdl(pdl, combine_kernel<float, 1>, grid, dim3(kWarps * 32), 0, st, ypf, (const int32_t*)tok_rows, toff, ysf, p.N, p.d, p.k, o, xf);
+    else if (ku <= 2) launch_maybe_pdl(pdl, combine_kernel<float, 2>, grid, dim3(kWarps * 32), 0, st, ypf, (const int32_t*)tok_rows, toff, ysf, p.N, p.d, p.k, o, xf);
+    else if (ku <= 4) launch_maybe_pdl(pdl, combine_kernel<float, 4>, grid, dim3(kWarps * 32), 0, st, ypf, (const int32_t*)tok_rows, toff, ysf, p.N, p.d, p.k, o, xf);
+    else launch_maybe_pdl(pdl, combine_kernel<float, 8>, grid, dim3(kWarps * 32), 0, st, ypf, (const int32_t*)tok_rows, toff, ysf, p.N, p.d, p.k, o, xf);
   }
   return cudaGetLastError();
 }

@@ -597,7 +597,9 @@ cudaError_t launch_router_mma_t(const Plan& p, RouterArgs a, cudaStream_t st) {
   const int G = p.tile >= 32 ? 2 : 1;  // a block routes a whole number of permute tiles
   const int64_t TB = 16 * G;
   const int64_t blocks = ceil_div(p.N, TB);
-  if (G == 1 && blocks < 148) {  // few groups: more warps split each group's K range
+  // few groups in the batch: more warps split each group's K range (decided on the whole
+  // batch, so a shard sums its logits in the same order as the unsharded batch)
+  if (G == 1 && ceil_div(p.Ntot, TB) < 148) {
     return launch_pdl(router_mma_kernel<NT, KMAX, 16>, dim3((unsigned)blocks), dim3(32 * 16), 0, st, a);
   }
   return launch_pdl(router_mma_kernel<NT, KMAX, 4>, dim3((unsigned)blocks), dim3(32 * 4 * G), 0, st, a);
@@ -622,6 +624,12 @@ bool router_uses_mma(const Plan& p) { return p.bf16 && p.E <= 32 && (p.ec || p.k
 //  - fp32 layers (and bf16 with k > 8): the SIMT router (dot products on the CUDA
 //    cores, one warp per token).
 bool router_uses_tc(const Plan& p) { return p.bf16 && p.E >= kRouterTcMinE; }
+
+cudaError_t launch_router_stats_finalize(const Plan& p, void* ws, void* stats, cudaStream_t st) {
+  router_finalize_kernel<<<1, 512, 0, st>>>(stats_acc_at(ws_at<uint8_t>(ws, p.stat_acc), p.E), p.Ntot, p.E, p.k,
+                                            p.cap, p.ec ? 1 : 0, p.cfg.aux_alpha, stats);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_router(const Plan& p, const void* x, const moe_weights* w, int32_t* idx, float* gate,
                           float* logits, float* probs, void* stats, void* ws, cudaStream_t st,
@@ -666,7 +674,7 @@ cudaError_t launch_router(const Plan& p, const void* x, const moe_weights* w, in
   }
   if (err != cudaSuccess) return err;
   if (finalize) {
-    router_finalize_kernel<<<1, 512, 0, st>>>(a.acc, p.N, p.E, p.k, p.cap, p.ec ? 1 : 0, p.cfg.aux_alpha, stats);
+    router_finalize_kernel<<<1, 512, 0, st>>>(a.acc, p.Ntot, p.E, p.k, p.cap, p.ec ? 1 : 0, p.cfg.aux_alpha, stats);
   }
   return cudaGetLastError();
 }

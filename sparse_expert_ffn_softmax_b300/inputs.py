@@ -52,6 +52,8 @@ class Workload:
     logit_bias_max: float = 0.0  # per-expert logit offset rising linearly from 0 to this value
     aux_alpha: float = 0.01
     seed: int = 0
+    drop_passthrough: bool = False  # a token with no kept expert row gets x added to its output
+    gather_rows: bool = False  # bf16: the up-projection gathers its rows from x (no xp copy)
 
     def replace(self, **kw) -> "Workload":
         return dataclasses.replace(self, **kw)
@@ -80,8 +82,24 @@ WORKLOADS: Dict[str, Workload] = {
                  n_shared=1, d_ff_shared=2048),
         Workload("large_fine_decode", 128, 7168, 2048, 256, 8, 0.0, "softmax_topk", "swiglu", "bf16",
                  n_shared=1, d_ff_shared=2048),
+        # Reduced-expert stand-ins of the two fine-grained layers for profiler captures
+        # that must stay a few GB on the device: the same d, F, k, shared experts and
+        # rows per expert (16384*8/256 = 512; 8192*6/160 ~ 307), 16 routed experts.
+        Workload("large_fine_e16", 1024, 7168, 2048, 16, 8, 0.0, "softmax_topk", "swiglu", "bf16",
+                 n_shared=1, d_ff_shared=2048),
+        Workload("fine_skewed_e16", 832, 5120, 1536, 16, 6, 1.25, "softmax_topk", "swiglu", "bf16",
+                 n_shared=2, d_ff_shared=1536, logit_bias_max=2.0),
+        # The large layer's router at full size (16384 tokens, d = 7168, 256 experts,
+        # top-8) with small experts (F = 128), so its route stage can be captured alone.
+        Workload("large_fine_router", 16384, 7168, 128, 256, 8, 0.0, "softmax_topk", "swiglu", "bf16"),
+        Workload("fine_skewed_router", 8192, 5120, 128, 160, 6, 1.25, "softmax_topk", "swiglu", "bf16",
+                 logit_bias_max=2.0),
     ]
 }
+
+# The layers the benchmark reports, in order (the stand-ins above are for captures only).
+BENCH_WORKLOADS = ["tiny_f32", "small_bf16", "mixtral_prefill", "mixtral_decode", "fine_skewed", "large_fine",
+                   "large_fine_ec", "large_fine_decode"]
 
 
 def _seed_for(seed: int, name: str) -> int:
@@ -113,6 +131,16 @@ def normal(name: str, shape, std: float, dtype: torch.dtype, device, seed: int =
         out[i].copy_(t)
         del t
     return out
+
+
+def expert_slice(name: str, i: int, shape, std: float, dtype: torch.dtype, device, seed: int = 0) -> torch.Tensor:
+    """Slice ``i`` of a stacked weight drawn with ``chunk_dim0`` (the same bits as
+    ``normal(name, (n,) + shape, ..., chunk_dim0=True)[i]``), without drawing the rest."""
+    g = torch.Generator(device=torch.device(device))
+    g.manual_seed(_seed_for(seed, f"{name}[{i}]"))
+    t = torch.randn(tuple(int(s) for s in shape), generator=g, device=device, dtype=torch.float32)
+    t.mul_(std)
+    return t.to(dtype)
 
 
 def make_inputs(w: Workload, device="cpu", with_weights: bool = True,

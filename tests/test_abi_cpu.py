@@ -26,14 +26,15 @@ def test_header_symbols_exported():
 
 
 def test_abi_version_and_strings():
-    assert moe.abi_version() == 1
+    assert moe.abi_version() == 2
     for code in range(7):
         assert moe.status_string(code)
     assert moe.status_string(99) == "unknown status"
 
 
 def test_struct_sizes_match_header():
-    assert ctypes.sizeof(moe.moe_config) == 80
+    assert ctypes.sizeof(moe.moe_config) == 96
+    assert moe.moe_config.n_tokens_total.offset == 88 and moe.moe_config.flags.offset == 80
     assert ctypes.sizeof(moe.moe_weights) == 12 * 8
     assert ctypes.sizeof(moe.moe_stats_header) == 32
     assert moe.stats_bytes(8) == 32 + 16 * 8
@@ -45,7 +46,7 @@ def test_workspace_layout(name):
     cfg = moe.config(w)
     lay = moe.workspace_layout(cfg)
     assert lay.total_bytes == moe.workspace_size(cfg)
-    offs = [getattr(lay, f) for f, _ in moe.moe_workspace_layout._fields_[1:18]]
+    offs = [getattr(lay, f) for f, _ in moe.moe_workspace_layout._fields_[1:19]]
     assert all(o % 256 == 0 for o in offs)
     assert offs == sorted(offs) and offs[-1] <= lay.total_bytes
     if w.gating == "expert_choice":
@@ -56,6 +57,18 @@ def test_workspace_layout(name):
     b = 4 if w.dtype == "f32" else 2
     assert lay.h - lay.xp >= lay.max_rows * w.d_model * b
     assert lay.hs - lay.h >= lay.max_rows * w.d_ff * b
+    if w.dtype == "bf16":  # gathering the up-projection's rows from x: no xp region
+        lay_g = moe.workspace_layout(moe.config(w, flags=moe.FLAG_GATHER_ROWS))
+        assert lay_g.h - lay_g.xp == 256
+        assert lay.total_bytes - lay_g.total_bytes >= lay.max_rows * w.d_model * b - 256
+
+
+def test_sharded_capacity_follows_the_whole_batch():
+    w = WORKLOADS["small_bf16"]
+    lay = moe.workspace_layout(moe.config(w, n_tokens=2048, n_tokens_total=8192))
+    assert lay.capacity == 2560 and lay.max_rows == 2048 * 2
+    assert moe.stat_acc_bytes(8) == 8 * 12 + 16
+    assert lay.stat_acc % 256 == 0 and lay.stat_acc + moe.stat_acc_bytes(8) <= lay.scratch
 
 
 def test_capacity_from_config():
@@ -75,6 +88,10 @@ def test_capacity_from_config():
     (dict(dtype=1, d_model=96), 2),         # bf16 needs d % 64 == 0
     (dict(dtype=1, d_ff=100), 2),
     (dict(capacity_factor=float("nan")), 1),
+    (dict(flags=4), 1),                     # unknown flag bit
+    (dict(reserved=1), 1),
+    (dict(n_tokens_total=10), 1),           # whole batch smaller than the shard
+    (dict(gating=3, n_tokens_total=128), 2),  # expert choice is not sharded
 ])
 def test_config_validation(over, code):
     cfg = moe.config(WORKLOADS["tiny_f32"], **over)
@@ -103,3 +120,14 @@ def test_host_side_argument_errors():
     assert lib.moe_route(ctypes.byref(cfg), fake, ctypes.byref(w), fake, fake, None, None, None, fake, need,
                          None) == 1
     assert lib.moe_workspace_size(None, None) == 1
+    # a sharded batch has no one-call forward or unsharded permute; shard ranks are checked
+    cfg_s = moe.config(WORKLOADS["tiny_f32"], n_tokens=32, n_tokens_total=64)
+    need_s = moe.workspace_size(cfg_s)
+    assert lib.moe_forward(ctypes.byref(cfg_s), fake, ctypes.byref(w), fake, None, fake, need_s, None) == 1
+    assert lib.moe_permute(ctypes.byref(cfg_s), fake, fake, fake, fake, fake, None, fake, fake, fake, None, fake,
+                           need_s, None) == 1
+    assert lib.moe_permute_shard(ctypes.byref(cfg_s), fake, fake, fake, fake, 2, 2, fake, fake, fake, fake, fake,
+                                 None, fake, need_s, None) == 1
+    # pass-through needs the layer input in the combine
+    cfg_p = moe.config(WORKLOADS["tiny_f32"], flags=moe.FLAG_DROP_PASSTHROUGH)
+    assert lib.moe_combine(ctypes.byref(cfg_p), fake, fake, None, None, None, fake, None) == 1

@@ -47,3 +47,38 @@ def test_roof_choice(bench, name, bound):
             assert r["unit"] == "GB/s" and r["achieved"] == pytest.approx(nbytes / 1e-3 / 1e9)
         else:
             assert r["unit"] == "TFLOP/s" and r["achieved"] == pytest.approx(flops / 1e-3 / 1e12)
+
+
+def test_tensor_peak_choice(bench):
+    """Short grouped GEMM launches are measured against the burst bf16 peak, launches of
+    more than a millisecond (power-limited clocks) against the sustained one."""
+    assert bench.tensor_peak(PEAKS, 0.05)[0] == PEAKS["bf16"]
+    assert bench.tensor_peak(PEAKS, 8.0)[0] == PEAKS["bf16_sustained"]
+    r = bench.gemm_roofline(1e12, 1e6, 8e-3, PEAKS)
+    assert r["peak"] == PEAKS["bf16_sustained"] and r["frac_of_burst"] == pytest.approx(r["achieved"] / PEAKS["bf16"])
+
+
+def test_sample_sizes_fit_budget(bench):
+    w = WORKLOADS["large_fine"]
+    n_route, n_ffn = bench.sample_sizes(w, 6.0, (0.02, 1.6, 4, 2))  # 5 ms per routed token, 0.8 s per FFN token
+    assert 8 <= n_route <= w.n_tokens and 2 <= n_ffn <= n_route
+    assert n_route * 0.005 + n_ffn * 0.8 <= 6.0 * 1.05
+
+
+def test_reference_arm_runs_without_the_cuda_library():
+    """--impl reference times the oracle on the host and never loads libmoe_b300.so."""
+    import subprocess
+    import sys
+    code = ("import sys, json; sys.argv=['bench.py','--impl','reference','--workload','tiny_f32','--steps','2',"
+            "'--warmup','1']; import bench; bench.main(); "
+            "maps=open('/proc/self/maps').read(); "
+            "print(json.dumps({'lib': 'libmoe_b300' in maps, "
+            "'pkg': any(m.startswith('sparse_expert_ffn_softmax_b300') for m in sys.modules)}))")
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr
+    import json
+    lines = [json.loads(x) for x in r.stdout.strip().splitlines()]
+    ref, probe = lines[0], lines[-1]
+    assert ref["impl"] == "reference" and ref["config"]["workload"] == "tiny_f32" and ref["value"] > 0
+    assert ref["cpu_baseline"]["cores"] == 1 and ref["cpu_baseline"]["host_cores"] >= 1
+    assert probe == {"lib": False, "pkg": False}

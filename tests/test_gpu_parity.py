@@ -3,8 +3,11 @@
 Small layers are compared in full; they span several 128-row GEMM tiles, a
 ragged last tile, every gate rule, drops, shared experts, GELU and SwiGLU, fp32
 and bf16, the tile widths 64/128/256, and both routers (SIMT dot products;
-tensor-core logits, whole or split along K, with the routing kernel). The workload shapes themselves run at
-full size with routing compared on every token and outputs on sampled tokens.
+tensor-core logits, whole or split along K, with the routing kernel). The
+workload shapes themselves run at full size with routing compared on every
+token; the 8192-token layer and the decode batches compare every output token,
+the larger layers 64 sampled tokens plus the expert rows at every expert
+segment's ends and in the grouped GEMMs' ragged tiles.
 """
 import numpy as np
 import pytest
@@ -47,6 +50,14 @@ SMALL = [
        act="swiglu", n_shared=2, d_ff_shared=128, logit_bias_max=2.0),
     wl("bf16_heavy_drops", n_tokens=1000, d_model=64, d_ff=128, n_experts=8, top_k=2, capacity_factor=0.3,
        logit_bias_max=4.0),
+    # dropped-token pass-through: tokens with no kept choice (or, in expert choice, picked
+    # by no expert) add their input x
+    wl("bf16_drops_passthrough", n_tokens=1000, d_model=64, d_ff=128, n_experts=8, top_k=2, capacity_factor=0.3,
+       logit_bias_max=4.0, drop_passthrough=True),
+    wl("f32_passthrough_shared", dtype="f32", n_tokens=70, capacity_factor=0.4, n_shared=1, d_ff_shared=64,
+       has_bias=True, logit_bias_max=3.0, drop_passthrough=True),
+    wl("bf16_ec_passthrough", n_tokens=256, d_model=128, d_ff=128, n_experts=8, top_k=2, capacity_factor=0.5,
+       gating="expert_choice", act="swiglu", drop_passthrough=True),
     # 16+ token tiles (the router's tile counts and the permute's fused offsets over
     # many blocks): top-2, top-5 of 32 experts with a logit offset, expert choice
     wl("bf16_2k_tokens_B", n_tokens=2100, d_model=128, d_ff=64, n_experts=8, top_k=2, capacity_factor=1.25,
@@ -196,15 +207,73 @@ def test_device_index_check_reports():
     assert moe.get_device_status(cfg, ws) == (0, 0)  # cleared by the read
 
 
-FULL = [("small_bf16", 256), ("mixtral_decode", 6), ("mixtral_prefill", 6), ("fine_skewed", 8),
-        ("large_fine", 4), ("large_fine_ec", 4), ("large_fine_decode", 4)]
+# (workload, output tokens compared: None = every token). The large layers also
+# compare the expert rows of every segment's ends and of the GEMMs' ragged tiles.
+FULL = [("small_bf16", None), ("mixtral_decode", None), ("mixtral_prefill", 64), ("fine_skewed", 64),
+        ("large_fine", 64), ("large_fine_ec", 64), ("large_fine_decode", None)]
 
 
 @pytest.mark.parametrize("name,n_sample", FULL, ids=[f[0] for f in FULL])
 def test_full_size_workloads(name, n_sample):
     w = WORKLOADS[name]
     layer, t, res = run_gpu(w)
-    rep = check(w, t, res, n_sample=n_sample)
+    rep = check(w, t, res, n_sample=n_sample, raw_bar=True)
     print(name, rep)
     del layer, t, res
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("name,caps", [("overlap_small", (0, 64)), ("fine_skewed", (0, 96))])
+def test_forward_overlap_matches_forward(name, caps):
+    """Shared experts on a second stream (forked at the start of the forward, joined
+    before the combine) give the one-stream forward's output bit for bit."""
+    if name == "overlap_small":
+        w = wl("overlap_small", n_tokens=1500, d_model=256, d_ff=256, n_experts=16, top_k=4, capacity_factor=1.0,
+               act="swiglu", n_shared=2, d_ff_shared=256, logit_bias_max=1.0)
+    else:
+        w = WORKLOADS[name]
+    t = moe.make_inputs(w, "cuda")
+    layer = moe.Layer(w, t)
+    ref = layer.forward(t["x"]).clone()
+    side = torch.cuda.Stream()
+    ev_fork, ev_join = torch.cuda.Event(), torch.cuda.Event()
+    for cap in caps:
+        out = torch.empty_like(ref)
+        for _ in range(2):
+            moe.forward_overlap(layer.cfg, t["x"], layer.w, out, side, ev_fork, ev_join, cap, layer.stats, layer.ws)
+        torch.cuda.synchronize()
+        assert moe.get_device_status(layer.cfg, layer.ws) == (0, 0)
+        assert torch.equal(out, ref), cap
+    del layer, t
+    torch.cuda.empty_cache()
+
+
+GATHER = [
+    wl("gather_bf16_gelu_bias", n_tokens=1000, d_model=128, d_ff=256, n_experts=6, top_k=2, capacity_factor=1.0,
+       gating="topk_softmax", has_bias=True, logit_bias_max=2.0, gather_rows=True),
+    wl("gather_bf16_swiglu_shared_ec", n_tokens=700, d_model=256, d_ff=128, n_experts=8, top_k=2,
+       capacity_factor=1.0, gating="expert_choice", act="swiglu", n_shared=1, d_ff_shared=128, gather_rows=True),
+    wl("gather_bf16_ragged_many", n_tokens=333, d_model=64, d_ff=192, n_experts=40, top_k=4, capacity_factor=1.25,
+       gather_rows=True),
+]
+
+
+@pytest.mark.parametrize("w", GATHER, ids=lambda w: w.name)
+def test_gather_rows_matches_copy(w):
+    """The up-projection reading its rows from x with tile::gather4 (no xp copy) matches
+    the oracle and gives the copying forward's output bit for bit."""
+    layer, t, res = run_gpu(w)
+    assert res["xp"] is None  # no xp region in the workspace
+    check(w, t, res)
+    copy = moe.Layer(w.replace(gather_rows=False), t)
+    assert torch.equal(copy.forward(t["x"]), res["out"].cuda())
+
+
+def test_gather_rows_full_size_layer():
+    """The 8192-token layer, gathered, against the copying forward: every output bit."""
+    w = WORKLOADS["small_bf16"]
+    t = moe.make_inputs(w, "cuda")
+    a = moe.Layer(w.replace(gather_rows=True), t).forward(t["x"])
+    b = moe.Layer(w, t).forward(t["x"])
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
