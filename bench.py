@@ -42,6 +42,8 @@ HEADLINE = "large_fine"
 # A grouped GEMM launch longer than this runs long enough for the power limit to
 # pull the SM clock down, so it is measured against the sustained bf16 peak.
 SUSTAINED_AFTER_MS = 1.0
+# CTA caps of the shared experts' side-stream launches timed for moe_forward_overlap (0: none)
+OVERLAP_CAPS = (0, 32, 64, 96)
 
 
 def load_inputs_module():
@@ -180,7 +182,7 @@ class InputCache:
 
     def get(self, w):
         key = (w.d_model, w.d_ff, w.n_experts, w.n_shared, w.d_ff_shared, w.act, w.dtype, w.has_bias,
-               w.logit_bias_max, w.seed)
+               w.logit_bias_max, w.seed, w.expert_weights)
         if key != self.key:
             self.key, self.weights = None, None
             torch.cuda.empty_cache()
@@ -241,12 +243,13 @@ def run_e2e(moe, layer, x, steps: int, dev) -> float:
 def algorithmic(w, rows, touched):
     """Algorithmic FLOPs / bytes per forward (kept rows only, each operand once)."""
     b = 4 if w.dtype == "f32" else 2
+    bw = 1 + 1 / 32 if getattr(w, "expert_weights", "bf16") == "mxfp8" else b  # routed weight bytes per element
     m_up = 2 if w.act == "swiglu" else 1
     N, d, F, E, S, Fs = w.n_tokens, w.d_model, w.d_ff, w.n_experts, w.n_shared, w.d_ff_shared
     up_flops = 2 * rows * d * F * m_up + 2 * N * d * S * Fs * m_up
     down_flops = 2 * rows * F * d + 2 * N * S * Fs * d
-    w_up = touched * F * d * m_up * b + S * Fs * d * m_up * b
-    w_down = touched * d * F * b + S * d * Fs * b
+    w_up = touched * F * d * m_up * bw + S * Fs * d * m_up * b
+    w_down = touched * d * F * bw + S * d * Fs * b
     return dict(
         up_flops=up_flops, down_flops=down_flops,
         up_bytes=rows * d * b + N * d * b * (S > 0) + w_up + rows * F * b + N * S * Fs * b,
@@ -366,6 +369,39 @@ def measure(moe, w, t, dev, steps, warmup, flush, dist=False):
     return layer, out, total_ms, stage_ms / n_traced
 
 
+def measure_overlap(moe, layer, x, flush, steps, caps):
+    """ms per forward with the shared experts on a side stream (moe_forward_overlap), per
+    CTA cap of the side launches, against the one-stream forward timed in the same loop
+    (the variants take turns, so clock and power changes fall on all of them alike)."""
+    out = torch.empty_like(x)
+    side = torch.cuda.Stream()
+    ev_fork, ev_join = torch.cuda.Event(), torch.cuda.Event()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    variants = [None] + list(caps)
+
+    def run(v):
+        if v is None:
+            moe.forward(layer.cfg, x, layer.w, out, layer.stats, layer.ws)
+        else:
+            moe.forward_overlap(layer.cfg, x, layer.w, out, side, ev_fork, ev_join, v, layer.stats, layer.ws)
+
+    for v in variants:
+        for _ in range(2):
+            run(v)
+    torch.cuda.synchronize()
+    tot = {v: 0.0 for v in variants}
+    for _ in range(steps):
+        for v in variants:
+            flush.zero_()
+            t0.record()
+            run(v)
+            t1.record()
+            t1.synchronize()
+            tot[v] += t0.elapsed_time(t1)
+    return {"one_stream_ms": tot[None] / steps,
+            "side_stream_ms_by_cta_cap": {str(c): tot[c] / steps for c in caps}}
+
+
 # ---------------------------------------------------------------------------------------
 # CPU oracle legs (the oracle as it stands, single-threaded, pinned to one host core)
 
@@ -424,11 +460,17 @@ def device_expert_weights(w, t):
     """expert_weights_for() over device tensors: host copies of the listed experts only."""
     from oracle import torch_to_numpy
 
+    from oracle import as_bf16_bits, mxfp8_dequant
+
     def get(experts):
         h = {}
         for n in ("w1", "w3", "b1", "w2", "b2"):
             if t.get(n) is not None:
-                h[n] = torch_to_numpy(t[n][torch.as_tensor(experts, device=t[n].device, dtype=torch.long)])
+                sel = torch.as_tensor(experts, device=t[n].device, dtype=torch.long)
+                if t.get(n + "_scale") is not None:  # MXFP8: the oracle takes the exact dequantised values
+                    h[n] = as_bf16_bits(mxfp8_dequant(t[n][sel].cpu().numpy(), t[n + "_scale"][sel].cpu().numpy()))
+                else:
+                    h[n] = torch_to_numpy(t[n][sel])
         for n in ("ws1", "ws3", "bs1", "ws2", "bs2"):
             if t.get(n) is not None:
                 h[n] = torch_to_numpy(t[n])
@@ -523,6 +565,8 @@ def main():
     rows = int(st["rows"])
     touched = int((st["kept"].numpy() > 0).sum())
     rep, alg = stage_report(w, stage_avg, rows, touched, pk)
+    overlap = measure_overlap(moe, layer, x, flush, min(args.steps, 10), OVERLAP_CAPS) \
+        if w.n_shared > 0 and w.dtype == "bf16" else None
     # dominant kernel: the larger of the two grouped-GEMM launches
     gi = 2 if stage_avg[2] >= stage_avg[3] else 3
     flops = alg["up_flops"] if gi == 2 else alg["down_flops"]
@@ -553,6 +597,8 @@ def main():
         "gpu_launches": launches_per_step(w) * args.steps,
         "clocks": clk.summary(),
     }
+    if overlap:
+        line["shared_on_side_stream_ms"] = overlap
     cpu_inputs = None
     if rank == 0 and not args.no_cpu_baseline and world == 1:
         from oracle import torch_to_numpy
@@ -565,8 +611,8 @@ def main():
         per = {w.name: {"tokens_per_s": value, "ms_per_step": total_ms / args.steps, **rep,
                         "clocks": line["clocks"]}}
         # layers that share the headline's weights first (no second draw of them)
-        same = lambda v: (v.d_model, v.d_ff, v.n_experts, v.n_shared, v.act) == \
-            (w.d_model, w.d_ff, w.n_experts, w.n_shared, w.act)
+        same = lambda v: (v.d_model, v.d_ff, v.n_experts, v.n_shared, v.act, v.expert_weights) == \
+            (w.d_model, w.d_ff, w.n_experts, w.n_shared, w.act, w.expert_weights)
         order = sorted((n for n in BENCH_WORKLOADS if n != w.name), key=lambda n: not same(WORKLOADS[n]))
         for name in order:
             wc = WORKLOADS[name]
@@ -574,12 +620,16 @@ def main():
             steps_c = min(args.steps, 10)
             clk_c = ClockSampler(local).__enter__()
             lc, _, tot_c, stage_c = measure(moe, wc, tc, dev, steps_c, 3, flush, dist)
+            ov = measure_overlap(moe, lc, tc["x"], flush, steps_c, OVERLAP_CAPS) \
+                if wc.n_shared > 0 and wc.dtype == "bf16" and wc.n_tokens >= 4096 else None
             clk_c.__exit__(None, None, None)
             stc = lc.read_stats()
             rc, _ = stage_report(wc, stage_c, int(stc["rows"]), int((stc["kept"].numpy() > 0).sum()), pk)
             per[name] = {"tokens_per_s": job_tokens_per_s(wc.n_tokens, steps_c, world, tot_c),
                          "ms_per_step": tot_c / steps_c, "steps": steps_c, **rc,
                          "gpu_launches": launches_per_step(wc) * steps_c, "clocks": clk_c.summary()}
+            if ov:
+                per[name]["shared_on_side_stream_ms"] = ov
             del lc, tc
         line["per_config"] = per
     if cpu_inputs is not None:
@@ -627,15 +677,25 @@ def run_reference(args, world):
 
     def weights_for(experts):
         if full is not None:
-            h = {n: torch_to_numpy(full[n][torch.as_tensor(experts, dtype=torch.long)])
+            from oracle import as_bf16_bits, mxfp8_dequant
+            sel = torch.as_tensor(experts, dtype=torch.long)
+            h = {n: (as_bf16_bits(mxfp8_dequant(full[n][sel].numpy(), full[n + "_scale"][sel].numpy()))
+                     if full.get(n + "_scale") is not None else torch_to_numpy(full[n][sel]))
                  for n in ("w1", "w3", "b1", "w2", "b2") if full.get(n) is not None}
         else:
             d, F = w.d_model, w.d_ff
             specs = [("w1", (F, d), 1.0 / _m.sqrt(d)), ("w2", (d, F), 1.0 / _m.sqrt(F))]
             if w.act == "swiglu":
                 specs.append(("w3", (F, d), 1.0 / _m.sqrt(d)))
-            h = {n: torch_to_numpy(torch.stack([inp.expert_slice(n, e, shp, sd, dt, "cpu", w.seed)
-                                                for e in experts])) for n, shp, sd in specs}
+            h = {}
+            for n, shp, sd in specs:
+                v = torch.stack([inp.expert_slice(n, e, shp, sd, dt, "cpu", w.seed) for e in experts])
+                if w.expert_weights == "mxfp8":  # the stored codes, as their exact values
+                    from oracle import as_bf16_bits, mxfp8_dequant
+                    codes, scales = inp.mxfp8_quantize(v)
+                    h[n] = as_bf16_bits(mxfp8_dequant(codes.numpy(), scales.numpy()))
+                else:
+                    h[n] = torch_to_numpy(v)
             if w.has_bias:
                 h["b1"] = torch_to_numpy(inp.normal("b1", (w.n_experts, F), 0.1, dt, "cpu", w.seed)[experts])
                 h["b2"] = torch_to_numpy(inp.normal("b2", (w.n_experts, d), 0.1, dt, "cpu", w.seed)[experts])

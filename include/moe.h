@@ -105,6 +105,18 @@ typedef enum moe_dtype { MOE_DT_F32 = 0, MOE_DT_BF16 = 1 } moe_dtype;
  *   layer's 8.7 -> 22.2 ms). [AIE] "Gather/scatter outputs from experts". */
 #define MOE_FLAG_GATHER_ROWS 2
 
+/* Storage of the routed experts' weight matrices w1, w3, w2 (bf16 layers).
+ * MOE_WEIGHTS_MXFP8: OCP microscaling "MXFP8": each matrix [rows, K] is FP8 E4M3 codes
+ *   (1 byte, exponent bias 7, max 448) and one E8M0 scale byte s per 32 consecutive
+ *   codes along K (value = code * 2^(s - 127)), scales [rows, K / 32] row-major
+ *   (moe_weights.w1_scale ...). Needs d % 512 == 0 and F % 512 == 0. The weights are
+ *   dequantised to bf16 exactly in shared memory and the activations stay bf16, so the
+ *   layer computes with exactly the dequantised weights while a decode batch, bound by
+ *   streaming the expert weights, reads half the bytes. ("Mixture of Experts (MoE)"
+ *   (learn.starphix.com), "Quantization": lower-precision experts.) Shared experts and
+ *   the router stay bf16. */
+typedef enum moe_weight_format { MOE_WEIGHTS_DTYPE = 0, MOE_WEIGHTS_MXFP8 = 1 } moe_weight_format;
+
 /* Layer description (plain data, 96 bytes). */
 typedef struct moe_config {
   int64_t n_tokens;      /* N: tokens (B*T flattened)                                 */
@@ -123,14 +135,15 @@ typedef struct moe_config {
   int32_t has_bias;      /* GELU experts: b1/b2 (and bs1/bs2) present                 */
   float aux_alpha;       /* alpha of the auxiliary loss ([AIG]: ~0.01)                */
   int32_t flags;         /* MOE_FLAG_* bits                                           */
-  int32_t reserved;      /* 0                                                         */
+  int32_t weight_format; /* moe_weight_format of the routed experts' w1, w3, w2       */
   int64_t n_tokens_total; /* token-sharded batch: tokens of the whole batch over all
                             shards (capacity, statistics and kernel shapes follow it);
                             0 or n_tokens: this call holds the whole batch             */
 } moe_config;
 
 /* Weights, nn.Linear [out, in] layout, all device pointers of cfg->dtype except
- * logit_bias (fp32). Unused entries may be NULL. */
+ * logit_bias (fp32) and, with MOE_WEIGHTS_MXFP8, w1 / w3 / w2 (E4M3 codes, 1 byte)
+ * and their scales. Unused entries may be NULL. */
 typedef struct moe_weights {
   const void* w_router;    /* [E, d]   router, no bias ([AIG], [VAN], [STP])          */
   const float* logit_bias; /* [E] fp32 constant added to every token's logits, or NULL */
@@ -144,6 +157,9 @@ typedef struct moe_weights {
   const void* bs1;         /* [S, Fs]  shared, GELU with bias only                    */
   const void* ws2;         /* [S, d, Fs] shared                                       */
   const void* bs2;         /* [S, d]   shared, GELU with bias only                    */
+  const uint8_t* w1_scale; /* MOE_WEIGHTS_MXFP8: E8M0 scales of w1 [E, F, d / 32], else NULL */
+  const uint8_t* w3_scale; /* ... of w3 [E, F, d / 32] (SwiGLU)                         */
+  const uint8_t* w2_scale; /* ... of w2 [E, d, F / 32]                                  */
 } moe_weights;
 
 /* Router statistics, written to a caller-owned DEVICE buffer of

@@ -79,6 +79,8 @@ class Oracle:
         lib.oracle_stats.argtypes = [_P, _P, _P, _P, _P, _P]
         lib.oracle_expert_apply.argtypes = [_P, _P, ctypes.c_int32, _I64, _P, _P]
         lib.oracle_combine_tokens.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _P, _I64, _P]
+        lib.oracle_round_bf16.argtypes = [ctypes.c_float]
+        lib.oracle_round_bf16.restype = ctypes.c_float
         lib.oracle_entropy.argtypes = [_P, _I64]
         lib.oracle_entropy.restype = ctypes.c_double
         self.lib = lib
@@ -196,6 +198,10 @@ class Oracle:
                                      self._ptr(y))
         return y
 
+    def round_bf16(self, v: float) -> float:
+        """The mimic mode's fp32 -> bf16 rounding of one value."""
+        return float(self.lib.oracle_round_bf16(float(v)))
+
     def entropy(self, p: Sequence[float]) -> float:
         a = np.ascontiguousarray(np.asarray(p, np.float64))
         return float(self.lib.oracle_entropy(self._ptr(a), a.size))
@@ -251,6 +257,51 @@ class Oracle:
                                            self._ptr(g), self._ptr(row_of), None, None, 0, self._ptr(tokens),
                                            tokens.size, self._ptr(out))
         return out
+
+
+def e4m3_value(codes: np.ndarray) -> np.ndarray:
+    """Value of FP8 E4M3 codes (OCP 8-bit floating point, "E4M3"): sign bit, 4
+    exponent bits with bias 7, 3 mantissa bits; exponent field 0 is subnormal
+    (m/8 * 2^-6); S.1111.111 is NaN; there are no infinities. fp64."""
+    c = np.asarray(codes, np.uint8).astype(np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = (c & 7).astype(np.float64)
+    v = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * np.exp2(e.astype(np.float64) - 7.0))
+    v = np.where((e == 15) & ((c & 7) == 7), np.nan, v)
+    return sign * v
+
+
+_E4M3_F32 = None
+
+
+def mxfp8_dequant(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    """OCP MX "MXFP8" weights [..., K] back to their values: E4M3 code value times
+    2^(s - 127), one E8M0 scale byte s per 32 consecutive elements along K. fp32, which
+    holds every such product exactly (a code has at most 4 significant bits); the code
+    values come from the table e4m3_value gives for all 256 codes."""
+    global _E4M3_F32
+    if _E4M3_F32 is None:
+        _E4M3_F32 = e4m3_value(np.arange(256, dtype=np.uint8)).astype(np.float32)
+    codes = np.asarray(codes, np.uint8)
+    K = codes.shape[-1]
+    s = np.asarray(scales, np.uint8)
+    assert s.shape[-1] * 32 == K and not np.any(s == 255)
+    v = _E4M3_F32[codes].reshape(codes.shape[:-1] + (K // 32, 32))
+    v *= np.exp2(s.astype(np.float32) - np.float32(127.0))[..., None]
+    return v.reshape(codes.shape)
+
+
+def as_bf16_bits(v: np.ndarray) -> np.ndarray:
+    """fp64 values that are exactly bf16 numbers, as the oracle's bf16 bit patterns
+    (asserts exactness: the dequantised MXFP8 weights have at most 4 significant bits)."""
+    v = np.asarray(v)
+    f = v if v.dtype == np.float32 else v.astype(np.float32)
+    if v.dtype != np.float32:
+        assert np.array_equal(f.astype(np.float64), v.astype(np.float64)), "not exact in fp32"
+    bits = np.ascontiguousarray(f).view(np.uint32)
+    assert np.all((bits & 0xFFFF) == 0), "not exact in bf16"
+    return np.ascontiguousarray((bits >> 16).astype(np.uint16))
 
 
 def torch_to_numpy(t) -> np.ndarray:

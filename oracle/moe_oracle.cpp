@@ -467,6 +467,9 @@ void oracle_combine_tokens(const OracleConfig* c, const void* x, const OracleWei
   }
 }
 
+// The bf16 rounding the mimic mode applies (exported for its pin): nearest, ties to even.
+float oracle_round_bf16(float v) { return round_bf16(v); }
+
 // Routing entropy of a usage distribution, -sum p ln p over p > 0.
 // [AIG] collapse detector ("Logging the routing entropy").
 double oracle_entropy(const double* p, int64_t n) {

@@ -34,7 +34,7 @@ class moe_config(ctypes.Structure):
                 ("n_experts", ctypes.c_int64), ("n_shared", ctypes.c_int64), ("d_ff_shared", ctypes.c_int64),
                 ("top_k", ctypes.c_int64), ("capacity_factor", ctypes.c_float), ("gating", ctypes.c_int32),
                 ("act", ctypes.c_int32), ("dtype", ctypes.c_int32), ("has_bias", ctypes.c_int32),
-                ("aux_alpha", ctypes.c_float), ("flags", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("aux_alpha", ctypes.c_float), ("flags", ctypes.c_int32), ("weight_format", ctypes.c_int32),
                 ("n_tokens_total", ctypes.c_int64)]
 
 
@@ -42,7 +42,9 @@ FLAG_DROP_PASSTHROUGH = 1
 FLAG_GATHER_ROWS = 2
 
 
-WEIGHT_FIELDS = ("w_router", "logit_bias", "w1", "w3", "b1", "w2", "b2", "ws1", "ws3", "bs1", "ws2", "bs2")
+WEIGHT_FIELDS = ("w_router", "logit_bias", "w1", "w3", "b1", "w2", "b2", "ws1", "ws3", "bs1", "ws2", "bs2",
+                 "w1_scale", "w3_scale", "w2_scale")
+WEIGHT_FORMAT = {"bf16": 0, "f32": 0, "mxfp8": 1}
 
 
 class moe_weights(ctypes.Structure):
@@ -133,7 +135,7 @@ def config(w: Workload, **over) -> moe_config:
              gating=GATING[w.gating], act=ACT[w.act], dtype=DTYPE[w.dtype], has_bias=int(bool(w.has_bias)),
              aux_alpha=w.aux_alpha,
              flags=(FLAG_DROP_PASSTHROUGH if w.drop_passthrough else 0) | (FLAG_GATHER_ROWS if w.gather_rows else 0),
-             reserved=0, n_tokens_total=0)
+             weight_format=WEIGHT_FORMAT[w.expert_weights], n_tokens_total=0)
     d.update(over)
     return moe_config(**d)
 

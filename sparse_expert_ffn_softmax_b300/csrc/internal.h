@@ -19,6 +19,7 @@ struct Plan {
   bool sharded;       // Ntot > N: this call holds one contiguous token shard of the batch
   bool passthrough;   // MOE_FLAG_DROP_PASSTHROUGH
   bool gather;        // MOE_FLAG_GATHER_ROWS (bf16): the up-projection gathers its rows from x
+  bool fp8w;          // MOE_WEIGHTS_MXFP8: routed expert weights are E4M3 codes with E8M0 block scales
   bool bf16, swiglu, ec, bias;
   int64_t cap;       // C
   int64_t max_rows;  // rows reserved for xp / h / yp

@@ -40,14 +40,16 @@ moe_status make_plan(const moe_config* c, Plan* p) {
     return MOE_ERR_INVALID_ARG;
   if (!std::isfinite(c->capacity_factor) || !std::isfinite(c->aux_alpha)) return MOE_ERR_INVALID_ARG;
   if (c->n_tokens_total != 0 && c->n_tokens_total < c->n_tokens) return MOE_ERR_INVALID_ARG;
-  if ((c->flags & ~(int32_t)(MOE_FLAG_DROP_PASSTHROUGH | MOE_FLAG_GATHER_ROWS)) != 0 || c->reserved != 0)
-    return MOE_ERR_INVALID_ARG;
+  if ((c->flags & ~(int32_t)(MOE_FLAG_DROP_PASSTHROUGH | MOE_FLAG_GATHER_ROWS)) != 0) return MOE_ERR_INVALID_ARG;
+  if (c->weight_format != MOE_WEIGHTS_DTYPE && c->weight_format != MOE_WEIGHTS_MXFP8) return MOE_ERR_INVALID_ARG;
   p->Ntot = c->n_tokens_total > p->N ? c->n_tokens_total : p->N;
   p->sharded = p->Ntot > p->N;
   p->passthrough = (c->flags & MOE_FLAG_DROP_PASSTHROUGH) != 0;
   if (p->k > p->E || p->k > 32 || p->E > 512 || p->S > 64) return MOE_ERR_UNSUPPORTED;
   p->bf16 = c->dtype == MOE_DT_BF16;
   p->gather = p->bf16 && (c->flags & MOE_FLAG_GATHER_ROWS) != 0;
+  p->fp8w = c->weight_format == MOE_WEIGHTS_MXFP8;
+  if (p->fp8w && (!p->bf16 || p->d % 512 || p->F % 512)) return MOE_ERR_UNSUPPORTED;
   p->swiglu = c->act == MOE_ACT_SWIGLU;
   p->ec = c->gating == MOE_GATE_EXPERT_CHOICE;
   p->bias = c->has_bias != 0;
@@ -154,6 +156,8 @@ moe_status check_weights(const Plan& p, const moe_weights* w, bool router, bool 
   if (experts) {
     if (!ok_ptr(w->w1) || !ok_ptr(w->w2)) return MOE_ERR_INVALID_ARG;
     if (p.swiglu && !ok_ptr(w->w3)) return MOE_ERR_INVALID_ARG;
+    if (p.fp8w && (!ok_ptr(w->w1_scale) || !ok_ptr(w->w2_scale) || (p.swiglu && !ok_ptr(w->w3_scale))))
+      return MOE_ERR_INVALID_ARG;
     if (p.bias && (!ok_ptr(w->b1) || !ok_ptr(w->b2))) return MOE_ERR_INVALID_ARG;
     if (p.S > 0) {
       if (!ok_ptr(w->ws1) || !ok_ptr(w->ws2)) return MOE_ERR_INVALID_ARG;

@@ -215,33 +215,37 @@ __global__ void __launch_bounds__(kRouterWarps * 32) router_kernel(RouterArgs a)
     }
     if (!ec) {
       // ---- top-k on logits: repeated warp arg-max, ties to the lower expert id ----
-      uint32_t taken = 0;
+      // Logits as order-preserving unsigned keys (flip the sign bit of positives, all
+      // bits of negatives; -0 as +0; a taken or absent expert has key 0): a round is the lane's
+      // best key (ascending i, so the lower id on ties), one warp max-reduction of the
+      // keys and one min-reduction of the ids holding that key.
+      uint32_t key[EPL];
+#pragma unroll
+      for (int i = 0; i < EPL; ++i) {
+        const uint32_t u = __float_as_uint(Lr[i]) & (Lr[i] == 0.f ? 0u : 0xFFFFFFFFu);  // -0 ties with +0
+        key[i] = lane + 32 * i < E ? ((u & 0x80000000u) ? ~u : (u | 0x80000000u)) : 0u;
+      }
       int my_e = 0;
       float my_l = 0.f;
       for (int j = 0; j < k; ++j) {
-        float bv = -FLT_MAX;
-        int be = 0x7fffffff;
+        uint32_t bk = key[0];
+        int bi = 0;
 #pragma unroll
-        for (int i = 0; i < EPL; ++i) {
-          const int e = lane + 32 * i;
-          if (e < E && !((taken >> i) & 1u) && (Lr[i] > bv || (Lr[i] == bv && e < be))) {
-            bv = Lr[i];
-            be = e;
+        for (int i = 1; i < EPL; ++i)
+          if (key[i] > bk) {
+            bk = key[i];
+            bi = i;
           }
-        }
+        const uint32_t mk = __reduce_max_sync(kFull, bk);
+        const uint32_t be = __reduce_min_sync(kFull, bk == mk ? (uint32_t)(lane + 32 * bi) : 0xFFFFFFFFu);
+        if ((int)(be & 31) == lane) {
 #pragma unroll
-        for (int sh = 16; sh >= 1; sh >>= 1) {
-          const float ov = __shfl_xor_sync(kFull, bv, sh);
-          const int oe = __shfl_xor_sync(kFull, be, sh);
-          if (ov > bv || (ov == bv && oe < be)) {
-            bv = ov;
-            be = oe;
-          }
+          for (int i = 0; i < EPL; ++i)
+            if (i == (int)(be >> 5)) key[i] = 0u;
         }
-        if ((be & 31) == lane) taken |= 1u << (be >> 5);
         if (lane == j) {
-          my_e = be;
-          my_l = bv;
+          my_e = (int)be;
+          my_l = __uint_as_float((mk & 0x80000000u) ? (mk & 0x7FFFFFFFu) : ~mk);
         }
       }
       // ---- gates ----

@@ -54,6 +54,7 @@ class Workload:
     seed: int = 0
     drop_passthrough: bool = False  # a token with no kept expert row gets x added to its output
     gather_rows: bool = False  # bf16: the up-projection gathers its rows from x (no xp copy)
+    expert_weights: str = "bf16"  # routed experts' w1/w3/w2: "bf16" (the layer dtype) or "mxfp8"
 
     def replace(self, **kw) -> "Workload":
         return dataclasses.replace(self, **kw)
@@ -82,6 +83,12 @@ WORKLOADS: Dict[str, Workload] = {
                  n_shared=1, d_ff_shared=2048),
         Workload("large_fine_decode", 128, 7168, 2048, 256, 8, 0.0, "softmax_topk", "swiglu", "bf16",
                  n_shared=1, d_ff_shared=2048),
+        # The decode batches with the routed experts' weights in MXFP8 (FP8 E4M3 codes,
+        # one power-of-two scale per 32 along K): half the bytes to stream.
+        Workload("mixtral_decode_fp8", 64, 4096, 14336, 8, 2, 0.0, "softmax_topk_renorm", "swiglu", "bf16",
+                 expert_weights="mxfp8"),
+        Workload("large_fine_decode_fp8", 128, 7168, 2048, 256, 8, 0.0, "softmax_topk", "swiglu", "bf16",
+                 n_shared=1, d_ff_shared=2048, expert_weights="mxfp8"),
         # Reduced-expert stand-ins of the two fine-grained layers for profiler captures
         # that must stay a few GB on the device: the same d, F, k, shared experts and
         # rows per expert (16384*8/256 = 512; 8192*6/160 ~ 307), 16 routed experts.
@@ -98,8 +105,8 @@ WORKLOADS: Dict[str, Workload] = {
 }
 
 # The layers the benchmark reports, in order (the stand-ins above are for captures only).
-BENCH_WORKLOADS = ["tiny_f32", "small_bf16", "mixtral_prefill", "mixtral_decode", "fine_skewed", "large_fine",
-                   "large_fine_ec", "large_fine_decode"]
+BENCH_WORKLOADS = ["tiny_f32", "small_bf16", "mixtral_prefill", "mixtral_decode", "mixtral_decode_fp8", "fine_skewed",
+                   "large_fine", "large_fine_ec", "large_fine_decode", "large_fine_decode_fp8"]
 
 
 def _seed_for(seed: int, name: str) -> int:
@@ -143,6 +150,25 @@ def expert_slice(name: str, i: int, shape, std: float, dtype: torch.dtype, devic
     return t.to(dtype)
 
 
+def mxfp8_quantize(w: torch.Tensor):
+    """Block-scaled FP8 copy of a weight matrix [..., K] (K % 32 == 0), the OCP MX
+    "MXFP8" format: every 32 consecutive elements along K share one power-of-two scale
+    2^(s - 127) (E8M0 byte s) and each element is an FP8 E4M3 code (bias 7, max 448).
+    The shared exponent is floor(log2(block max |w|)) - 8, so the block's largest
+    element scales into [256, 512) and clamps to 448; elements round to nearest even.
+    Returns (codes uint8 [..., K], scales uint8 [..., K / 32]). Input preparation
+    only: both the library and the oracle are given these codes."""
+    K = w.shape[-1]
+    assert K % 32 == 0
+    blocks = w.float().reshape(*w.shape[:-1], K // 32, 32)
+    amax = blocks.abs().amax(dim=-1)
+    e = torch.where(amax > 0, torch.floor(torch.log2(amax)) - 8, torch.zeros_like(amax)).clamp(-100, 100)
+    q = (blocks / torch.exp2(e).unsqueeze(-1)).clamp(-448.0, 448.0).to(torch.float8_e4m3fn)
+    codes = q.view(torch.uint8).reshape(w.shape)
+    scales = (e + 127).to(torch.uint8)
+    return codes.contiguous(), scales.contiguous()
+
+
 def make_inputs(w: Workload, device="cpu", with_weights: bool = True,
                 x_seed: Optional[int] = None) -> Dict[str, Optional[torch.Tensor]]:
     """Tokens ``x [N, d]`` and the layer's weights, in nn.Linear ``[out, in]`` layout.
@@ -171,6 +197,19 @@ def make_inputs(w: Workload, device="cpu", with_weights: bool = True,
     out["w3"] = normal("w3", (E, F, d), 1.0 / math.sqrt(d), dt, device, w.seed, chunk_dim0=big) \
         if w.act == "swiglu" else None
     out["w2"] = normal("w2", (E, d, F), 1.0 / math.sqrt(F), dt, device, w.seed, chunk_dim0=big)
+    if w.expert_weights == "mxfp8":  # the same draws, stored as MXFP8 codes and scales
+        for n in ("w1", "w3", "w2"):
+            if out[n] is None:
+                continue
+            src = out[n]
+            codes = torch.empty(src.shape, dtype=torch.uint8, device=src.device)
+            scales = torch.empty(src.shape[:-1] + (src.shape[-1] // 32,), dtype=torch.uint8, device=src.device)
+            for i in range(src.shape[0]):  # one expert at a time: small temporaries
+                codes[i], scales[i] = mxfp8_quantize(src[i])
+            out[n], out[n + "_scale"] = codes, scales
+            del src
+    else:
+        out["w1_scale"] = out["w3_scale"] = out["w2_scale"] = None
     out["b1"] = normal("b1", (E, F), 0.1, dt, device, w.seed) if w.has_bias else None
     out["b2"] = normal("b2", (E, d), 0.1, dt, device, w.seed) if w.has_bias else None
     if S > 0:

@@ -95,16 +95,29 @@ def sample_tokens(N, n, seed=0):
     return np.array(sorted(s), dtype=np.int64)
 
 
+def _oracle_array(t, n, experts=None):
+    """Host copy of weight ``n`` as the oracle takes it (only ``experts`` of a routed
+    stack if given). MXFP8 routed weights are given to the oracle as their exact
+    dequantised values (bf16 bit patterns): the layer is defined on those."""
+    from oracle import as_bf16_bits, mxfp8_dequant
+    v = t[n]
+    sel = None if experts is None else torch.as_tensor(experts, device=v.device, dtype=torch.long)
+    if sel is not None and n in ("w1", "w3", "b1", "w2", "b2"):
+        v = v[sel]
+    if t.get(n + "_scale") is not None:
+        sc = t[n + "_scale"] if sel is None else t[n + "_scale"][sel]
+        return as_bf16_bits(mxfp8_dequant(v.cpu().numpy(), sc.cpu().numpy()))
+    return torch_to_numpy(v)
+
+
 def host_weights(t, experts=None):
     """numpy copies of the weights the oracle needs (only ``experts`` of the routed stack if given)."""
     h = {}
     for n, v in t.items():
-        if v is None or n == "x":
+        if v is None or n == "x" or n.endswith("_scale"):
             h[n] = None
             continue
-        if experts is not None and n in ("w1", "w3", "b1", "w2", "b2"):
-            v = v[torch.as_tensor(experts, device=v.device, dtype=torch.long)]
-        h[n] = torch_to_numpy(v)
+        h[n] = _oracle_array(t, n, experts)
     return h
 
 
@@ -142,12 +155,9 @@ def _host_arrays(t, names, experts=None):
     """numpy host copies of the named weight tensors (of the listed experts only, if given)."""
     h = {}
     for n in names:
-        v = t.get(n)
-        if v is None:
+        if t.get(n) is None:
             continue
-        if experts is not None:
-            v = v[torch.as_tensor(experts, device=v.device, dtype=torch.long)]
-        h[n] = torch_to_numpy(v)
+        h[n] = _oracle_array(t, n, experts)
     return h
 
 

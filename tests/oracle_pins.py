@@ -476,7 +476,38 @@ def _check_shard_rows(sh, E):
     assert np.array_equal(np.diff(sh["expert_off"]), sh["kept"])
 
 
+def pin_round_bf16_nearest_even(o):
+    """The mimic mode's bf16 rounding is round-to-nearest-even: torch's bf16 cast (a
+    library routine) on random values, exact halfway cases and their neighbours."""
+    rs = np.random.RandomState(31)
+    vals = list((rs.standard_normal(2000) * np.exp2(rs.randint(-30, 30, 2000))).astype(np.float32))
+    for m in (0x3F80, 0x3F81, 0x4049, 0xC2AB, 0x0080):  # bf16 patterns: 1.0, 1+2^-7, ~3.14, negative, tiny normal
+        base = np.uint32(m) << 16
+        for low in (0x7FFF, 0x8000, 0x8001):  # just below, exactly at and just above the halfway point
+            vals.append(np.array([base | low], np.uint32).view(np.float32)[0])
+    vals = np.array(vals, np.float32)
+    got = np.array([o.round_bf16(v) for v in vals], np.float32)
+    ref = torch.from_numpy(vals).to(torch.bfloat16).float().numpy()
+    np.testing.assert_array_equal(got, ref)
+
+
+def pin_mxfp8_dequant(o):
+    """E4M3 code values against the format's closed forms and torch's float8_e4m3fn
+    conversion (a library routine); MX scales are powers of two per 32 elements."""
+    import oracle as orc
+    v = orc.e4m3_value(np.arange(256, dtype=np.uint8))
+    assert v[0x00] == 0.0 and v[0x01] == 2.0 ** -9 and v[0x07] == 7 * 2.0 ** -9 and v[0x08] == 2.0 ** -6
+    assert v[0x38] == 1.0 and v[0x7E] == 448.0 and v[0xFE] == -448.0 and v[0x3C] == 1.5
+    assert np.isnan(v[0x7F]) and np.isnan(v[0xFF]) and np.sum(np.isnan(v)) == 2
+    lib = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).double().numpy()
+    ok = ~np.isnan(v)
+    np.testing.assert_array_equal(v[ok], lib[ok])
+    codes = np.array([[0x38] * 32 + [0x3C] * 32], np.uint8)
+    scales = np.array([[127 + 3, 127 - 2]], np.uint8)
+    np.testing.assert_array_equal(orc.mxfp8_dequant(codes, scales), [[8.0] * 32 + [1.5 / 4] * 32])
+
+
 ALL_PINS = [pin_capacity, pin_router_logits, pin_softmax, pin_topk, pin_gates, pin_assign, pin_zero_router,
             pin_uniform_usage, pin_stats_formula, pin_single_expert_is_dense_ffn, pin_activation_zero,
             pin_brute_force, pin_dense_softmax_mixture, pin_expert_choice, pin_bf16_inputs_and_mimic,
-            pin_page_entropy, pin_passthrough, pin_assign_shard]
+            pin_page_entropy, pin_passthrough, pin_assign_shard, pin_mxfp8_dequant, pin_round_bf16_nearest_even]

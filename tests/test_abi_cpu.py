@@ -35,7 +35,7 @@ def test_abi_version_and_strings():
 def test_struct_sizes_match_header():
     assert ctypes.sizeof(moe.moe_config) == 96
     assert moe.moe_config.n_tokens_total.offset == 88 and moe.moe_config.flags.offset == 80
-    assert ctypes.sizeof(moe.moe_weights) == 12 * 8
+    assert ctypes.sizeof(moe.moe_weights) == 15 * 8
     assert ctypes.sizeof(moe.moe_stats_header) == 32
     assert moe.stats_bytes(8) == 32 + 16 * 8
 
@@ -89,7 +89,8 @@ def test_capacity_from_config():
     (dict(dtype=1, d_ff=100), 2),
     (dict(capacity_factor=float("nan")), 1),
     (dict(flags=4), 1),                     # unknown flag bit
-    (dict(reserved=1), 1),
+    (dict(weight_format=5), 1),
+    (dict(weight_format=1), 2),             # MXFP8 weights need a bf16 layer with d, F multiples of 512
     (dict(n_tokens_total=10), 1),           # whole batch smaller than the shard
     (dict(gating=3, n_tokens_total=128), 2),  # expert choice is not sharded
 ])

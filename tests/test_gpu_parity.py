@@ -210,7 +210,8 @@ def test_device_index_check_reports():
 # (workload, output tokens compared: None = every token). The large layers also
 # compare the expert rows of every segment's ends and of the GEMMs' ragged tiles.
 FULL = [("small_bf16", None), ("mixtral_decode", None), ("mixtral_prefill", 64), ("fine_skewed", 64),
-        ("large_fine", 64), ("large_fine_ec", 64), ("large_fine_decode", None)]
+        ("large_fine", 64), ("large_fine_ec", 64), ("large_fine_decode", None), ("mixtral_decode_fp8", None),
+        ("large_fine_decode_fp8", None)]
 
 
 @pytest.mark.parametrize("name,n_sample", FULL, ids=[f[0] for f in FULL])
@@ -246,6 +247,27 @@ def test_forward_overlap_matches_forward(name, caps):
         assert torch.equal(out, ref), cap
     del layer, t
     torch.cuda.empty_cache()
+
+
+# MXFP8 routed expert weights (FP8 E4M3 codes, one E8M0 scale per 32 along K; d, F
+# multiples of 512): the oracle computes with the exact dequantised weights
+FP8W = [
+    wl("fp8w_swiglu_shared", n_tokens=600, d_model=512, d_ff=1024, n_experts=8, top_k=2, capacity_factor=1.25,
+       act="swiglu", n_shared=1, d_ff_shared=256, expert_weights="mxfp8"),
+    wl("fp8w_gelu_bias_ec", n_tokens=300, d_model=512, d_ff=512, n_experts=6, top_k=2, capacity_factor=1.0,
+       gating="expert_choice", has_bias=True, expert_weights="mxfp8"),
+    wl("fp8w_decode_many", n_tokens=40, d_model=1024, d_ff=512, n_experts=64, top_k=6, capacity_factor=0.0,
+       act="swiglu", logit_bias_max=1.0, expert_weights="mxfp8"),
+    wl("fp8w_gather_drops", n_tokens=900, d_model=512, d_ff=512, n_experts=8, top_k=2, capacity_factor=0.6,
+       act="swiglu", logit_bias_max=2.0, expert_weights="mxfp8", gather_rows=True),
+]
+
+
+@pytest.mark.parametrize("w", FP8W, ids=lambda w: w.name)
+def test_mxfp8_expert_weights(w):
+    layer, t, res = run_gpu(w)
+    assert t["w1"].dtype == torch.uint8 and t["w1_scale"] is not None
+    check(w, t, res)
 
 
 GATHER = [
