@@ -47,6 +47,7 @@ class OracleConfig(ctypes.Structure):
         ("top_k", ctypes.c_int64), ("capacity_factor", ctypes.c_double), ("gating", ctypes.c_int32),
         ("act", ctypes.c_int32), ("has_bias", ctypes.c_int32), ("dtype", ctypes.c_int32),
         ("aux_alpha", ctypes.c_double), ("mimic_bf16", ctypes.c_int32), ("passthrough", ctypes.c_int32),
+        ("mx_act", ctypes.c_int32),
     ]
 
 
@@ -81,6 +82,7 @@ class Oracle:
         lib.oracle_combine_tokens.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _P, _I64, _P]
         lib.oracle_round_bf16.argtypes = [ctypes.c_float]
         lib.oracle_round_bf16.restype = ctypes.c_float
+        lib.oracle_mx_quantize.argtypes = [_P, _I64, _P, _P]
         lib.oracle_entropy.argtypes = [_P, _I64]
         lib.oracle_entropy.restype = ctypes.c_double
         self.lib = lib
@@ -102,7 +104,8 @@ class Oracle:
                  capacity_factor=w.capacity_factor, gating=GATING[w.gating], act=ACT[w.act],
                  has_bias=int(bool(w.has_bias)), dtype=0 if w.dtype == "f32" else 1,
                  aux_alpha=w.aux_alpha, mimic_bf16=int(mimic_bf16),
-                 passthrough=int(bool(getattr(w, "drop_passthrough", False))))
+                 passthrough=int(bool(getattr(w, "drop_passthrough", False))),
+                 mx_act=int(getattr(w, "expert_weights", "bf16") == "mxfp8"))
         g.update(over)
         return OracleConfig(**g)
 
@@ -197,6 +200,17 @@ class Oracle:
         self.lib.oracle_expert_apply(ctypes.byref(cfg), ctypes.byref(ow), int(shared), e, self._ptr(x_row),
                                      self._ptr(y))
         return y
+
+    def mx_quantize(self, v: np.ndarray):
+        """MXFP8 quantisation of the last axis (a multiple of 32): (E4M3 codes uint8,
+        E8M0 scale bytes uint8 [..., K / 32])."""
+        v = np.ascontiguousarray(v, np.float64)
+        K = v.shape[-1]
+        assert K % 32 == 0
+        codes = np.empty(v.shape, np.uint8)
+        scales = np.empty(v.shape[:-1] + (K // 32,), np.uint8)
+        self.lib.oracle_mx_quantize(self._ptr(v), v.size, self._ptr(codes), self._ptr(scales))
+        return codes, scales
 
     def round_bf16(self, v: float) -> float:
         """The mimic mode's fp32 -> bf16 rounding of one value."""

@@ -61,6 +61,9 @@ struct OracleConfig {
                            // bf16, the two places a bf16 pipeline must store bf16
   int32_t passthrough;     // a token with no kept expert gets its input added (see
                            // oracle_combine_tokens)
+  int32_t mx_act;          // routed experts compute in MXFP8: their input row and their
+                           // hidden activations are quantised (oracle_mx_quantize)
+                           // before each of their two matrix products
 };
 
 struct OracleWeights {
@@ -114,6 +117,71 @@ inline double store_round(double v, const OracleConfig* c) {
 inline double gelu(double u) {
   if (PLANT(5)) return 0.5 * u * (1.0 + std::erf(u));
   return 0.5 * u * (1.0 + std::erf(u / std::sqrt(2.0)));
+}
+
+// ---------------------------------------------------------------------------
+// FP8 E4M3 and the OCP microscaling (MX) block format "MXFP8". [STP] "Quantization"
+// names lower-precision experts; the number formats are the Open Compute Project's:
+// E4M3 is a sign bit, 4 exponent bits (bias 7) and 3 mantissa bits, exponent field 0
+// subnormal (m/8 * 2^-6), largest finite magnitude 448 (1.75 * 2^8), no infinities;
+// an MX block is 32 consecutive elements sharing one power-of-two scale 2^s whose
+// E8M0 byte is s + 127.
+
+// Nearest E4M3 magnitude to y >= 0, ties to the even code; anything above 448 gives
+// 448 (saturating conversion). Returned as its code (7 bits, no sign).
+inline uint8_t e4m3_code_sat(double y) {
+  if (!(y < 448.0)) return 0x7E;  // 448
+  int ex = 0;
+  std::frexp(y, &ex);  // y = f * 2^ex, f in [0.5, 1): floor(log2 y) = ex - 1
+  int E = ex - 1;
+  if (y == 0.0 || E < -6) E = -6;  // subnormal range: the spacing of the lowest binade
+  const double spacing = std::ldexp(1.0, E - 3);
+  double r = std::nearbyint(y / spacing);  // round half to even (default rounding mode)
+  if (PLANT(14)) r = std::floor(y / spacing + 0.5);  // ties away from zero
+  int m = static_cast<int>(r);
+  if (m >= 16) {  // rounded up into the next binade
+    E += 1;
+    m = 8;
+  }
+  if (m < 8) return static_cast<uint8_t>(m);  // subnormal (E == -6): code = m
+  return static_cast<uint8_t>(((E + 7) << 3) | (m - 8));
+}
+
+inline double e4m3_code_value(uint8_t c) {
+  const int e = (c >> 3) & 0xF, m = c & 7;
+  const double mag = e == 0 ? std::ldexp(m / 8.0, -6) : std::ldexp(1.0 + m / 8.0, e - 7);
+  return (c & 0x80) ? -mag : mag;
+}
+
+// One MX block of n <= 32 values: the shared exponent is s = floor(log2(max |v|)) - 8
+// (8 = the exponent of E4M3's largest power of two, so the block maximum lands in
+// [256, 512) before rounding and saturation), clamped to the E8M0 range [-127, 127];
+// an all-zero block takes s = -127. Each element is the E4M3 code of v / 2^s.
+inline void mx_block(const double* v, int n, uint8_t* codes, uint8_t* scale) {
+  double amax = 0.0;
+  for (int i = 0; i < n; ++i) amax = std::max(amax, std::fabs(v[i]));
+  int s = -127;
+  if (amax > 0.0) {
+    int ex = 0;
+    std::frexp(amax, &ex);
+    s = (ex - 1) - (PLANT(13) ? 7 : 8);
+    s = std::min(127, std::max(-127, s));
+  }
+  *scale = static_cast<uint8_t>(s + 127);
+  for (int i = 0; i < n; ++i) {
+    const uint8_t c = e4m3_code_sat(std::ldexp(std::fabs(v[i]), -s));
+    codes[i] = std::signbit(v[i]) ? static_cast<uint8_t>(c | 0x80) : c;
+  }
+}
+
+// v <- its MXFP8 value (quantise, then dequantise exactly), blocks of 32 along v.
+inline void mx_round_trip(double* v, int64_t n) {
+  uint8_t codes[32], scale;
+  for (int64_t b = 0; b < n; b += 32) {
+    const int m = static_cast<int>(std::min<int64_t>(32, n - b));
+    mx_block(v + b, m, codes, &scale);
+    for (int i = 0; i < m; ++i) v[b + i] = std::ldexp(e4m3_code_value(codes[i]), scale - 127);
+  }
 }
 
 // SiLU: u * sigmoid(u). [VAN] SwiGLUExpert.
@@ -389,6 +457,11 @@ void oracle_expert_apply(const OracleConfig* c, const OracleWeights* w, int32_t 
   const void* W2 = shared ? w->ws2 : w->w2;
   const void* B2 = shared ? w->bs2 : w->b2;
   const int32_t dt = c->dtype;
+  // MXFP8 routed experts: the input row and (below) the hidden row are quantised
+  const bool mx = c->mx_act && !shared;
+  std::vector<double> xq(x, x + d);
+  if (mx) mx_round_trip(xq.data(), d);
+  x = xq.data();
   std::vector<double> h(static_cast<size_t>(F));
   for (int64_t f = 0; f < F; ++f) {
     double a = 0.0;
@@ -401,8 +474,9 @@ void oracle_expert_apply(const OracleConfig* c, const OracleWeights* w, int32_t 
       for (int64_t i = 0; i < d; ++i) b += load(W3, (e * F + f) * d + i, dt) * x[i];
       h[f] = silu(a) * b;
     }
-    h[f] = store_round(h[f], c);
+    if (!mx) h[f] = store_round(h[f], c);
   }
+  if (mx && !PLANT(15)) mx_round_trip(h.data(), F);
   for (int64_t n = 0; n < d; ++n) {
     double s = 0.0;
     for (int64_t f = 0; f < F; ++f) {
@@ -469,6 +543,12 @@ void oracle_combine_tokens(const OracleConfig* c, const void* x, const OracleWei
 
 // The bf16 rounding the mimic mode applies (exported for its pin): nearest, ties to even.
 float oracle_round_bf16(float v) { return round_bf16(v); }
+
+// MXFP8 quantisation of n values (n % 32 == 0): E4M3 codes [n] and E8M0 scale bytes
+// [n / 32], the rule mx_block states (exported for its pins and the code-level checks).
+void oracle_mx_quantize(const double* v, int64_t n, uint8_t* codes, uint8_t* scales) {
+  for (int64_t b = 0; b < n; b += 32) mx_block(v + b, 32, codes + b, scales + b / 32);
+}
 
 // Routing entropy of a usage distribution, -sum p ln p over p > 0.
 // [AIG] collapse detector ("Logging the routing entropy").

@@ -507,7 +507,131 @@ def pin_mxfp8_dequant(o):
     np.testing.assert_array_equal(orc.mxfp8_dequant(codes, scales), [[8.0] * 32 + [1.5 / 4] * 32])
 
 
+def _e4m3_nearest_code(y):
+    """Brute force: the E4M3 code (0..126) whose value is nearest to each y >= 0, ties
+    to the even code, values above 448 to 448 (the saturating conversion)."""
+    import oracle as orc
+    mags = orc.e4m3_value(np.arange(127, dtype=np.uint8))
+    y = np.asarray(y, np.float64)
+    dist = np.abs(y[:, None] - mags[None, :])
+    best = dist.min(axis=1, keepdims=True)
+    cand = dist == best
+    # among equally near codes take the even one (two candidates at most)
+    even = cand & (np.arange(127)[None, :] % 2 == 0)
+    code = np.where(even.any(axis=1), even.argmax(axis=1), cand.argmax(axis=1))
+    return np.where(y >= 448.0, 126, code).astype(np.uint8)
+
+
+def pin_e4m3_rounding(o):
+    """MXFP8 element rounding: nearest E4M3 value, ties to the even code, saturating at
+    448, against brute force over the code table and torch's float8_e4m3fn cast (a
+    library routine) below 448. A block led by 300 has scale 2^0, so its other elements'
+    codes are the plain E4M3 roundings."""
+    import oracle as orc
+    mags = orc.e4m3_value(np.arange(127, dtype=np.uint8))
+    mids = (mags[:-1] + mags[1:]) / 2
+    rs = np.random.RandomState(41)
+    ys = np.concatenate([mids, mids * (1 + 2.0 ** -40), mids * (1 - 2.0 ** -40), mags,
+                         rs.uniform(0, 448, 600), np.exp2(rs.uniform(-12, 8.8, 600)),
+                         [448.0, 449.0, 463.9, 464.0, 470.0, 500.0, 0.0, 2.0 ** -10, 3 * 2.0 ** -11]])
+    ys = ys[: (len(ys) // 31) * 31].reshape(-1, 31)
+    blocks = np.concatenate([np.full((len(ys), 1), 300.0), ys], axis=1)
+    codes, scales = o.mx_quantize(blocks)
+    assert np.all(scales == 127)
+    np.testing.assert_array_equal(codes[:, 1:].ravel(), _e4m3_nearest_code(ys.ravel()))
+    # (torch casts through fp32: compare values that fp32 holds exactly)
+    low = (ys.ravel() < 448.0) & (ys.ravel().astype(np.float32) == ys.ravel())
+    lib = torch.from_numpy(ys.ravel()[low].astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    np.testing.assert_array_equal(codes[:, 1:].ravel()[low], lib)
+    # signs: the code of -v is the code of v with bit 7 set
+    neg, _ = o.mx_quantize(-blocks)
+    np.testing.assert_array_equal(neg, codes | 0x80)
+
+
+def pin_mx_block_scale(o):
+    """MX shared exponent s = floor(log2(max |v|)) - 8, clamped to [-127, 127], zero
+    blocks s = -127 (E8M0 byte s + 127): closed forms; the block maximum's code lies in
+    [256, 448]; each element is within half an E4M3 step (times 2^s) of its value; a
+    block of E4M3 values times 2^s comes back exactly."""
+    import oracle as orc
+    rs = np.random.RandomState(43)
+    for p in (-20, -8, -1, 0, 3, 9, 17):
+        for f in (1.0, 1.37, 1.999):
+            v = rs.uniform(-1, 1, 32) * (f * 2.0 ** p)
+            v[rs.randint(32)] = -f * 2.0 ** p
+            c, s = o.mx_quantize(v)
+            assert int(s[0]) == p - 8 + 127, (p, f, s)
+            q = orc.e4m3_value(c) * 2.0 ** (int(s[0]) - 127)
+            assert 256.0 <= np.max(np.abs(orc.e4m3_value(c))) <= 448.0
+            # each element within half the E4M3 spacing of its binade (2^(E-3), E >= -6),
+            # times 2^s; a saturated element (|v| / 2^s in [448, 512)) is off by < 64 * 2^s
+            a = np.abs(v) * 2.0 ** -(int(s[0]) - 127)
+            E = np.maximum(np.floor(np.log2(np.maximum(a, 2.0 ** -30))), -6)
+            bound = np.where(a >= 448, 64.0, 2.0 ** (E - 4)) * 2.0 ** (int(s[0]) - 127)
+            assert np.all(np.abs(q - v) <= bound * (1 + 1e-12)), (p, f)
+    c, s = o.mx_quantize(np.zeros(32))
+    assert s[0] == 0 and np.all(c == 0)
+    c, s = o.mx_quantize(np.full(32, 2.0 ** -140))
+    assert s[0] == 0
+    c, s = o.mx_quantize(np.full(32, 2.0 ** 140))
+    assert s[0] == 254
+    exact = orc.e4m3_value(rs.randint(0, 127, 64).astype(np.uint8)) * 2.0 ** -5
+    exact[0], exact[32] = 448 * 2.0 ** -5, -256 * 2.0 ** -5
+    c, s = o.mx_quantize(exact)
+    np.testing.assert_array_equal(orc.mxfp8_dequant(c[None], s[None])[0], exact)
+
+
+def _mx_round_trip_np(v):
+    """Quantise-dequantise along the last axis with the brute-force E4M3 rounding and
+    the shared-exponent closed form (independent of the oracle's C code)."""
+    import oracle as orc
+    v = np.asarray(v, np.float64)
+    b = v.reshape(v.shape[:-1] + (v.shape[-1] // 32, 32))
+    amax = np.abs(b).max(axis=-1, keepdims=True)
+    s = np.where(amax > 0, np.floor(np.log2(np.where(amax > 0, amax, 1.0))) - 8, -127)
+    s = np.clip(s, -127, 127)
+    a = np.abs(b) * np.exp2(-s)
+    q = orc.e4m3_value(_e4m3_nearest_code(a.ravel())).reshape(a.shape) * np.sign(b) * np.exp2(s)
+    return q.reshape(v.shape)
+
+
+def pin_mx_layer(o):
+    """MXFP8 routed experts (mx_act): each routed expert computes on its MXFP8-rounded
+    input row and MXFP8-rounded hidden row, shared experts on the plain row; checked
+    against torch fp64 library ops fed by an independent quantiser, on tiny layers."""
+    for act, bias in (("swiglu", False), ("gelu", True)):
+        w = wl(n_tokens=6, d_model=64, d_ff=64, n_experts=4, top_k=2, act=act, has_bias=bias, n_shared=1,
+               d_ff_shared=32, gating="softmax_topk")
+        t = rand_layer(w, 47)
+        cfg = o.config(w, mx_act=1)
+        ow = o.weights(t)
+        r = o.route(cfg, t["x"], ow)
+        got = o.outputs(cfg, t["x"], ow, r)
+        xq = torch.from_numpy(_mx_round_trip_np(t["x"].astype(np.float64)))
+        ref = torch.from_numpy(torch_expert(t, 0, t["x"].astype(np.float64), act, bias, shared=True))
+        for tok in range(w.n_tokens):
+            for j in range(w.top_k):
+                e = int(r["idx"][tok, j])
+                W1 = torch.from_numpy(t["w1"][e].astype(np.float64))
+                a = xq[tok] @ W1.T
+                if act == "gelu":
+                    hh = torch.nn.functional.gelu(a + torch.from_numpy(t["b1"][e].astype(np.float64)))
+                else:
+                    W3 = torch.from_numpy(t["w3"][e].astype(np.float64))
+                    hh = torch.nn.functional.silu(a) * (xq[tok] @ W3.T)
+                hq = torch.from_numpy(_mx_round_trip_np(hh.numpy()))
+                y = hq @ torch.from_numpy(t["w2"][e].astype(np.float64)).T
+                if act == "gelu":
+                    y = y + torch.from_numpy(t["b2"][e].astype(np.float64))
+                ref[tok] += float(r["gate"][tok, j]) * y
+        np.testing.assert_allclose(got, ref.numpy(), rtol=1e-9, atol=1e-9)
+        # and it differs from the unquantised layer (the rounding is really applied)
+        plain = o.outputs(o.config(w), t["x"], ow, r)
+        assert np.max(np.abs(plain - got)) > 1e-4
+
+
 ALL_PINS = [pin_capacity, pin_router_logits, pin_softmax, pin_topk, pin_gates, pin_assign, pin_zero_router,
             pin_uniform_usage, pin_stats_formula, pin_single_expert_is_dense_ffn, pin_activation_zero,
             pin_brute_force, pin_dense_softmax_mixture, pin_expert_choice, pin_bf16_inputs_and_mimic,
-            pin_page_entropy, pin_passthrough, pin_assign_shard, pin_mxfp8_dequant, pin_round_bf16_nearest_even]
+            pin_page_entropy, pin_passthrough, pin_assign_shard, pin_mxfp8_dequant, pin_round_bf16_nearest_even,
+            pin_e4m3_rounding, pin_mx_block_scale, pin_mx_layer]

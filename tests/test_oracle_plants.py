@@ -4,8 +4,9 @@ The plants (sites marked PLANT(n) in oracle/moe_oracle.cpp) are the kinds of
 error the pins are meant to catch: a dropped bias term, a wrong tie-break, a
 transposed operand, a capacity formula without k, a wrong GELU or SiLU, missing
 renormalisation, reversed dropping order, a missing factor in the aux loss and
-an unsquared z-loss, a pass-through of tokens that kept an expert, and a shard
-that ignores the earlier shards' counts. Only the oracle is planted, on the CPU.
+an unsquared z-loss, a pass-through of tokens that kept an expert, a shard
+that ignores the earlier shards' counts, and three MXFP8 slips (scale exponent,
+tie rule, a skipped quantisation). Only the oracle is planted, on the CPU.
 """
 import os
 
@@ -27,6 +28,9 @@ PLANTS = {
     10: "z-loss not squared",
     11: "pass-through for a token with any dropped slot",
     12: "shard ranks without the earlier shards' counts",
+    13: "MX shared exponent one too small (floor(log2 max) - 7)",
+    14: "E4M3 rounding ties away from zero",
+    15: "MXFP8 experts without the hidden-row quantisation",
 }
 
 
