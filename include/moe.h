@@ -106,15 +106,22 @@ typedef enum moe_dtype { MOE_DT_F32 = 0, MOE_DT_BF16 = 1 } moe_dtype;
 #define MOE_FLAG_GATHER_ROWS 2
 
 /* Storage of the routed experts' weight matrices w1, w3, w2 (bf16 layers).
- * MOE_WEIGHTS_MXFP8: OCP microscaling "MXFP8": each matrix [rows, K] is FP8 E4M3 codes
- *   (1 byte, exponent bias 7, max 448) and one E8M0 scale byte s per 32 consecutive
- *   codes along K (value = code * 2^(s - 127)), scales [rows, K / 32] row-major
- *   (moe_weights.w1_scale ...). Needs d % 512 == 0 and F % 512 == 0. The weights are
- *   dequantised to bf16 exactly in shared memory and the activations stay bf16, so the
- *   layer computes with exactly the dequantised weights while a decode batch, bound by
- *   streaming the expert weights, reads half the bytes. ("Mixture of Experts (MoE)"
- *   (learn.starphix.com), "Quantization": lower-precision experts.) Shared experts and
- *   the router stay bf16. */
+ * MOE_WEIGHTS_MXFP8: the routed experts compute in OCP microscaling "MXFP8". Each
+ *   weight matrix [rows, K] is FP8 E4M3 codes (1 byte: sign, 4 exponent bits with bias
+ *   7, 3 mantissa bits; max 448) with one E8M0 scale byte s per 32 consecutive codes
+ *   along K (value = code * 2^(s - 127)), scales [rows, K / 32] row-major
+ *   (moe_weights.w1_scale ...). The experts' inputs are quantised the same way: each
+ *   permuted token row and each hidden row H is cut into blocks of 32 values whose
+ *   shared exponent is floor(log2(max |v|)) - 8 (at least -127) and whose elements
+ *   round to the nearest E4M3 code (ties to even, saturating at 448); both matrix
+ *   products run on the tensor cores' block-scaled FP8 path with fp32 accumulation.
+ *   xp then holds the rows' codes [max_rows, d] followed, from the next 256-byte
+ *   boundary after max_rows * d bytes, by their scales [max_rows, d / 32]; the
+ *   workspace's h region holds H the same way ([max_rows, F] codes, then scales).
+ *   A decode batch, bound by streaming the expert weights, reads half the bytes of
+ *   bf16. Needs d % 512 == 0 and F % 512 == 0 and no MOE_FLAG_GATHER_ROWS. Shared
+ *   experts and the router stay bf16. ("Mixture of Experts (MoE)"
+ *   (learn.starphix.com), "Quantization": lower-precision experts.) */
 typedef enum moe_weight_format { MOE_WEIGHTS_DTYPE = 0, MOE_WEIGHTS_MXFP8 = 1 } moe_weight_format;
 
 /* Layer description (plain data, 96 bytes). */
@@ -199,8 +206,10 @@ typedef struct moe_workspace_layout {
   size_t row_token;   /* int32 [max_rows]                                       */
   size_t row_gate;    /* fp32 [max_rows]                                        */
   size_t xp;          /* dtype [max_rows, d] permuted tokens (empty with
-                         MOE_FLAG_GATHER_ROWS)                                   */
-  size_t h;           /* dtype [max_rows, F] routed hidden activations          */
+                         MOE_FLAG_GATHER_ROWS; MXFP8 codes + scales with
+                         MOE_WEIGHTS_MXFP8)                                      */
+  size_t h;           /* dtype [max_rows, F] routed hidden activations (MXFP8
+                         codes + scales with MOE_WEIGHTS_MXFP8)                  */
   size_t hs;          /* dtype [N, S*Fs] shared hidden activations              */
   size_t yp;          /* fp32 [max_rows, d] gate-scaled expert outputs          */
   size_t ys;          /* fp32 [N, d] sum of shared expert outputs               */
@@ -256,7 +265,8 @@ MOE_API moe_status moe_route(const moe_config* cfg, const void* x, const moe_wei
  * numbered expert by expert, in token order inside each expert; row r of xp is
  * x[row_token[r]].
  *  x          [N, d] dtype;  idx / gate as written by moe_route.
- *  xp         [max_rows, d] dtype: rows [0, R) written.
+ *  xp         [max_rows, d] dtype: rows [0, R) written (MOE_WEIGHTS_MXFP8: their E4M3
+ *             codes and E8M0 scales, laid out as that format states).
  *  tok_rows   token choice: [N, k] row of each choice or -1 if dropped.
  *             expert choice: [E*C] rows listed token by token (ascending expert id).
  *  tok_off    expert choice: [N+1] start of each token's list in tok_rows
@@ -299,7 +309,8 @@ MOE_API moe_status moe_permute_shard(const moe_config* cfg, const void* x, const
 /* Grouped expert FFNs over the expert-contiguous rows, and the shared experts
  * over all tokens ([VAN] SwiGLUExpert / StandardExpert / HybridMoE;
  * [VAN] "Efficient Batched MoE": one grouped computation instead of a loop).
- *  xp         [max_rows, d]; expert_off [E+1] (device; read on the device only).
+ *  xp         [max_rows, d] as moe_permute wrote it (MOE_WEIGHTS_MXFP8: codes + scales);
+ *             expert_off [E+1] (device; read on the device only).
  *  row_gate   [max_rows] fp32: yp row r = row_gate[r] * E_e(xp[r]).
  *  x          [N, d] (needed when S > 0).
  *  yp         [max_rows, d] fp32: rows [0, R) written (fp32 for every layer dtype,

@@ -168,6 +168,20 @@ def workspace_layout(cfg: moe_config) -> moe_workspace_layout:
     return lay
 
 
+def mx_views(cfg: moe_config, ws: torch.Tensor, region: str):
+    """(codes uint8 [max_rows, K], scales uint8 [max_rows, K / 32]) views of the
+    workspace's ``xp`` (K = d) or ``h`` (K = F) region of a MOE_WEIGHTS_MXFP8 layer:
+    codes first, scales from the next 256-byte boundary (include/moe.h)."""
+    lay = workspace_layout(cfg)
+    R = int(lay.max_rows)
+    K = int(cfg.d_model if region == "xp" else cfg.d_ff)
+    base = int(getattr(lay, region))
+    off = (R * K + 255) // 256 * 256
+    codes = ws[base:base + R * K].view(R, K)
+    scales = ws[base + off:base + off + R * (K // 32)].view(R, K // 32)
+    return codes, scales
+
+
 def workspace_init(cfg: moe_config, ws: torch.Tensor, stream=None):
     _check(_lib.moe_workspace_init(ctypes.byref(cfg), _ptr(ws), ws.numel(), _stream(stream)), "moe_workspace_init")
 

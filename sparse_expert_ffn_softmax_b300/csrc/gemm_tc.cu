@@ -34,18 +34,25 @@
 // barrier, the leader issues the MMAs, its commits arrive at both CTAs, and each CTA
 // drains its own 128 accumulator rows, the peer signalling the leader when done.
 //
+// MXFP8 form (layers whose routed experts compute in MXFP8, "Mixture of Experts (MoE)"
+// (learn.starphix.com), "Quantization"): A and B are E4M3 codes with an E8M0 scale per
+// 32 elements along K, multiplied by tcgen05.mma kind::mxf8f6f4 with block scaling
+// (M=128, N=128, K=32 per instruction, 128 codes per stage). The producer warp's lanes
+// copy each stage's scale bytes into shared memory (cp.async), the MMA thread moves
+// them into tensor memory (tcgen05.cp) ahead of the stage's MMAs, and the
+// up-projection's epilogue quantises H to MXFP8 for the down-projection.
+//
 // Every mbarrier wait is bounded by the global timer; on expiry the CTA records
 // MOE_ERR_TIMEOUT in the workspace error word, waits (bounded) for its own TMA
 // copies and MMAs in flight, frees its TMEM and exits.
 #include <cuda.h>
-#include <cuda_fp16.h>
-#include <cuda_fp8.h>
 
 #include <cstdlib>
 
 #include "act.cuh"
 #include "common.cuh"
 #include "internal.h"
+#include "mx.cuh"
 
 namespace moe {
 namespace tc {
@@ -86,11 +93,17 @@ struct Family {
   int32_t gather_n;       // gather_rows: rows of the gathered matrix (bounds of the row ids)
   const int32_t* gather_rows;  // non-null: A row r of a group is row gather_rows[r] of the a_map matrix,
                                // loaded with tile::gather4 (a_map has one-row boxes)
-  // FP8 B (MXFP8 weights): b_map / b3_map hold E4M3 codes; one E8M0 scale byte per 32
-  // codes along K, rows of scale_ld bytes (K / 32, a multiple of 16)
-  const uint8_t* b_scale;
-  const uint8_t* b3_scale;
+  // MXFP8 form: A and B are E4M3 codes (the maps' rows are bytes) with one E8M0 scale
+  // byte per 32 codes along K, scales row-major [rows, K / 32]; H tiles are stored as
+  // codes + scales (out_scale) for the next GEMM.
+  int32_t a_rows;           // rows of the A matrix (bound of the A scale reads)
+  const uint8_t* a_scale;   // [a_rows, a_scale_ld]
+  int64_t a_scale_ld;
+  const uint8_t* b_scale;   // rows of b_map
+  const uint8_t* b3_scale;  // rows of b3_map
   int64_t scale_ld;
+  uint8_t* out_scale;       // [rows of out, out_scale_ld]
+  int64_t out_scale_ld;
 };
 
 struct Params {
@@ -370,61 +383,80 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-// 16 FP8 E4M3 codes times a power-of-two scale -> 16 bf16 values (exact: a code has at
-// most 4 significant bits, so code x 2^k is a bf16 number in the normal range). CUDA's
-// fp8 -> half conversion, then fp32 scale, then the bf16 pack.
-__device__ __forceinline__ void fp8x16_to_bf16(uint4 raw, float scale, uint4& lo, uint4& hi) {
-  const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-  uint32_t o[8];
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const __half2_raw hr =
-          __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)((w[i] >> (16 * h)) & 0xFFFFu), __NV_E4M3);
-      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hr));
-      const __nv_bfloat162 b = __floats2bfloat162_rn(f.x * scale, f.y * scale);
-      o[2 * i + h] = *reinterpret_cast<const uint32_t*>(&b);
-    }
-  lo = make_uint4(o[0], o[1], o[2], o[3]);
-  hi = make_uint4(o[4], o[5], o[6], o[7]);
+// Instruction descriptor, kind::mxf8f6f4 with block scaling: A and B E4M3 (format 0),
+// both K-major, scale factors E8M0 (bit 23), M x N; the scale-factor IDs (bits 29-30
+// for A, 4-5 for B) pick the byte of each 32-bit tensor-memory scale word, i.e. which
+// 32-element K block of the stage the MMA uses.
+__host__ __device__ constexpr uint32_t idesc_mx(int M, int N, uint32_t sf_id) {
+  return (sf_id << 4) | (1u << 23) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24) | (sf_id << 29);
+}
+// D (+)= (A x 2^sA) (B x 2^sB)^T over K = 32 E4M3 elements, scales read from tensor memory.
+__device__ __forceinline__ void umma_mx(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                        uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.block32 [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+      :
+      : "r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+// Shared-memory descriptor of a 32-row x 16-byte scale atom (no swizzle: 8-row core
+// matrices of 128 contiguous bytes, 128 bytes apart), the source of tcgen05.cp.
+__device__ __forceinline__ uint64_t sf_desc(uint32_t saddr) {
+  uint64_t desc = 0;
+  desc |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  desc |= (uint64_t)(128 >> 4) << 16;
+  desc |= (uint64_t)(128 >> 4) << 32;
+  desc |= (uint64_t)1 << 46;
+  return desc;
+}
+// Copy a scale atom (32 rows of 16 bytes) into 4 tensor-memory columns of every lane
+// quadrant: lane 32q + i, column c holds the 4 scale bytes of row 32c + i. The MMA
+// reads row r's scale at lane r % 32 (+ 32q), column r / 32, byte = scale-factor ID.
+__device__ __forceinline__ void tc_cp_sf(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+// 4-byte asynchronous copy global -> shared; src_bytes 0 writes zeros and reads nothing.
+__device__ __forceinline__ void cp_async4(void* dst, const void* src, bool read) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(read ? 4 : 0)
+               : "memory");
+}
+// The barrier receives one arrival once all of this thread's earlier cp.async copies
+// have landed (counted in the barrier's expected arrivals).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
 // PAIR: the tile is 256 x BN on a CTA pair; each CTA stages its 128 rows of A and
 // half (BN / 2 rows) of B.
-// FP8R > 0 (MXFP8 routed weights): B arrives as E4M3 codes (64 bytes per row and K block,
-// 64-byte swizzle) in a deep ring of its own, and eight converter warps write the bf16 B
-// tile into the short ring of MMA operands; the epilogue has 4 warps, so the block keeps
-// its 448 threads. A tile covers FP8R rows of A (32 for decode batches: a 4 KB box; the
-// M = 128 MMA reads the 16 KB after it, whose extra rows are never stored).
-template <int BN, bool PAIR = false, int FP8R = 0>
+// MXR > 0, the MXFP8 form (tcgen05 kind::mxf8f6f4 with E8M0 block scales): A and B
+// arrive as E4M3 codes, 128 per row and stage (one 128-byte swizzle atom, as 64 bf16
+// are), and each stage's scale bytes go to a third ring of 32 x 16-byte atoms that
+// tcgen05.cp moves into tensor memory beside the accumulators. A tile covers MXR rows
+// of A (32 for decode batches: a 4 KB box; the M = 128 MMA reads the 16 KB after the
+// slot's start, whose extra rows are never stored).
+template <int BN, bool PAIR = false, int MXR = 0>
 struct Cfg {
-  static constexpr bool kFp8 = FP8R != 0;
-  static constexpr int kTileRows = kFp8 ? FP8R : BM;  // A rows of a tile
-  static constexpr int kEpiW = kFp8 ? 4 : kEpiWarps;  // epilogue warps
-  static constexpr int kConvW = kFp8 ? 8 : 0;         // converter warps (two per scheduler)
-  static constexpr int kStagingBytes = 2048;          // per epilogue warp: 32 rows x 64 B (bf16 block of 32 x 32)
-  static constexpr int kABytes = kTileRows * BK * 2;  // A bytes loaded per K block
-  static constexpr int kBBytes = (PAIR ? BN / 2 : BN) * BK * 2;
-  static constexpr int kStageBytes = kABytes + kBBytes;  // bf16 form: one stage of A and B
-  // bf16 form: one ring of A + B stages. FP8 form: a ring of A slots (the producer runs far
-  // ahead on them), a short ring of converted bf16 B tiles, and a ring of FP8 codes whose
-  // stages hold two K blocks (128-byte rows, full-line copies).
-  static constexpr int kStages =
-      kFp8 ? 2 : ((192 * 1024) / kStageBytes > 8 ? 8 : (192 * 1024) / kStageBytes);
-  static constexpr int kAStages = kFp8 ? (kTileRows <= 32 ? 8 : 4) : kStages;
-  static constexpr int kRawBytes = kFp8 ? BN * 2 * BK : 1;
-  static constexpr int kRawBudget = 220 * 1024 - kEpiW * kStagingBytes - kAStages * kABytes - kStages * kBBytes;
-  static constexpr int kRawStages = !kFp8 ? 0 : (kRawBudget / kRawBytes > 8 ? 8 : kRawBudget / kRawBytes);
-  static constexpr int kRingBytes = kAStages * kABytes + kStages * kBBytes + (kFp8 ? kRawStages * kRawBytes : 0);
-  static constexpr int kTmemCols = 2 * BN;
-  static constexpr size_t kSmem = (size_t)kRingBytes + (size_t)kEpiW * kStagingBytes + 1024;
-  static_assert(64 + 32 * (kEpiW + kConvW) == kThreads, "every form runs 448 threads");
-  static_assert(!kFp8 || !PAIR, "FP8 B on single CTAs only");
-  static_assert(!kFp8 || kRawStages >= 2, "the FP8 code ring needs depth");
-  // the M = 128 MMA reads 16 KB of A from a slot's start: past a short slot come later A
-  // slots and then the B ring, all shared memory of this block
-  static_assert(kStages * kBBytes >= BM * BK * 2 - kABytes, "A overhang");
+  static constexpr bool kMx = MXR != 0;
+  static constexpr int kTileRows = kMx ? MXR : BM;  // A rows of a tile
+  static constexpr int kStageK = kMx ? 128 : BK;    // K elements per stage (128 bytes of a row)
+  static constexpr int kStagingBytes = 2048;        // per epilogue warp: 32 rows x 64 B
+  static constexpr int kABytes = kTileRows * 128;
+  static constexpr int kBBytes = (PAIR ? BN / 2 : BN) * 128;
+  static constexpr int kSFBytes = kMx ? 512 * (1 + BN / 128) : 0;  // the A atom, then B's
+  static constexpr int kTxBytes = kABytes + kBBytes;                // TMA bytes per stage
+  static constexpr int kStageBytes = kTxBytes + kSFBytes;
+  static constexpr int kStages = (192 * 1024) / kStageBytes > 8 ? 8 : (192 * 1024) / kStageBytes;
+  static constexpr int kRingBytes = kStages * kStageBytes;  // A slots, B slots, scale atoms
+  static constexpr int kSFCols = 4 + 4 * (BN / 128);         // tensor-memory columns of a stage's scales
+  static constexpr int kTmemCols = kMx ? 512 : 2 * BN;       // two accumulators (+ the scale ring)
+  static constexpr size_t kSmem = (size_t)kRingBytes + (size_t)kEpiWarps * kStagingBytes + 1024;
+  static_assert(!kMx || (!PAIR && BN == 128), "MXFP8 tiles: single CTAs, 128 columns");
+  static_assert(!kMx || 2 * BN + kStages * kSFCols <= 512, "accumulators and scales fit tensor memory");
+  // the M = 128 MMA reads 16 KB of A from a slot's start: past a short slot come later
+  // A slots, then the B slots and the scale atoms, all shared memory of this block
+  static_assert((kStages - 1) * kABytes + BM * 128 <= kRingBytes, "A overhang");
 };
 
 struct TileInfo {
@@ -496,7 +528,7 @@ __device__ __forceinline__ const CUtensorMap* pick_map(int i, const CUtensorMap&
   }
 }
 
-template <int BN, int EPI, bool PAIR, int FP8R = 0>
+template <int BN, int EPI, bool PAIR, int MXR = 0>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap m0, const __grid_constant__ CUtensorMap m1,
                         const __grid_constant__ CUtensorMap m2, const __grid_constant__ CUtensorMap m3,
@@ -504,28 +536,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const __grid_constant__ CUtensorMap o0, const __grid_constant__ CUtensorMap o1,
                         const __grid_constant__ Params P) {
   static_assert(!PAIR || EPI == kLinear, "CTA pairs serve the down-projection (one B map, linear epilogue)");
-  using C = Cfg<BN, PAIR, FP8R>;
-  constexpr bool FP8B = C::kFp8;
+  using C = Cfg<BN, PAIR, MXR>;
+  constexpr bool kMx = C::kMx;
   constexpr int kTR = C::kTileRows;
-  constexpr int kEpiW = C::kEpiW;
+  constexpr int kKE = C::kStageK;
   constexpr int kStages = C::kStages;
-  constexpr int kAStages = C::kAStages;
-  constexpr int kRawStages = C::kRawStages;
   constexpr int kOutCols = EPI == kSwiglu ? BN / 2 : BN;
   constexpr uint32_t kIdesc = idesc_bf16(PAIR ? 2 * BM : BM, BN);
-  // half tiles (N = BN / 2) for the last wave: one-B-map, whole-width epilogues only
-  constexpr bool kCanSplit = !PAIR && (EPI == kGelu || EPI == kLinear);
+  // half tiles (N = BN / 2) for the last wave: bf16, one-B-map, whole-width epilogues only
+  constexpr bool kCanSplit = !PAIR && !kMx && (EPI == kGelu || EPI == kLinear);
   constexpr uint32_t kIdescHalf = idesc_bf16(BM, BN / 2);
 
   extern __shared__ uint8_t smem_raw[];
-  // full_bar: the A (+ B) bytes of a slot of the A ring; empty_bar: the MMA is done with a
-  // stage of the B ring (bf16 form: the same ring). FP8 form: a_empty frees A slots,
-  // bfull_bar counts the converter warps' bf16 B tiles, raw_full / raw_empty run the ring
-  // of FP8 codes.
-  __shared__ __align__(8) uint64_t full_bar[kAStages], empty_bar[kStages], tfull_bar[2], tempty_bar[2], done_bar;
-  __shared__ __align__(8) uint64_t a_empty[FP8B ? kAStages : 1], bfull_bar[FP8B ? kStages : 1];
-  __shared__ __align__(8) uint64_t raw_full[FP8B ? kRawStages : 1], raw_empty[FP8B ? kRawStages : 1];
-  __shared__ int32_t s_gid[FP8B ? kTR : 1];  // FP8B with gathered A: the tile's row ids
+  // full_bar: a stage's operands have landed (MXFP8 form: and the 32 producer lanes'
+  // scale copies); empty_bar: the MMAs are done with the stage.
+  __shared__ __align__(8) uint64_t full_bar[kStages], empty_bar[kStages], tfull_bar[2], tempty_bar[2], done_bar;
   __shared__ uint32_t s_tmem_base;
   __shared__ int32_t s_start[kMaxGroups + 1];
   __shared__ Family s_fam[2];
@@ -538,29 +563,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int walk_step = PAIR ? (int)nclusters_x() : (int)gridDim.x;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   uint8_t* sA = smem;
-  uint8_t* sB = smem + kAStages * C::kABytes;
-  uint8_t* sRaw = sB + kStages * C::kBBytes;  // FP8B: the ring of FP8 B codes
+  uint8_t* sB = smem + kStages * C::kABytes;
+  uint8_t* sSF = sB + kStages * C::kBBytes;  // MXFP8 form: the scale atoms of each stage
   const int32_t* off = P.expert_off;
 
   if (threadIdx.x == 0) {
     s_fam[0] = P.fam[0];
     s_fam[1] = P.fam[1];
     s_abort = 0;
-    for (int s = 0; s < kAStages; ++s) {
-      mbar_init(&full_bar[s], 1);
-      if (FP8B) mbar_init(&a_empty[s], 1);
-    }
     for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full_bar[s], kMx ? 33 : 1);  // MXFP8: + one cp.async arrival per producer lane
       mbar_init(&empty_bar[s], 1);
-      if (FP8B) mbar_init(&bfull_bar[s], C::kConvW);
-    }
-    for (int s = 0; s < kRawStages; ++s) {
-      mbar_init(&raw_full[s], 1);
-      mbar_init(&raw_empty[s], C::kConvW);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull_bar[a], 1);
-      mbar_init(&tempty_bar[a], PAIR ? 2 * kEpiW : kEpiW);
+      mbar_init(&tempty_bar[a], PAIR ? 2 * kEpiWarps : kEpiWarps);
     }
     mbar_init(&done_bar, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -621,104 +638,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   volatile int32_t* abort_flag = &s_abort;
 
-  if (FP8B && warp == 0) {
-    // ---------------- TMA producer, FP8 form ----------------
-    // Lane 0 issues, per pair of K blocks, one copy of the FP8 codes (128-byte rows) into
-    // the code ring, and per K block the tile's A rows into the A ring (a box, or gathered
-    // rows with the ids in s_gid); both rings run ahead of the converters and the MMA.
-    if (lane == 0) {
-      int rst = 0, ast = 0;
-      uint32_t rph = 0, aph = 0;
-      int32_t raw_parity[kRawStages > 0 ? kRawStages : 1], a_parity[kAStages];
-#pragma unroll
-      for (int s = 0; s < kRawStages; ++s) raw_parity[s] = -1;
-#pragma unroll
-      for (int s = 0; s < kAStages; ++s) a_parity[s] = -1;
-      bool ok = true;
-      for (int it = 0, tile, half; ok && walk.item(it, tile, half); ++it) {
-        const TileInfo ti = decode_tile<false, kTR>(tile, s_start, G, G0, s_fam, off, 0);
-        const Family& F = s_fam[ti.fam];
-        const CUtensorMap* ma = pick_map(F.a_map, m0, m1, m2, m3, m4, m5);
-        const CUtensorMap* mb = pick_map(F.b_map, m0, m1, m2, m3, m4, m5);
-        const CUtensorMap* mb3 = pick_map(F.b3_map, m0, m1, m2, m3, m4, m5);
-        const bool gather = F.gather_rows != nullptr;
-        if (gather) {  // the tile's row ids (rows past the group's end repeat its first row)
-          const int row0 = ti.a_row0 - ti.mt * kTR;
-          for (int r = 0; r < kTR; ++r) {
-            const int src = ti.mt * kTR + r < ti.m ? ti.a_row0 + r : row0;
-            int32_t id = F.gather_rows[src];
-            if (id < 0 || id >= F.gather_n) {
-              record_error(P.status, kErrIndex, 204, src, id);
-              id = 0;
-            }
-            s_gid[r] = id;
-          }
-        }
-        for (int kb = 0; kb < F.k_blocks; ++kb) {
-          if ((kb & 1) == 0) {  // codes of K blocks kb and kb + 1 (k_blocks is even)
-            if (!mbar_wait<false>(&raw_empty[rst], rph ^ 1u, abort_flag, P.wait_ns)) {
-              ok = false;
-              break;
-            }
-            raw_parity[rst] = (int32_t)rph;
-            uint64_t* rb = &raw_full[rst];
-            mbar_arrive_expect_tx(rb, C::kRawBytes);
-            uint8_t* raw = sRaw + rst * C::kRawBytes;
-            if (EPI == kSwiglu) {
-              const int by = ti.g * F.b_rows_group + ti.nt * (BN / 2);
-              tma_load_2d(mb, rb, raw, kb * BK, by);
-              tma_load_2d(mb3, rb, raw + (BN / 2) * 2 * BK, kb * BK, by);
-            } else {
-              tma_load_2d(mb, rb, raw, kb * BK, ti.g * F.b_rows_group + ti.nt * BN);
-            }
-            if (++rst == kRawStages) {
-              rst = 0;
-              rph ^= 1u;
-            }
-          }
-          if (!mbar_wait<false>(&a_empty[ast], aph ^ 1u, abort_flag, P.wait_ns)) {
-            ok = false;
-            break;
-          }
-          a_parity[ast] = (int32_t)aph;
-          mbar_arrive_expect_tx(&full_bar[ast], C::kABytes);
-          uint8_t* a = sA + ast * C::kABytes;
-          if (gather) {
-            for (int i = 0; i < kTR / 4; ++i)
-              tma_gather4(ma, &full_bar[ast], a + i * (4 * BK * 2), kb * BK, s_gid[4 * i], s_gid[4 * i + 1],
-                          s_gid[4 * i + 2], s_gid[4 * i + 3]);
-          } else {
-            tma_load_2d(ma, &full_bar[ast], a, kb * BK, ti.a_row0);
-          }
-          if (++ast == kAStages) {
-            ast = 0;
-            aph ^= 1u;
-          }
-        }
-      }
-      if (!ok) {
-        record_error(P.status, kErrTimeout, 201, (int32_t)blockIdx.x, 0);
-        s_abort = 1;
-        // let our own copies land before the CTA's shared memory goes away
-        for (int s = 0; s < kRawStages; ++s)
-          if (raw_parity[s] >= 0) {
-            const unsigned long long t0 = globaltimer();
-            while (!mbar_try_wait<true>(&raw_full[s], (uint32_t)raw_parity[s]) && globaltimer() - t0 < kTimeoutNs) {
-            }
-          }
-        for (int s = 0; s < kAStages; ++s)
-          if (a_parity[s] >= 0) {
-            const unsigned long long t0 = globaltimer();
-            while (!mbar_try_wait<true>(&full_bar[s], (uint32_t)a_parity[s]) && globaltimer() - t0 < kTimeoutNs) {
-            }
-          }
-      }
-    }
-  } else if (warp == 0 && !FP8B) {
+  if (warp == 0) {
     // ---------------- TMA producer ----------------
     // Lane 0 waits for free stages and issues the copies; for a gathering family the
     // 32 lanes issue one tile::gather4 each (4 of the tile's 128 A rows, row ids held in
-    // registers for the tile), after lane 0 has set the stage's expected bytes.
+    // registers for the tile), after lane 0 has set the stage's expected bytes. MXFP8
+    // form: the 32 lanes also copy the stage's scale bytes (cp.async, 4 bytes = one
+    // row's four 32-element blocks) into the tensor-memory copy layout, row r of a
+    // 128-row atom at byte 16 (r % 32) + 4 (r / 32), each lane then adding one arrival
+    // on the stage's barrier when its copies have landed.
     int stage = 0;
     uint32_t phase = 0;
     int32_t last_parity[kStages];
@@ -726,7 +654,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < kStages; ++s) last_parity[s] = -1;
     bool ok = true;
     for (int it = 0, tile, half; ok && walk.item(it, tile, half); ++it) {
-      const TileInfo ti = decode_tile<PAIR>(tile, s_start, G, G0, s_fam, off, (int)rank);
+      const TileInfo ti = decode_tile<PAIR, kTR>(tile, s_start, G, G0, s_fam, off, (int)rank);
       const Family& F = s_fam[ti.fam];
       const CUtensorMap* ma = pick_map(F.a_map, m0, m1, m2, m3, m4, m5);
       const CUtensorMap* mb = pick_map(F.b_map, m0, m1, m2, m3, m4, m5);
@@ -774,18 +702,42 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else {
             // a half tile stages the whole B tile too (one BN-row copy: two half-height
             // copies per stage measured slower than the bytes they save)
-            mbar_arrive_expect_tx(&full_bar[stage], C::kStageBytes);
+            mbar_arrive_expect_tx(&full_bar[stage], C::kTxBytes);
             last_parity[stage] = (int32_t)phase;
-            if (!gather) tma_load_2d(ma, &full_bar[stage], sA + stage * C::kABytes, (k0 + kb) * BK, ti.a_row0);
+            if (!gather) tma_load_2d(ma, &full_bar[stage], sA + stage * C::kABytes, (k0 + kb) * kKE, ti.a_row0);
             if (EPI == kSwiglu) {
               const int by = ti.g * F.b_rows_group + kseg * F.b_rows_kseg + ti.nt * (BN / 2);
-              tma_load_2d(mb, &full_bar[stage], sB + stage * C::kBBytes, kin * BK, by);
-              tma_load_2d(mb3, &full_bar[stage], sB + stage * C::kBBytes + (BN / 2) * BK * 2, kin * BK, by);
+              tma_load_2d(mb, &full_bar[stage], sB + stage * C::kBBytes, kin * kKE, by);
+              tma_load_2d(mb3, &full_bar[stage], sB + stage * C::kBBytes + (BN / 2) * 128, kin * kKE, by);
             } else {
               const int by = ti.g * F.b_rows_group + kseg * F.b_rows_kseg + ti.nt * BN;
-              tma_load_2d(mb, &full_bar[stage], sB + stage * C::kBBytes, kin * BK, by);
+              tma_load_2d(mb, &full_bar[stage], sB + stage * C::kBBytes, kin * kKE, by);
             }
           }
+        }
+        if constexpr (kMx) {
+          uint8_t* sf = sSF + stage * C::kSFBytes;
+#pragma unroll
+          for (int j = 0; j < kTR / 32; ++j) {  // A rows past the matrix read nothing (zeros)
+            const int row = ti.a_row0 + lane + 32 * j;
+            const bool in = row < F.a_rows;
+            cp_async4(sf + 16 * lane + 4 * j, F.a_scale + (int64_t)(in ? row : 0) * F.a_scale_ld + 4 * kb, in);
+          }
+#pragma unroll
+          for (int j = 0; j < BN / 32; ++j) {  // B rows: W1 then W3 halves (SwiGLU), else BN rows
+            const int n = lane + 32 * j;
+            const uint8_t* src;
+            if (EPI == kSwiglu) {
+              const bool up = n >= BN / 2;
+              const int64_t brow =
+                  (int64_t)ti.g * F.b_rows_group + (int64_t)ti.nt * (BN / 2) + (up ? n - BN / 2 : n);
+              src = (up ? F.b3_scale : F.b_scale) + brow * F.scale_ld;
+            } else {
+              src = F.b_scale + ((int64_t)ti.g * F.b_rows_group + (int64_t)ti.nt * BN + n) * F.scale_ld;
+            }
+            cp_async4(sf + 512 * (1 + (j >> 2)) + 16 * lane + 4 * (j & 3), src + 4 * kb, true);
+          }
+          cp_async_arrive_noinc(&full_bar[stage]);
         }
         if (gather) {
           __syncwarp();  // the stage's expected bytes are set before any gathered row lands
@@ -813,15 +765,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------- MMA issuer ----------------
-      int stage = 0, acc = 0, ast = 0;
-      uint32_t phase = 0, acc_phase = 0, aph = 0;
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
       for (int it = 0, tile, half; ok && (!PAIR || rank == 0) && walk.item(it, tile, half); ++it) {
         const TileInfo ti = decode_tile<PAIR, kTR>(tile, s_start, G, G0, s_fam, off, (int)rank);
         const int kblocks = s_fam[ti.fam].k_blocks;
         // a half tile multiplies by B's rows [half * BN/2, (half + 1) * BN/2) into accumulator columns [0, BN/2)
         const uint32_t idesc = half < 0 ? kIdesc : kIdescHalf;
-        const uint32_t b_off = half < 0 ? 0u : (uint32_t)half * (BN / 2) * BK * 2;
+        const uint32_t b_off = half < 0 ? 0u : (uint32_t)half * (BN / 2) * 128;
         if (!mbar_wait<false>(&tempty_bar[acc], acc_phase ^ 1u, abort_flag, P.wait_ns)) {
           ok = false;
           break;
@@ -829,32 +781,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
         for (int kb = 0; kb < kblocks; ++kb) {
-          // A slot ast and B stage `stage` (the same index in the bf16 form's one ring)
-          if (!mbar_wait<false>(&full_bar[FP8B ? ast : stage], FP8B ? aph : phase, abort_flag, P.wait_ns) ||
-              (FP8B && !mbar_wait<false>(&bfull_bar[stage], phase, abort_flag, P.wait_ns))) {
+          if (!mbar_wait<false>(&full_bar[stage], phase, abort_flag, P.wait_ns)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t a_addr = smem_u32(sA + (FP8B ? ast : stage) * C::kABytes);
+          const uint32_t a_addr = smem_u32(sA + stage * C::kABytes);
           const uint32_t b_addr = smem_u32(sB + stage * C::kBBytes) + b_off;
+          if constexpr (kMx) {
+            // the stage's scale atoms (written through the generic proxy by cp.async) into
+            // its tensor-memory columns; a stage's columns are reused only after the stage
+            // has been refilled, i.e. after the MMAs that read them have completed
+            fence_proxy_async_smem();
+            const uint32_t sfa = tmem_base + (uint32_t)(2 * BN + stage * C::kSFCols);
+            const uint32_t sf_smem = smem_u32(sSF + stage * C::kSFBytes);
+            tc_cp_sf(sfa, sf_desc(sf_smem));
+            tc_cp_sf(sfa + 4, sf_desc(sf_smem + 512));
 #pragma unroll
-          for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-            if constexpr (PAIR)
-              umma_bf16_pair(d_tmem, sw128_desc(a_addr + kk * UMMA_K * 2), sw128_desc(b_addr + kk * UMMA_K * 2),
-                             kIdesc, (kb | kk) != 0 ? 1u : 0u);
-            else
-              umma_bf16(d_tmem, sw128_desc(a_addr + kk * UMMA_K * 2), sw128_desc(b_addr + kk * UMMA_K * 2), idesc,
-                        (kb | kk) != 0 ? 1u : 0u);
-          }
-          umma_commit_t<PAIR>(&empty_bar[stage]);
-          if (FP8B) {
-            umma_commit_t<PAIR>(&a_empty[ast]);
-            if (++ast == kAStages) {
-              ast = 0;
-              aph ^= 1u;
+            for (int kk = 0; kk < 4; ++kk)  // K = 32 codes per MMA: the scale word's byte kk
+              umma_mx(d_tmem, sw128_desc(a_addr + kk * 32), sw128_desc(b_addr + kk * 32),
+                      idesc_mx(BM, BN, (uint32_t)kk), sfa, sfa + 4, (kb | kk) != 0 ? 1u : 0u);
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+              if constexpr (PAIR)
+                umma_bf16_pair(d_tmem, sw128_desc(a_addr + kk * UMMA_K * 2), sw128_desc(b_addr + kk * UMMA_K * 2),
+                               kIdesc, (kb | kk) != 0 ? 1u : 0u);
+              else
+                umma_bf16(d_tmem, sw128_desc(a_addr + kk * UMMA_K * 2), sw128_desc(b_addr + kk * UMMA_K * 2),
+                          idesc, (kb | kk) != 0 ? 1u : 0u);
             }
           }
+          umma_commit_t<PAIR>(&empty_bar[stage]);
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1u;
@@ -877,105 +835,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       const unsigned long long t0 = globaltimer();
       while (!mbar_try_wait<true>(&done_bar, 0u) && globaltimer() - t0 < kTimeoutNs) {
       }
-    }
-  } else if (FP8B && warp >= 2 + kEpiW) {
-    // ---------------- FP8 B converters ----------------
-    // 16-byte units: unit u of a K block is chunk u % 4 (16 codes) of B row u / 4; thread
-    // ct (0..255) takes units ct, ct + 256, ... A warp's 32 units are 8 whole rows, read
-    // from the code ring (64-byte swizzle: chunk j of row r at j ^ ((r >> 1) & 3)) and
-    // written as bf16 into the operand ring in the MMA's 128-byte swizzle (16-byte chunk c
-    // of row r at c ^ (r & 7)), both without bank conflicts. Each chunk's 16 codes share
-    // the row's E8M0 byte for their half of the K block; scale bytes come from global
-    // memory 16 at a time (8 K blocks), the next 16 loaded one group ahead.
-    const int ct = (int)threadIdx.x - 32 * (2 + kEpiW);
-    constexpr int kUnits = BN * 4;  // 16-byte chunks of codes per K block
-    constexpr int kConvT = 32 * (C::kConvW > 0 ? C::kConvW : 1);
-    constexpr int kUnitsPerThread = (kUnits + kConvT - 1) / kConvT;
-    int rs = 0, stage = 0;
-    uint32_t rphase = 0, phase = 0;
-    bool ok = true;
-    for (int it = 0, tile, half; ok && walk.item(it, tile, half); ++it) {
-      const TileInfo ti = decode_tile<false, kTR>(tile, s_start, G, G0, s_fam, off, 0);
-      const Family& F = s_fam[ti.fam];
-      const uint8_t* srow[kUnitsPerThread];
-#pragma unroll
-      for (int i = 0; i < kUnitsPerThread; ++i) {
-        const int r = (ct + kConvT * i) >> 2;
-        int64_t brow;
-        const uint8_t* base;
-        if (EPI == kSwiglu) {
-          const bool up = r >= BN / 2;
-          brow = (int64_t)ti.g * F.b_rows_group + (int64_t)ti.nt * (BN / 2) + (up ? r - BN / 2 : r);
-          base = up ? F.b3_scale : F.b_scale;
-        } else {
-          brow = (int64_t)ti.g * F.b_rows_group + (int64_t)ti.nt * BN + r;
-          base = F.b_scale;
-        }
-        srow[i] = base + brow * F.scale_ld;
-      }
-      uint4 sc[kUnitsPerThread], sc_next[kUnitsPerThread];
-#pragma unroll
-      for (int i = 0; i < kUnitsPerThread; ++i)
-        if (ct + kConvT * i < kUnits) sc_next[i] = __ldg(reinterpret_cast<const uint4*>(srow[i]));
-      for (int kb = 0; kb < F.k_blocks; ++kb) {
-        if ((kb & 7) == 0) {
-#pragma unroll
-          for (int i = 0; i < kUnitsPerThread; ++i) {
-            sc[i] = sc_next[i];
-            if (ct + kConvT * i < kUnits && kb + 8 < F.k_blocks)
-              sc_next[i] = __ldg(reinterpret_cast<const uint4*>(srow[i]) + (kb >> 3) + 1);
-          }
-        }
-        int w_ok = 1;
-        // the codes have landed and the MMA is done with the operand slot (polled: these
-        // waits are on the weight stream's critical path)
-        if (lane == 0)
-          w_ok = mbar_wait<false>(&raw_full[rs], rphase, abort_flag, P.wait_ns) &&
-                         mbar_wait<false>(&empty_bar[stage], phase ^ 1u, abort_flag, P.wait_ns)
-                     ? 1
-                     : 0;
-        if (!__shfl_sync(kFull, w_ok, 0)) {
-          ok = false;
-          break;
-        }
-        const uint8_t* raw = sRaw + rs * C::kRawBytes;
-        const int kh = kb & 1;  // which of the code stage's two K blocks
-        uint8_t* bt = sB + stage * C::kBBytes;
-#pragma unroll
-        for (int i = 0; i < kUnitsPerThread; ++i) {
-          const int u = ct + kConvT * i;
-          if (u >= kUnits) continue;
-          const int r = u >> 2, j = u & 3;
-          // this chunk's scale: byte 2 (kb % 8) + j / 2 of the row's 16-byte group
-          const uint32_t sb = (uint32_t)(kb & 7) * 2 + (uint32_t)(j >> 1);
-          const uint32_t sword = (&sc[i].x)[sb >> 2];
-          const float scale = __uint_as_float(((sword >> (8 * (sb & 3))) & 0xFFu) << 23);
-          // 128-byte rows of two K blocks, 128-byte swizzle: chunk c of row r at c ^ (r & 7)
-          const uint4 codes = *reinterpret_cast<const uint4*>(raw + r * 128 + 16 * ((4 * kh + j) ^ (r & 7)));
-          uint4 lo, hi;
-          fp8x16_to_bf16(codes, scale, lo, hi);
-          *reinterpret_cast<uint4*>(bt + r * 128 + 16 * ((2 * j) ^ (r & 7))) = lo;
-          *reinterpret_cast<uint4*>(bt + r * 128 + 16 * ((2 * j + 1) ^ (r & 7))) = hi;
-        }
-        fence_proxy_async_smem();  // the tensor core reads the tile through the async proxy
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&bfull_bar[stage]);
-          if (kh) mbar_arrive(&raw_empty[rs]);  // both K blocks of the code stage are converted
-        }
-        if (kh && ++rs == kRawStages) {
-          rs = 0;
-          rphase ^= 1u;
-        }
-        if (++stage == kStages) {
-          stage = 0;
-          phase ^= 1u;
-        }
-      }
-    }
-    if (!ok && lane == 0) {
-      record_error(P.status, kErrTimeout, 205, (int32_t)blockIdx.x, 0);
-      s_abort = 1;
     }
   } else {
     // ---------------- epilogue warps ----------------
@@ -1007,7 +866,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool valid = r < kTR && ti.mt * kTR + r < ti.m;
       // bf16 outputs of a warp whose 32 rows all belong to the group go out as one
       // TMA block store; a group's ragged last rows are stored row by row.
-      const bool use_tma = EPI != kLogits && F.tma_out && q * 32 + 32 <= kTR && ti.mt * kTR + q * 32 + 32 <= ti.m;
+      const bool use_tma = EPI != kLogits && (!kMx || EPI == kLinear) && F.tma_out && q * 32 + 32 <= kTR &&
+                           ti.mt * kTR + q * 32 + 32 <= ti.m;
       const int64_t grow = (int64_t)ti.a_row0 + r;
       const uint32_t tbase = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(q * 32) << 16);
       // H tiles (GELU / SwiGLU) are stored as bf16 for the next GEMM; gate-scaled
@@ -1025,6 +885,53 @@ __global__ void __launch_bounds__(kThreads, 1)
       // one 32-column chunk: registers v (and u, the W3 half for SwiGLU) -> outputs.
       // bf16 results are packed in place (pk), fp32 results overwrite v.
       auto finish_chunk = [&](uint32_t(&v)[32], uint32_t(&u)[32], int c) {
+        if constexpr (kMx && EPI != kLinear) {
+          // MXFP8 H: the chunk's 32 columns of the row are one MX block, stored as 32
+          // E4M3 codes and their E8M0 scale byte
+          float hv[32];
+          if (EPI == kSwiglu) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float2 h = act::silu_mul2(make_float2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])),
+                                              make_float2(__uint_as_float(u[2 * i]), __uint_as_float(u[2 * i + 1])));
+              hv[2 * i] = h.x;
+              hv[2 * i + 1] = h.y;
+            }
+          } else {
+            uint4 braw[4] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0),
+                             make_uint4(0, 0, 0, 0)};
+            if (bias) {  // routed experts: one bias vector
+              const uint4* bp = reinterpret_cast<const uint4*>(bias + bcol0 + c);
+#pragma unroll
+              for (int q4 = 0; q4 < 4; ++q4) braw[q4] = __ldg(bp + q4);
+            }
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const uint32_t bw = (&braw[i >> 2].x)[i & 3];  // bf16x2: low half = column 2i
+              const float2 a = __fadd2_rn(make_float2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])),
+                                          make_float2(__uint_as_float(bw << 16), __uint_as_float(bw & 0xFFFF0000u)));
+              const float2 g = act::gelu2_as7128(a);
+              hv[2 * i] = g.x;
+              hv[2 * i + 1] = g.y;
+            }
+          }
+          float amax = 0.f;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(hv[i]));
+          const uint32_t sb = mx::scale_byte(amax);
+          const float inv = mx::inv_scale(sb);
+          uint32_t q8[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            q8[i] = mx::e4m3x4(hv[4 * i] * inv, hv[4 * i + 1] * inv, hv[4 * i + 2] * inv, hv[4 * i + 3] * inv);
+          if (valid) {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(F.out) + out_off + c);
+            dst[0] = make_uint4(q8[0], q8[1], q8[2], q8[3]);
+            dst[1] = make_uint4(q8[4], q8[5], q8[6], q8[7]);
+            F.out_scale[grow * F.out_scale_ld + (bcol0 + c) / 32] = (uint8_t)sb;
+          }
+          return;
+        }
         uint32_t pk[16];
         if (EPI == kSwiglu) {
 #pragma unroll
@@ -1136,9 +1043,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       };
 
-      // chunks c = part*32, part*32 + 32*(kEpiW/4), ... (none for quadrants past the tile's rows)
+      // chunks c = part*32, part*32 + 32*(kEpiWarps/4), ... (none for quadrants past the tile's rows)
       uint32_t va[32], ua[32];
-      for (int c = part * 32; q * 32 < kTR && c < out_cols; c += 32 * (kEpiW / 4)) {
+      for (int c = part * 32; q * 32 < kTR && c < out_cols; c += 32 * (kEpiWarps / 4)) {
         tmem_ld32(tbase + (uint32_t)c, va);
         if (EPI == kSwiglu) tmem_ld32(tbase + (uint32_t)(BN / 2 + c), ua);
         tmem_ld_wait(va);
@@ -1239,11 +1146,11 @@ int num_sms() {
 }
 
 // grid_cap > 0: at most this many CTAs (the rest of the SMs stay free for other work).
-template <int BN, int EPI, int FP8R = 0>
+template <int BN, int EPI, int MXR = 0>
 cudaError_t launch_t(const CUtensorMap (&maps)[8], const Params& P, int64_t max_tiles, cudaStream_t st,
                      int64_t grid_cap = 0) {
-  using C = Cfg<BN, false, FP8R>;
-  auto kern = grouped_gemm_kernel<BN, EPI, false, FP8R>;
+  using C = Cfg<BN, false, MXR>;
+  auto kern = grouped_gemm_kernel<BN, EPI, false, MXR>;
   static cudaError_t attr = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
   if (attr != cudaSuccess) return attr;
   int64_t grid = max_tiles < num_sms() ? max_tiles : num_sms();
@@ -1294,29 +1201,29 @@ cudaError_t launch_pair_t(const CUtensorMap (&maps)[8], const Params& P, int64_t
   return cudaLaunchKernelEx(&cfg, kern, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6], maps[7], P);
 }
 
-template <int EPI, int FP8R = 0>
+template <int EPI>
 cudaError_t launch_bn(int bn, const CUtensorMap (&maps)[8], const Params& P, int64_t max_tiles, cudaStream_t st,
                       int64_t grid_cap = 0) {
   switch (bn) {
-    case 256: return launch_t<256, EPI, FP8R>(maps, P, max_tiles, st, grid_cap);
-    case 128: return launch_t<128, EPI, FP8R>(maps, P, max_tiles, st, grid_cap);
-    default: return launch_t<64, EPI, FP8R>(maps, P, max_tiles, st, grid_cap);
+    case 256: return launch_t<256, EPI>(maps, P, max_tiles, st, grid_cap);
+    case 128: return launch_t<128, EPI>(maps, P, max_tiles, st, grid_cap);
+    default: return launch_t<64, EPI>(maps, P, max_tiles, st, grid_cap);
   }
 }
 
-// MXFP8 routed weights: tiles of 32 A rows when the experts average at most 32 rows
+// MXFP8 form: 128-column tiles of 32 A rows when the experts average at most 32 rows
 // (decode batches: the weight stream is the work, A is a 4 KB box), else 128.
 template <int EPI>
-cudaError_t launch_fp8(int bn, int rows, const CUtensorMap (&maps)[8], const Params& P, int64_t max_tiles,
-                       cudaStream_t st, int64_t grid_cap) {
-  return rows == 32 ? launch_bn<EPI, 32>(bn, maps, P, max_tiles, st, grid_cap)
-                    : launch_bn<EPI, 128>(bn, maps, P, max_tiles, st, grid_cap);
+cudaError_t launch_mx(int rows, const CUtensorMap (&maps)[8], const Params& P, int64_t max_tiles, cudaStream_t st,
+                      int64_t grid_cap) {
+  return rows == 32 ? launch_t<128, EPI, 32>(maps, P, max_tiles, st, grid_cap)
+                    : launch_t<128, EPI, 128>(maps, P, max_tiles, st, grid_cap);
 }
 
-// FP8 codes of a weight matrix [rows, K] (bytes): 128-byte rows (two K blocks) x
-// box_rows, 128-byte swizzle (the converters' conflict-free read order).
-bool make_fp8_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int box_rows) {
-  return make_map_ex(m, ptr, rows, cols, 2 * BK, box_rows, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1,
+// E4M3 codes of a matrix [rows, K] (bytes): 128-byte rows (128 codes, one stage) x
+// box_rows, 128-byte swizzle (the MMA's operand layout, as for 64 bf16).
+bool make_code_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int box_rows) {
+  return make_map_ex(m, ptr, rows, cols, 128, box_rows, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1,
                      CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
@@ -1382,19 +1289,121 @@ bool use_pair_tiles(const Plan& p, int bn) {
   return bn == 256 && R >= (int64_t)8 * tc::BM * p.E;
 }
 
+namespace {
+
+// The routed experts of an MXFP8 layer (kind::mxf8f6f4): xp holds the permuted rows'
+// E4M3 codes [R, d] and their E8M0 scales [R, d / 32] (mx::scale_offset), H is written
+// and read back the same way ([R, F] codes, [R, F / 32] scales), the weights are codes
+// and scales. The up-projection quantises H in its epilogue; the down-projection writes
+// gate-scaled fp32 rows like the bf16 form.
+cudaError_t launch_ffn_mx(const Plan& p, const void* xp, const int32_t* expert_off, const float* row_gate,
+                          const moe_weights* w, void* h, void* yp, int32_t* status, cudaStream_t st, int part,
+                          int64_t grid_cap) {
+  using namespace tc;
+  const int64_t R = p.max_rows > 0 ? p.max_rows : 1;
+  const int rows = R <= 32 * p.E ? 32 : 128;  // A rows per tile
+  const uint8_t* xq = static_cast<const uint8_t*>(xp);
+  uint8_t* h8 = static_cast<uint8_t*>(h);
+  if (part & 1) {
+    const int brows = p.swiglu ? 64 : 128;  // B rows per map copy (W1 and W3 halves for SwiGLU)
+    CUtensorMap maps[8];
+    bool ok = make_code_map(&maps[0], xq, R, p.d, rows) && make_code_map(&maps[2], w->w1, p.E * p.F, p.d, brows);
+    if (p.swiglu) ok = ok && make_code_map(&maps[3], w->w3, p.E * p.F, p.d, brows);
+    if (!ok) return cudaErrorInvalidValue;
+    for (int i : {1, 4, 5, 6, 7}) maps[i] = maps[0];
+    if (!p.swiglu) maps[3] = maps[0];
+    Params P{};
+    Family& f = P.fam[0];
+    f.groups = (int32_t)p.E;
+    f.m_from_off = 1;
+    f.n_tiles = (int32_t)(p.F / brows);
+    f.k_blocks = f.kseg_blocks = (int32_t)(p.d / 128);
+    f.b_rows_group = (int32_t)p.F;
+    f.a_map = 0;
+    f.b_map = 2;
+    f.b3_map = 3;
+    f.out = h8;
+    f.ld_out = p.F;
+    f.bias = static_cast<const __nv_bfloat16*>(p.bias ? w->b1 : nullptr);
+    f.bias_group = p.F;
+    f.bias_nsum = p.bias ? 1 : 0;
+    f.a_rows = (int32_t)R;
+    f.a_scale = xq + mx::scale_offset(R, p.d);
+    f.a_scale_ld = p.d / 32;
+    f.b_scale = w->w1_scale;
+    f.b3_scale = w->w3_scale;
+    f.scale_ld = p.d / 32;
+    f.out_scale = h8 + mx::scale_offset(R, p.F);
+    f.out_scale_ld = p.F / 32;
+    P.expert_off = expert_off;
+    P.status = status;
+    P.wait_ns = wait_limit_ns();
+    const int64_t max_tiles = (R / rows + p.E) * f.n_tiles;
+    const cudaError_t err = p.swiglu ? launch_mx<kSwiglu>(rows, maps, P, max_tiles, st, grid_cap)
+                                     : launch_mx<kGelu>(rows, maps, P, max_tiles, st, grid_cap);
+    if (err != cudaSuccess) return err;
+  }
+  if (part & 2) {
+    CUtensorMap maps[8];
+    if (!make_code_map(&maps[0], h8, R, p.F, rows) || !make_code_map(&maps[2], w->w2, p.E * p.d, p.F, 128) ||
+        !make_out_map_f32(&maps[6], yp, R, p.d))
+      return cudaErrorInvalidValue;
+    for (int i : {1, 3, 4, 5, 7}) maps[i] = maps[0];
+    Params P{};
+    Family& f = P.fam[0];
+    f.tma_out = 1;
+    f.groups = (int32_t)p.E;
+    f.m_from_off = 1;
+    f.n_tiles = (int32_t)(p.d / 128);
+    f.k_blocks = f.kseg_blocks = (int32_t)(p.F / 128);
+    f.b_rows_group = (int32_t)p.d;
+    f.a_map = 0;
+    f.b_map = 2;
+    f.b3_map = 2;
+    f.out = yp;
+    f.ld_out = p.d;
+    f.bias = static_cast<const __nv_bfloat16*>(p.bias ? w->b2 : nullptr);
+    f.bias_group = p.d;
+    f.bias_nsum = p.bias ? 1 : 0;
+    f.row_gate = row_gate;
+    f.a_rows = (int32_t)R;
+    f.a_scale = h8 + mx::scale_offset(R, p.F);
+    f.a_scale_ld = p.F / 32;
+    f.b_scale = w->w2_scale;
+    f.scale_ld = p.F / 32;
+    P.expert_off = expert_off;
+    P.status = status;
+    P.wait_ns = wait_limit_ns();
+    const cudaError_t err = launch_mx<kLinear>(rows, maps, P, (R / rows + p.E) * f.n_tiles, st, grid_cap);
+    if (err != cudaSuccess) return err;
+  }
+  return cudaSuccess;
+}
+
+}  // namespace
+
 // part: bit 0 = up-projections (routed + shared), bit 1 = down-projections.
 // gather_rows non-null: the routed up-projection reads its A rows straight from x
 // (row r of the expert-contiguous order is x[gather_rows[r]]) with tile::gather4, and
-// xp is not used.
+// xp is not used. MXFP8 layers: the routed experts run in the MXFP8 form, the shared
+// experts (bf16 weights) in launches of their own.
 cudaError_t launch_ffn_bf16(const Plan& p, const void* xp, const int32_t* expert_off, const float* row_gate,
                             const void* x, const moe_weights* w, void* h, void* hs, void* yp, void* ys,
                             int32_t* status, cudaStream_t st, int part, const int32_t* gather_rows, int families,
                             int64_t grid_cap) {
   using namespace tc;
+  if (p.fp8w) {
+    if (families & kRoutedFamily) {
+      const cudaError_t err = launch_ffn_mx(p, xp, expert_off, row_gate, w, h, yp, status, st, part, grid_cap);
+      if (err != cudaSuccess) return err;
+    }
+    if (!(families & kSharedFamily) || p.S == 0) return cudaSuccess;
+    Plan q = p;
+    q.fp8w = false;
+    return launch_ffn_bf16(q, xp, expert_off, row_gate, x, w, h, hs, yp, ys, status, st, part, nullptr,
+                           kSharedFamily, grid_cap);
+  }
   const int64_t R = p.max_rows > 0 ? p.max_rows : 1;
-  // MXFP8 routed weights: rows of A per tile (32 when the experts average at most 32 rows)
-  const int fp8r = R <= 32 * p.E ? 32 : 128;
-  const int a_rows = p.fp8w ? fp8r : BM;
   if (part & 1) {
     const int bn = pick_bn(p.swiglu, p.F, p.S > 0 ? p.Fs : 0);
     if (!bn) return cudaErrorInvalidValue;
@@ -1405,20 +1414,16 @@ cudaError_t launch_ffn_bf16(const Plan& p, const void* xp, const int32_t* expert
     const bool ok_a = !(families & kRoutedFamily) ? make_map(&maps[0], x, p.N, p.d, BM)
                       : gather_rows ? make_map_ex(&maps[0], x, p.N, p.d, BK, 1, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
                                                   CU_TENSOR_MAP_SWIZZLE_128B)
-                                    : make_map(&maps[0], xp, R, p.d, a_rows);
+                                    : make_map(&maps[0], xp, R, p.d, BM);
     if (!ok_a) return cudaErrorInvalidValue;
     for (int i = 1; i < 8; ++i) maps[i] = maps[0];  // unused slots hold a valid map
-    // routed B: bf16 rows, or (MXFP8 weights) FP8 codes that the converter warps dequantise
-    bool ok = p.fp8w ? make_fp8_map(&maps[2], w->w1, p.E * p.F, p.d, brows)
-                     : make_map(&maps[2], w->w1, p.E * p.F, p.d, brows);
-    if (p.swiglu)
-      ok = ok && (p.fp8w ? make_fp8_map(&maps[3], w->w3, p.E * p.F, p.d, brows)
-                         : make_map(&maps[3], w->w3, p.E * p.F, p.d, brows));
+    bool ok = (families & kRoutedFamily) ? make_map(&maps[2], w->w1, p.E * p.F, p.d, brows) : true;
+    if (p.swiglu && (families & kRoutedFamily)) ok = ok && make_map(&maps[3], w->w3, p.E * p.F, p.d, brows);
     if (p.S > 0) {
       ok = ok && make_map(&maps[1], x, p.N, p.d, BM) && make_map(&maps[4], w->ws1, p.S * p.Fs, p.d, brows);
       if (p.swiglu) ok = ok && make_map(&maps[5], w->ws3, p.S * p.Fs, p.d, brows);
     }
-    ok = ok && make_out_map(&maps[6], h, R, p.F);
+    if (families & kRoutedFamily) ok = ok && make_out_map(&maps[6], h, R, p.F);
     if (p.S > 0) ok = ok && make_out_map(&maps[7], hs, p.N, p.S * p.Fs);
     if (!ok) return cudaErrorInvalidValue;
     Params P{};
@@ -1440,11 +1445,6 @@ cudaError_t launch_ffn_bf16(const Plan& p, const void* xp, const int32_t* expert
     f0.bias_nsum = p.bias ? 1 : 0;
     f0.gather_rows = gather_rows;
     f0.gather_n = (int32_t)p.N;
-    if (p.fp8w) {
-      f0.b_scale = w->w1_scale;
-      f0.b3_scale = w->w3_scale;
-      f0.scale_ld = p.d / 32;
-    }
     if (p.S > 0) {
       Family& f1 = P.fam[1];
       f1.groups = (int32_t)p.S;
@@ -1467,43 +1467,29 @@ cudaError_t launch_ffn_bf16(const Plan& p, const void* xp, const int32_t* expert
     P.wait_ns = wait_limit_ns();
     if (!(families & kRoutedFamily)) f0.groups = 0;
     if (!(families & kSharedFamily)) P.fam[1].groups = 0;
-    // MXFP8 routed weights: the routed tiles run in the converting form, the shared
-    // experts (bf16) in a launch of their own
-    auto launch_up = [&](const Params& Pl, bool fp8) -> cudaError_t {
-      const int64_t max_tiles = (Pl.fam[0].groups ? (R / (fp8 ? fp8r : BM) + p.E) * Pl.fam[0].n_tiles : 0) +
-                                (Pl.fam[1].groups ? p.S * ceil_div(p.N, BM) * Pl.fam[1].n_tiles : 0);
-      if (max_tiles == 0) return cudaSuccess;
-      if (fp8)
-        return p.swiglu ? launch_fp8<kSwiglu>(bn, fp8r, maps, Pl, max_tiles, st, grid_cap)
-                        : launch_fp8<kGelu>(bn, fp8r, maps, Pl, max_tiles, st, grid_cap);
-      return p.swiglu ? launch_bn<kSwiglu>(bn, maps, Pl, max_tiles, st, grid_cap)
-                      : launch_bn<kGelu>(bn, maps, Pl, max_tiles, st, grid_cap);
-    };
-    cudaError_t err;
-    if (p.fp8w) {
-      Params Pr = P, Ps = P;
-      Pr.fam[1].groups = 0;
-      Ps.fam[0].groups = 0;
-      err = launch_up(Pr, true);
-      if (err == cudaSuccess) err = launch_up(Ps, false);
-    } else {
-      err = launch_up(P, false);
+    const int64_t max_tiles = (f0.groups ? (R / BM + p.E) * f0.n_tiles : 0) +
+                              (P.fam[1].groups ? p.S * ceil_div(p.N, BM) * P.fam[1].n_tiles : 0);
+    if (max_tiles > 0) {
+      const cudaError_t err = p.swiglu ? launch_bn<kSwiglu>(bn, maps, P, max_tiles, st, grid_cap)
+                                       : launch_bn<kGelu>(bn, maps, P, max_tiles, st, grid_cap);
+      if (err != cudaSuccess) return err;
     }
-    if (err != cudaSuccess) return err;
   }
   if (part & 2) {
     const int bn = pick_bn(false, p.d, 0);
     if (!bn) return cudaErrorInvalidValue;
-    const bool pair = !p.fp8w && use_pair_tiles(p, bn);
+    const bool pair = use_pair_tiles(p, bn);
     const int brows = pair ? bn / 2 : bn;
     CUtensorMap maps[8];
-    if (!make_map(&maps[0], h, R, p.F, a_rows)) return cudaErrorInvalidValue;
+    // (a launch of the shared experts alone never reads the routed maps: any valid map)
+    const bool routed = (families & kRoutedFamily) != 0;
+    if (!(routed ? make_map(&maps[0], h, R, p.F, BM) : make_map(&maps[0], hs, p.N, p.S * p.Fs, BM)))
+      return cudaErrorInvalidValue;
     for (int i = 1; i < 8; ++i) maps[i] = maps[0];
-    bool ok = p.fp8w ? make_fp8_map(&maps[2], w->w2, p.E * p.d, p.F, brows)
-                     : make_map(&maps[2], w->w2, p.E * p.d, p.F, brows);
+    bool ok = routed ? make_map(&maps[2], w->w2, p.E * p.d, p.F, brows) : true;
     if (p.S > 0)
       ok = ok && make_map(&maps[1], hs, p.N, p.S * p.Fs, BM) && make_map(&maps[3], w->ws2, p.S * p.d, p.Fs, brows);
-    ok = ok && make_out_map_f32(&maps[6], yp, R, p.d);
+    if (routed) ok = ok && make_out_map_f32(&maps[6], yp, R, p.d);
     if (p.S > 0) ok = ok && make_out_map_f32(&maps[7], ys, p.N, p.d);
     if (!ok) return cudaErrorInvalidValue;
     Params P{};
@@ -1524,10 +1510,6 @@ cudaError_t launch_ffn_bf16(const Plan& p, const void* xp, const int32_t* expert
     f0.bias_group = p.d;
     f0.bias_nsum = p.bias ? 1 : 0;
     f0.row_gate = row_gate;
-    if (p.fp8w) {
-      f0.b_scale = w->w2_scale;
-      f0.scale_ld = p.F / 32;
-    }
     if (p.S > 0) {
       Family& f1 = P.fam[1];
       f1.groups = 1;
@@ -1548,26 +1530,17 @@ cudaError_t launch_ffn_bf16(const Plan& p, const void* xp, const int32_t* expert
     P.expert_off = expert_off;
     P.status = status;
     P.wait_ns = pair ? kTimeoutNs : wait_limit_ns();  // the pair form keeps the full bound
-    if (!(families & kRoutedFamily)) f0.groups = 0;
+    if (!routed) f0.groups = 0;
     if (!(families & kSharedFamily)) P.fam[1].groups = 0;
-    cudaError_t err;
-    auto tiles_of = [&](const Params& Pl) {
-      return (Pl.fam[0].groups ? (R / BM + p.E) * Pl.fam[0].n_tiles : 0) +
-             (Pl.fam[1].groups ? ceil_div(p.N, BM) * Pl.fam[1].n_tiles : 0);
-    };
+    cudaError_t err = cudaSuccess;
     if (pair) {
       const int64_t max_pairs = (f0.groups ? (R / (2 * BM) + p.E) * f0.n_tiles : 0) +
                                 (P.fam[1].groups ? ceil_div(p.N, 2 * BM) * P.fam[1].n_tiles : 0);
-      err = launch_pair_t<256, kLinear>(maps, P, max_pairs, st, grid_cap);
-    } else if (p.fp8w) {
-      Params Pr = P, Ps = P;
-      Pr.fam[1].groups = 0;
-      Ps.fam[0].groups = 0;
-      const int64_t tr = Pr.fam[0].groups ? (R / fp8r + p.E) * Pr.fam[0].n_tiles : 0;
-      err = tr ? launch_fp8<kLinear>(bn, fp8r, maps, Pr, tr, st, grid_cap) : cudaSuccess;
-      if (err == cudaSuccess && tiles_of(Ps)) err = launch_bn<kLinear>(bn, maps, Ps, tiles_of(Ps), st, grid_cap);
+      if (max_pairs > 0) err = launch_pair_t<256, kLinear>(maps, P, max_pairs, st, grid_cap);
     } else {
-      err = launch_bn<kLinear>(bn, maps, P, tiles_of(P), st, grid_cap);
+      const int64_t tiles = (f0.groups ? (R / BM + p.E) * f0.n_tiles : 0) +
+                            (P.fam[1].groups ? ceil_div(p.N, BM) * P.fam[1].n_tiles : 0);
+      if (tiles > 0) err = launch_bn<kLinear>(bn, maps, P, tiles, st, grid_cap);
     }
     if (err != cudaSuccess) return err;
   }

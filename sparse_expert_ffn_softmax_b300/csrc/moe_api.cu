@@ -49,7 +49,7 @@ moe_status make_plan(const moe_config* c, Plan* p) {
   p->bf16 = c->dtype == MOE_DT_BF16;
   p->gather = p->bf16 && (c->flags & MOE_FLAG_GATHER_ROWS) != 0;
   p->fp8w = c->weight_format == MOE_WEIGHTS_MXFP8;
-  if (p->fp8w && (!p->bf16 || p->d % 512 || p->F % 512)) return MOE_ERR_UNSUPPORTED;
+  if (p->fp8w && (!p->bf16 || p->gather || p->d % 512 || p->F % 512)) return MOE_ERR_UNSUPPORTED;
   p->swiglu = c->act == MOE_ACT_SWIGLU;
   p->ec = c->gating == MOE_GATE_EXPERT_CHOICE;
   p->bias = c->has_bias != 0;

@@ -27,8 +27,11 @@
 // the first ties in token order, and lists them in ascending token order; a
 // bitmap of (token, expert) then gives each token its rows in ascending expert
 // order (a CSR: tok_off / tok_rows) for the copy and the combine.
+#include <type_traits>
+
 #include "common.cuh"
 #include "internal.h"
+#include "mx.cuh"
 #include "offsets.cuh"
 #include "stats.cuh"
 
@@ -119,16 +122,35 @@ __global__ void shard_base_kernel(const int32_t* __restrict__ shard_counts, int3
 // Otherwise tile_base [E][T+1] and expert_off come from scan_offsets_kernel.
 // rank_base (token-sharded batch, else null): assignments to each expert in earlier
 // shards; (t, j) is kept when rank_base[e] + its rank in this shard < C.
+// MXFP8 rows (bf16 layers whose routed experts compute in MXFP8): a lane's 16-byte
+// chunk is 8 values of the row and lanes 4q .. 4q + 3 hold one 32-value MX block (the
+// chunks a warp covers start at a multiple of 4). Returns the lane's 8 E4M3 codes and,
+// in sb, the block's E8M0 scale byte. Every lane of the warp takes part.
+__device__ __forceinline__ uint2 mx_chunk(uint4 v, uint32_t& sb) {
+  float f[8];
+  Vec16<__nv_bfloat16>::unpack(v, f);
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+  amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));
+  amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 2));
+  sb = mx::scale_byte(amax);
+  const float inv = mx::inv_scale(sb);
+  return make_uint2(mx::e4m3x4(f[0] * inv, f[1] * inv, f[2] * inv, f[3] * inv),
+                    mx::e4m3x4(f[4] * inv, f[5] * inv, f[6] * inv, f[7] * inv));
+}
+
 template <typename DT, bool kFused>
 __global__ void __launch_bounds__(kWarps * 32) scatter_kernel(
     const DT* __restrict__ x, const int32_t* __restrict__ idx, const float* __restrict__ gate,
     const int32_t* __restrict__ counts_or_base, int32_t* __restrict__ expert_off, int64_t N, int64_t d, int64_t k,
     int64_t E, int64_t T, int64_t TT, int64_t cap, DT* __restrict__ xp, int32_t* __restrict__ tok_rows,
     int32_t* __restrict__ row_token, float* __restrict__ row_gate, void* stats, int32_t* status,
-    RouterStatsArgs rs, const int32_t* __restrict__ rank_base) {
+    RouterStatsArgs rs, const int32_t* __restrict__ rank_base, uint8_t* __restrict__ xs) {
   // blockIdx.y selects a slice of the row's 16-byte chunks: small batches copy
   // their rows with more blocks. Every slice ranks the tile (cheap); slice 0
-  // writes the row metadata.
+  // writes the row metadata. xs non-null (bf16, MXFP8 experts): xp receives the rows'
+  // E4M3 codes [rows, d] and xs their E8M0 scales [rows, d / 32].
   const bool meta = blockIdx.y == 0;
   extern __shared__ uint32_t s_dyn[];
   pdl_wait();
@@ -247,8 +269,35 @@ __global__ void __launch_bounds__(kWarps * 32) scatter_kernel(
   __syncthreads();
   if (xp == nullptr) return;  // metadata only: the up-projection gathers the rows from x
   const int64_t nchunk = d / VT::n;
-  const int64_t cs = ceil_div(nchunk, (int64_t)gridDim.y);
+  int64_t cs = ceil_div(nchunk, (int64_t)gridDim.y);
+  if (xs) cs = (cs + 3) & ~(int64_t)3;  // slices of whole MX blocks
   const int64_t cbeg = (int64_t)blockIdx.y * cs, cend = cbeg + cs < nchunk ? cbeg + cs : nchunk;
+  if constexpr (std::is_same<DT, __nv_bfloat16>::value) {
+    if (xs) {
+      uint8_t* xq = reinterpret_cast<uint8_t*>(xp);
+      for (int tt = warp; tt < TT; tt += kWarps) {
+        const int64_t tok = tile * TT + tt;
+        if (tok >= N) break;
+        const int32_t my_row = lane < k ? s_rows[tt * k + lane] : -1;
+        const uint4* src = reinterpret_cast<const uint4*>(x) + tok * nchunk;
+        for (int64_t c0 = cbeg; c0 < cend; c0 += 32) {
+          const int64_t c = c0 + lane;
+          const bool act = c < cend;
+          const uint4 v = act ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+          uint32_t sb;
+          const uint2 q = mx_chunk(v, sb);
+          for (int j = 0; j < k; ++j) {
+            const int32_t row = __shfl_sync(kFull, my_row, j);
+            if (act && row >= 0) {
+              *reinterpret_cast<uint2*>(xq + (int64_t)row * d + c * 8) = q;
+              if ((c & 3) == 0) xs[(int64_t)row * (d / 32) + (c >> 2)] = (uint8_t)sb;
+            }
+          }
+        }
+      }
+      return;
+    }
+  }
   for (int tt = warp; tt < TT; tt += kWarps) {
     const int64_t tok = tile * TT + tt;
     if (tok >= N) break;
@@ -406,13 +455,32 @@ template <typename T>
 __global__ void __launch_bounds__(kWarps * 32) copy_rows_csr_kernel(const T* __restrict__ x,
                                                                     const int32_t* __restrict__ tok_rows,
                                                                     const int32_t* __restrict__ tok_off, int64_t N,
-                                                                    int64_t d, T* __restrict__ xp) {
+                                                                    int64_t d, T* __restrict__ xp,
+                                                                    uint8_t* __restrict__ xs) {
   using VT = Vec16<T>;
   const int lane = threadIdx.x & 31;
   const int64_t nchunk = d / VT::n;
   for (int64_t t = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5); t < N; t += (int64_t)gridDim.x * kWarps) {
     const int32_t beg = tok_off[t], n = tok_off[t + 1] - beg;
     const uint4* src = reinterpret_cast<const uint4*>(x) + t * nchunk;
+    if constexpr (std::is_same<T, __nv_bfloat16>::value) {
+      if (xs) {  // MXFP8 rows: codes into xp, scales into xs (see scatter_kernel)
+        uint8_t* xq = reinterpret_cast<uint8_t*>(xp);
+        for (int64_t c0 = 0; c0 < nchunk; c0 += 32) {
+          const int64_t c = c0 + lane;
+          const bool act = c < nchunk;
+          const uint4 v = act ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+          uint32_t sb;
+          const uint2 q = mx_chunk(v, sb);
+          for (int i = 0; act && i < n; ++i) {
+            const int64_t row = tok_rows[beg + i];
+            *reinterpret_cast<uint2*>(xq + row * d + c * 8) = q;
+            if ((c & 3) == 0) xs[row * (d / 32) + (c >> 2)] = (uint8_t)sb;
+          }
+        }
+        continue;
+      }
+    }
     for (int64_t c = lane; c < nchunk; c += 32) {
       const uint4 v = __ldg(src + c);
       for (int i = 0; i < n; ++i) reinterpret_cast<uint4*>(xp)[(int64_t)tok_rows[beg + i] * nchunk + c] = v;
@@ -517,6 +585,8 @@ cudaError_t launch_permute_t(const Plan& p, const void* x, const int32_t* idx, c
                              const int32_t* shard_counts, int32_t n_shards, int32_t shard_rank) {
   int32_t* status = status_ptr(p, ws);
   int32_t* rank_base = nullptr;
+  // MXFP8 experts: the rows go out quantised, scales after the codes (mx::scale_offset)
+  uint8_t* xs = p.fp8w && xp ? static_cast<uint8_t*>(xp) + mx::scale_offset(p.max_rows, p.d) : nullptr;
   if (shard_counts) {
     if (p.ec || mode != kCountsFromIdx) return cudaErrorInvalidValue;
     rank_base = ws_at<int32_t>(ws, p.rank_base);
@@ -537,7 +607,7 @@ cudaError_t launch_permute_t(const Plan& p, const void* x, const int32_t* idx, c
     if (xp) {
       const int64_t blocks = ceil_div(p.N, kWarps) < 148 * 16 ? ceil_div(p.N, kWarps) : 148 * 16;
       copy_rows_csr_kernel<T><<<(unsigned)blocks, kWarps * 32, 0, st>>>(static_cast<const T*>(x), tok_rows, tok_off,
-                                                                        p.N, p.d, static_cast<T*>(xp));
+                                                                        p.N, p.d, static_cast<T*>(xp), xs);
     }
     return cudaGetLastError();
   }
@@ -557,7 +627,7 @@ cudaError_t launch_permute_t(const Plan& p, const void* x, const int32_t* idx, c
     return launch_pdl(scatter_kernel<T, true>, dim3((unsigned)p.tiles + 1, (unsigned)slices), dim3(kWarps * 32),
                       sc_smem, st, static_cast<const T*>(x), idx, gate, (const int32_t*)tile_counts, expert_off, p.N,
                       p.d, p.k, p.E, (int64_t)p.tiles, p.tile, p.cap, static_cast<T*>(xp), tok_rows, row_token,
-                      row_gate, stats, status, fin, (const int32_t*)nullptr);
+                      row_gate, stats, status, fin, (const int32_t*)nullptr, xs);
   }
   if (mode == kCountsFromIdx) {
     const size_t hist_smem = (size_t)kWarps * p.E * 4;
@@ -579,7 +649,7 @@ cudaError_t launch_permute_t(const Plan& p, const void* x, const int32_t* idx, c
   const size_t sc_smem = (size_t)p.E * 4 + (size_t)kMaxTileTokens * p.k * 4;
   scatter_kernel<T, false><<<dim3((unsigned)p.tiles, (unsigned)slices), kWarps * 32, sc_smem, st>>>(
       static_cast<const T*>(x), idx, gate, tile_base, expert_off, p.N, p.d, p.k, p.E, p.tiles, p.tile, p.cap,
-      static_cast<T*>(xp), tok_rows, row_token, row_gate, stats, status, RouterStatsArgs{}, rank_base);
+      static_cast<T*>(xp), tok_rows, row_token, row_gate, stats, status, RouterStatsArgs{}, rank_base, xs);
   return cudaGetLastError();
 }
 

@@ -6,7 +6,9 @@ routing, the GPU's own fp32 logits / probabilities) and compares:
 
 * routing (top-k ids, ranks, drops, row numbering, expert offsets, counts): bit-exact
 * gates, probabilities and statistics: relative 1e-5
-* permuted rows: bit-exact copies of the token rows
+* permuted rows: bit-exact copies of the token rows (MXFP8 layers: their codes and
+  scales equal the oracle's quantisation of the token rows; H blocks obey the
+  block rule)
 * outputs: fp32 layers |y - y_ref| <= 1e-4 (|y_ref| + rms(y_ref)) per element;
   bf16 layers max |y - y_ref| <= 2e-2 rms(y_ref) (``raw_bar``, the workload
   shapes). The small coverage layers have heavy-tailed outputs (max |y_ref| up to
@@ -64,6 +66,7 @@ def run_gpu(w, tensors=None, layer=None, repeat=1):
     R = lay.max_rows
     dt = w.torch_dtype
     v = layer.view
+    mx = getattr(w, "expert_weights", "bf16") == "mxfp8"
     res = dict(
         out=out.detach().cpu(),
         logits=v("logits", (N, E), torch.float32).cpu().numpy(),
@@ -75,8 +78,12 @@ def run_gpu(w, tensors=None, layer=None, repeat=1):
         expert_off=v("expert_off", (E + 1,), torch.int32).cpu().numpy(),
         row_token=v("row_token", (R,), torch.int32).cpu().numpy(),
         row_gate=v("row_gate", (R,), torch.float32).cpu().numpy(),
-        # bf16 layers gather the up-projection's rows from x (no xp copy in the workspace)
-        xp=v("xp", (R, d), dt).cpu() if lay.h - lay.xp >= R * d * (2 if dt == torch.bfloat16 else 4) else None,
+        # bf16 layers gather the up-projection's rows from x (no xp copy in the workspace);
+        # MXFP8 layers hold the rows' E4M3 codes and E8M0 scales there (mx below)
+        xp=v("xp", (R, d), dt).cpu()
+        if not mx and lay.h - lay.xp >= R * d * (2 if dt == torch.bfloat16 else 4) else None,
+        mx=tuple(a.cpu() for a in moe.mx_views(layer.cfg, layer.ws, "xp") + moe.mx_views(layer.cfg, layer.ws, "h"))
+        if mx else None,
         stats=layer.read_stats(),
         capacity=C,
         # gate-scaled expert rows (fp32 [R, d]) and the shared experts' sum (fp32 [N, d])
@@ -382,6 +389,31 @@ def check_big_layer(w, t, res, r, tokens):
     return ref, report
 
 
+def check_mx_rows(t, mx, row_token, rows_valid, max_rows_checked=4096):
+    """MXFP8 layers: the permuted rows' codes and scales equal the oracle's MXFP8
+    quantisation of their token rows (bit for bit: both quantise the same bf16
+    values); the hidden rows H obey the block rule: each block's largest code lies in
+    [256, 448] (a scale byte 0 block may hold less: its values are below 2^-119) and
+    no code is NaN."""
+    from oracle import e4m3_value
+    o = oracle()
+    xq, xs, hq, hs = mx
+    n = min(rows_valid, max_rows_checked)
+    rows = np.unique(np.concatenate([np.arange(min(n, rows_valid)),
+                                     np.arange(max(0, rows_valid - 64), rows_valid)])).astype(np.int64)
+    x = t["x"][torch.as_tensor(row_token[rows], device=t["x"].device, dtype=torch.long)]
+    codes, scales = o.mx_quantize(x.float().cpu().numpy().astype(np.float64))
+    got_c, got_s = xq[torch.as_tensor(rows)].numpy(), xs[torch.as_tensor(rows)].numpy()
+    assert np.array_equal(got_s, scales), f"xp scale bytes differ in {np.count_nonzero(got_s != scales)} blocks"
+    assert np.array_equal(got_c, codes), f"xp codes differ in {np.count_nonzero(got_c != codes)} elements"
+    h = e4m3_value(hq[torch.as_tensor(rows)].numpy())
+    assert not np.any(np.isnan(h)), "NaN code in H"
+    hb = np.abs(h).reshape(len(rows), -1, 32).max(axis=2)
+    sc = hs[torch.as_tensor(rows)].numpy()
+    assert np.all(((hb >= 256) & (hb <= 448)) | (sc == 0)), "H block without a code in [256, 448]"
+    return {"mx_rows_checked": int(len(rows))}
+
+
 def check(w, t, res, n_sample=None, check_self_routed=True, raw_bar=False):
     o = oracle()
     N, E, k, d = w.n_tokens, w.n_experts, w.top_k, w.d_model
@@ -437,6 +469,8 @@ def check(w, t, res, n_sample=None, check_self_routed=True, raw_bar=False):
     if res["xp"] is not None:
         x = t["x"].detach().cpu()
         assert torch.equal(res["xp"][:rows_valid], x[torch.as_tensor(ref_row_token, dtype=torch.long)])
+    if res.get("mx") is not None:
+        report.update(check_mx_rows(t, res["mx"], ref_row_token, rows_valid))
     # ---- statistics ---------------------------------------------------------
     ost = r["stats"]
     np.testing.assert_allclose(st["f"].numpy(), ost["f"], rtol=1e-5, atol=1e-7)

@@ -57,7 +57,7 @@ def test_workspace_layout(name):
     b = 4 if w.dtype == "f32" else 2
     assert lay.h - lay.xp >= lay.max_rows * w.d_model * b
     assert lay.hs - lay.h >= lay.max_rows * w.d_ff * b
-    if w.dtype == "bf16":  # gathering the up-projection's rows from x: no xp region
+    if w.dtype == "bf16" and w.expert_weights == "bf16":  # gathering the rows from x: no xp region
         lay_g = moe.workspace_layout(moe.config(w, flags=moe.FLAG_GATHER_ROWS))
         assert lay_g.h - lay_g.xp == 256
         assert lay.total_bytes - lay_g.total_bytes >= lay.max_rows * w.d_model * b - 256
@@ -132,3 +132,21 @@ def test_host_side_argument_errors():
     # pass-through needs the layer input in the combine
     cfg_p = moe.config(WORKLOADS["tiny_f32"], flags=moe.FLAG_DROP_PASSTHROUGH)
     assert lib.moe_combine(ctypes.byref(cfg_p), fake, fake, None, None, None, fake, None) == 1
+
+
+def test_mxfp8_layer_validation():
+    """MXFP8 experts: bf16 layers with d, F multiples of 512, without row gathering;
+    xp and h hold codes, then scales from the next 256-byte boundary, inside the
+    regions a bf16 layer reserves."""
+    w = WORKLOADS["mixtral_decode_fp8"]
+    cfg = moe.config(w)
+    lay = moe.workspace_layout(cfg)
+    R = lay.max_rows
+    assert lay.h - lay.xp >= (R * w.d_model + 255) // 256 * 256 + R * w.d_model // 32
+    assert lay.hs - lay.h >= (R * w.d_ff + 255) // 256 * 256 + R * w.d_ff // 32
+    with pytest.raises(moe.MoEError) as e:
+        moe.workspace_size(moe.config(w, flags=moe.FLAG_GATHER_ROWS))
+    assert e.value.code == 2
+    with pytest.raises(moe.MoEError) as e:
+        moe.workspace_size(moe.config(w, d_ff=w.d_ff + 256))
+    assert e.value.code == 2

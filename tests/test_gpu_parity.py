@@ -249,8 +249,9 @@ def test_forward_overlap_matches_forward(name, caps):
     torch.cuda.empty_cache()
 
 
-# MXFP8 routed expert weights (FP8 E4M3 codes, one E8M0 scale per 32 along K; d, F
-# multiples of 512): the oracle computes with the exact dequantised weights
+# MXFP8 routed experts (FP8 E4M3 codes, one E8M0 scale per 32 along K; d, F multiples
+# of 512): the oracle computes with the exact dequantised weights and rounds each
+# routed expert's input and hidden rows to MXFP8 by the same block rule
 FP8W = [
     wl("fp8w_swiglu_shared", n_tokens=600, d_model=512, d_ff=1024, n_experts=8, top_k=2, capacity_factor=1.25,
        act="swiglu", n_shared=1, d_ff_shared=256, expert_weights="mxfp8"),
@@ -258,8 +259,11 @@ FP8W = [
        gating="expert_choice", has_bias=True, expert_weights="mxfp8"),
     wl("fp8w_decode_many", n_tokens=40, d_model=1024, d_ff=512, n_experts=64, top_k=6, capacity_factor=0.0,
        act="swiglu", logit_bias_max=1.0, expert_weights="mxfp8"),
-    wl("fp8w_gather_drops", n_tokens=900, d_model=512, d_ff=512, n_experts=8, top_k=2, capacity_factor=0.6,
-       act="swiglu", logit_bias_max=2.0, expert_weights="mxfp8", gather_rows=True),
+    wl("fp8w_drops_passthrough", n_tokens=900, d_model=512, d_ff=512, n_experts=8, top_k=2, capacity_factor=0.6,
+       act="swiglu", logit_bias_max=2.0, expert_weights="mxfp8", drop_passthrough=True),
+    wl("fp8w_ragged_32row_tiles", n_tokens=70, d_model=1536, d_ff=1024, n_experts=12, top_k=3,
+       capacity_factor=0.0, gating="topk_softmax", act="gelu", has_bias=True, n_shared=1, d_ff_shared=512,
+       expert_weights="mxfp8"),
 ]
 
 
