@@ -431,32 +431,43 @@ __device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
 // PAIR: the tile is 256 x BN on a CTA pair; each CTA stages its 128 rows of A and
 // half (BN / 2 rows) of B.
 // MXR > 0, the MXFP8 form (tcgen05 kind::mxf8f6f4 with E8M0 block scales): A and B
-// arrive as E4M3 codes, 128 per row and stage (one 128-byte swizzle atom, as 64 bf16
-// are), and each stage's scale bytes go to a third ring of 32 x 16-byte atoms that
-// tcgen05.cp moves into tensor memory beside the accumulators. A tile covers MXR rows
-// of A (32 for decode batches: a 4 KB box; the M = 128 MMA reads the 16 KB after the
-// slot's start, whose extra rows are never stored).
+// arrive as E4M3 codes in 128-byte K atoms (128 codes of a row, one swizzle atom, as
+// 64 bf16 are), and each stage's scale bytes go to a third ring of 32 x 16-byte atoms
+// that tcgen05.cp moves into tensor memory beside the accumulators. A tile covers MXR
+// rows of A. MXR = 32 (decode batches: the weight stream is the work) takes two K atoms
+// per stage, 32 KB of weights, since a stage's fixed costs (barriers, scale copies)
+// otherwise bound the stream (measured: 16 KB stages stream at about half the HBM
+// rate of 32 KB ones); its A atoms are 4 KB boxes, and the M = 128 MMA reads the 16 KB
+// after an atom's start, whose extra rows are never stored.
+constexpr int mx_atoms(int mxr) { return mxr == 32 ? 2 : 1; }
+
 template <int BN, bool PAIR = false, int MXR = 0>
 struct Cfg {
   static constexpr bool kMx = MXR != 0;
   static constexpr int kTileRows = kMx ? MXR : BM;  // A rows of a tile
-  static constexpr int kStageK = kMx ? 128 : BK;    // K elements per stage (128 bytes of a row)
-  static constexpr int kStagingBytes = 2048;        // per epilogue warp: 32 rows x 64 B
-  static constexpr int kABytes = kTileRows * 128;
-  static constexpr int kBBytes = (PAIR ? BN / 2 : BN) * 128;
-  static constexpr int kSFBytes = kMx ? 512 * (1 + BN / 128) : 0;  // the A atom, then B's
-  static constexpr int kTxBytes = kABytes + kBBytes;                // TMA bytes per stage
+  static constexpr int kAtoms = kMx ? mx_atoms(MXR) : 1;  // 128-byte K atoms per stage
+  static constexpr int kStageK = kMx ? 128 * kAtoms : BK;  // K elements per stage
+  static constexpr int kStagingBytes = 2048;               // per epilogue warp: 32 rows x 64 B
+  static constexpr int kAAtomBytes = kTileRows * 128;
+  static constexpr int kBAtomBytes = (PAIR ? BN / 2 : BN) * 128;
+  static constexpr int kABytes = kAtoms * kAAtomBytes;
+  static constexpr int kBBytes = kAtoms * kBAtomBytes;
+  static constexpr int kSFAtomBytes = kMx ? 512 * (1 + BN / 128) : 0;  // per K atom: A's scale atom, then B's
+  static constexpr int kSFBytes = kAtoms * kSFAtomBytes;
+  static constexpr int kTxBytes = kABytes + kBBytes;  // TMA bytes per stage
   static constexpr int kStageBytes = kTxBytes + kSFBytes;
   static constexpr int kStages = (192 * 1024) / kStageBytes > 8 ? 8 : (192 * 1024) / kStageBytes;
   static constexpr int kRingBytes = kStages * kStageBytes;  // A slots, B slots, scale atoms
-  static constexpr int kSFCols = 4 + 4 * (BN / 128);         // tensor-memory columns of a stage's scales
-  static constexpr int kTmemCols = kMx ? 512 : 2 * BN;       // two accumulators (+ the scale ring)
+  static constexpr int kSFAtomCols = 4 + 4 * (BN / 128);     // tensor-memory columns of one K atom's scales
+  static constexpr int kSFCols = kAtoms * kSFAtomCols;
+  static constexpr int kTmemCols = kMx ? 512 : 2 * BN;  // two accumulators (+ the scale ring)
   static constexpr size_t kSmem = (size_t)kRingBytes + (size_t)kEpiWarps * kStagingBytes + 1024;
   static_assert(!kMx || (!PAIR && BN == 128), "MXFP8 tiles: single CTAs, 128 columns");
   static_assert(!kMx || 2 * BN + kStages * kSFCols <= 512, "accumulators and scales fit tensor memory");
-  // the M = 128 MMA reads 16 KB of A from a slot's start: past a short slot come later
-  // A slots, then the B slots and the scale atoms, all shared memory of this block
-  static_assert((kStages - 1) * kABytes + BM * 128 <= kRingBytes, "A overhang");
+  static_assert(kStages >= 3, "pipeline depth");
+  // the M = 128 MMA reads 16 KB of A from an atom's start: past a short atom come later
+  // atoms and slots, then the B slots and the scale atoms, all shared memory of this block
+  static_assert((kStages - 1) * kABytes + (kAtoms - 1) * kAAtomBytes + BM * 128 <= kRingBytes, "A overhang");
 };
 
 struct TileInfo {
@@ -545,6 +556,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr uint32_t kIdesc = idesc_bf16(PAIR ? 2 * BM : BM, BN);
   // half tiles (N = BN / 2) for the last wave: bf16, one-B-map, whole-width epilogues only
   constexpr bool kCanSplit = !PAIR && !kMx && (EPI == kGelu || EPI == kLinear);
+  // MXFP8 decode tiles (32 A rows): warp 2, whose TMEM lane quadrant holds no rows of
+  // such a tile, copies the scale bytes, so the TMA producer only issues tensor copies
+  constexpr bool kScaleWarp = kMx && kTR == 32;
+  constexpr int kDrainWarps = kEpiWarps - (kScaleWarp ? 1 : 0);
   constexpr uint32_t kIdescHalf = idesc_bf16(BM, BN / 2);
 
   extern __shared__ uint8_t smem_raw[];
@@ -577,7 +592,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull_bar[a], 1);
-      mbar_init(&tempty_bar[a], PAIR ? 2 * kEpiWarps : kEpiWarps);
+      mbar_init(&tempty_bar[a], PAIR ? 2 * kEpiWarps : kDrainWarps);
     }
     mbar_init(&done_bar, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -637,16 +652,46 @@ __global__ void __launch_bounds__(kThreads, 1)
     return;
   }
   volatile int32_t* abort_flag = &s_abort;
+  // MXFP8 form: the 32 lanes of the calling warp copy stage `stage`'s scale bytes (4 per
+  // row and K atom: its four 32-element blocks) into the tensor-memory copy layout, row r
+  // of a 128-row atom at byte 16 (r % 32) + 4 (r / 32), then each lane adds one arrival
+  // on the stage's barrier once its copies have landed.
+  auto mx_scale_copies = [&](const TileInfo& ti, const Family& F, int kb, int stage) {
+#pragma unroll
+    for (int a = 0; a < C::kAtoms; ++a) {
+      uint8_t* sf = sSF + stage * C::kSFBytes + a * C::kSFAtomBytes;
+      const int sc = 4 * (kb * C::kAtoms + a);  // the atom's 4 scale bytes in a row's scales
+#pragma unroll
+      for (int j = 0; j < kTR / 32; ++j) {  // A rows past the matrix read nothing (zeros)
+        const int row = ti.a_row0 + lane + 32 * j;
+        const bool in = row < F.a_rows;
+        cp_async4(sf + 16 * lane + 4 * j, F.a_scale + (int64_t)(in ? row : 0) * F.a_scale_ld + sc, in);
+      }
+#pragma unroll
+      for (int j = 0; j < BN / 32; ++j) {  // B rows: W1 then W3 halves (SwiGLU), else BN rows
+        const int n = lane + 32 * j;
+        const uint8_t* src;
+        if (EPI == kSwiglu) {
+          const bool up = n >= BN / 2;
+          const int64_t brow =
+              (int64_t)ti.g * F.b_rows_group + (int64_t)ti.nt * (BN / 2) + (up ? n - BN / 2 : n);
+          src = (up ? F.b3_scale : F.b_scale) + brow * F.scale_ld;
+        } else {
+          src = F.b_scale + ((int64_t)ti.g * F.b_rows_group + (int64_t)ti.nt * BN + n) * F.scale_ld;
+        }
+        cp_async4(sf + 512 * (1 + (j >> 2)) + 16 * lane + 4 * (j & 3), src + sc, true);
+      }
+    }
+    cp_async_arrive_noinc(&full_bar[stage]);
+  };
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
     // Lane 0 waits for free stages and issues the copies; for a gathering family the
     // 32 lanes issue one tile::gather4 each (4 of the tile's 128 A rows, row ids held in
     // registers for the tile), after lane 0 has set the stage's expected bytes. MXFP8
-    // form: the 32 lanes also copy the stage's scale bytes (cp.async, 4 bytes = one
-    // row's four 32-element blocks) into the tensor-memory copy layout, row r of a
-    // 128-row atom at byte 16 (r % 32) + 4 (r / 32), each lane then adding one arrival
-    // on the stage's barrier when its copies have landed.
+    // form: the 32 lanes also copy the stage's scale bytes (mx_scale_copies), or the
+    // scale warp does (decode tiles).
     int stage = 0;
     uint32_t phase = 0;
     int32_t last_parity[kStages];
@@ -704,41 +749,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             // copies per stage measured slower than the bytes they save)
             mbar_arrive_expect_tx(&full_bar[stage], C::kTxBytes);
             last_parity[stage] = (int32_t)phase;
-            if (!gather) tma_load_2d(ma, &full_bar[stage], sA + stage * C::kABytes, (k0 + kb) * kKE, ti.a_row0);
-            if (EPI == kSwiglu) {
-              const int by = ti.g * F.b_rows_group + kseg * F.b_rows_kseg + ti.nt * (BN / 2);
-              tma_load_2d(mb, &full_bar[stage], sB + stage * C::kBBytes, kin * kKE, by);
-              tma_load_2d(mb3, &full_bar[stage], sB + stage * C::kBBytes + (BN / 2) * 128, kin * kKE, by);
-            } else {
-              const int by = ti.g * F.b_rows_group + kseg * F.b_rows_kseg + ti.nt * BN;
-              tma_load_2d(mb, &full_bar[stage], sB + stage * C::kBBytes, kin * kKE, by);
+#pragma unroll
+            for (int a = 0; a < C::kAtoms; ++a) {  // K atom a of the stage (MXFP8: codes [kKE kb + 128 a, + 128))
+              const int ka = (k0 + kb) * kKE + 128 * a, kba = kin * kKE + 128 * a;
+              uint8_t* a_dst = sA + stage * C::kABytes + a * C::kAAtomBytes;
+              uint8_t* b_dst = sB + stage * C::kBBytes + a * C::kBAtomBytes;
+              if (!gather) tma_load_2d(ma, &full_bar[stage], a_dst, ka, ti.a_row0);
+              if (EPI == kSwiglu) {
+                const int by = ti.g * F.b_rows_group + kseg * F.b_rows_kseg + ti.nt * (BN / 2);
+                tma_load_2d(mb, &full_bar[stage], b_dst, kba, by);
+                tma_load_2d(mb3, &full_bar[stage], b_dst + (BN / 2) * 128, kba, by);
+              } else {
+                const int by = ti.g * F.b_rows_group + kseg * F.b_rows_kseg + ti.nt * BN;
+                tma_load_2d(mb, &full_bar[stage], b_dst, kba, by);
+              }
             }
           }
         }
-        if constexpr (kMx) {
-          uint8_t* sf = sSF + stage * C::kSFBytes;
-#pragma unroll
-          for (int j = 0; j < kTR / 32; ++j) {  // A rows past the matrix read nothing (zeros)
-            const int row = ti.a_row0 + lane + 32 * j;
-            const bool in = row < F.a_rows;
-            cp_async4(sf + 16 * lane + 4 * j, F.a_scale + (int64_t)(in ? row : 0) * F.a_scale_ld + 4 * kb, in);
-          }
-#pragma unroll
-          for (int j = 0; j < BN / 32; ++j) {  // B rows: W1 then W3 halves (SwiGLU), else BN rows
-            const int n = lane + 32 * j;
-            const uint8_t* src;
-            if (EPI == kSwiglu) {
-              const bool up = n >= BN / 2;
-              const int64_t brow =
-                  (int64_t)ti.g * F.b_rows_group + (int64_t)ti.nt * (BN / 2) + (up ? n - BN / 2 : n);
-              src = (up ? F.b3_scale : F.b_scale) + brow * F.scale_ld;
-            } else {
-              src = F.b_scale + ((int64_t)ti.g * F.b_rows_group + (int64_t)ti.nt * BN + n) * F.scale_ld;
-            }
-            cp_async4(sf + 512 * (1 + (j >> 2)) + 16 * lane + 4 * (j & 3), src + 4 * kb, true);
-          }
-          cp_async_arrive_noinc(&full_bar[stage]);
-        }
+        if constexpr (kMx && !kScaleWarp) mx_scale_copies(ti, s_fam[ti.fam], kb, stage);
         if (gather) {
           __syncwarp();  // the stage's expected bytes are set before any gathered row lands
           tma_gather4(ma, &full_bar[stage], sA + stage * C::kABytes + lane * (4 * BK * 2), (k0 + kb) * BK, gr[0],
@@ -754,10 +782,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       record_error(P.status, kErrTimeout, 201, (int32_t)blockIdx.x, 0);
       s_abort = 1;
       // let our own copies land before the CTA's shared memory goes away (every lane's
-      // gathers of a stage complete on the same barrier as lane 0's copies)
+      // gathers of a stage complete on the same barrier as lane 0's copies). One 2 s
+      // bound for all stages: a stage whose scale copies the aborted scale warp never
+      // issued does not complete, and by then the tensor copies have long landed.
+      const unsigned long long t0 = globaltimer();
       for (int s = 0; s < kStages; ++s)
         if (last_parity[s] >= 0) {
-          const unsigned long long t0 = globaltimer();
           while (!mbar_try_wait<true>(&full_bar[s], (uint32_t)last_parity[s]) && globaltimer() - t0 < kTimeoutNs) {
           }
         }
@@ -793,14 +823,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             // its tensor-memory columns; a stage's columns are reused only after the stage
             // has been refilled, i.e. after the MMAs that read them have completed
             fence_proxy_async_smem();
-            const uint32_t sfa = tmem_base + (uint32_t)(2 * BN + stage * C::kSFCols);
-            const uint32_t sf_smem = smem_u32(sSF + stage * C::kSFBytes);
-            tc_cp_sf(sfa, sf_desc(sf_smem));
-            tc_cp_sf(sfa + 4, sf_desc(sf_smem + 512));
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)  // K = 32 codes per MMA: the scale word's byte kk
-              umma_mx(d_tmem, sw128_desc(a_addr + kk * 32), sw128_desc(b_addr + kk * 32),
-                      idesc_mx(BM, BN, (uint32_t)kk), sfa, sfa + 4, (kb | kk) != 0 ? 1u : 0u);
+            for (int a = 0; a < C::kAtoms; ++a) {
+              const uint32_t sfa = tmem_base + (uint32_t)(2 * BN + stage * C::kSFCols + a * C::kSFAtomCols);
+              const uint32_t sf_smem = smem_u32(sSF + stage * C::kSFBytes + a * C::kSFAtomBytes);
+              tc_cp_sf(sfa, sf_desc(sf_smem));
+              tc_cp_sf(sfa + 4, sf_desc(sf_smem + 512));
+              const uint32_t aa = a_addr + a * C::kAAtomBytes, ba = b_addr + a * C::kBAtomBytes;
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)  // K = 32 codes per MMA: the scale word's byte kk
+                umma_mx(d_tmem, sw128_desc(aa + kk * 32), sw128_desc(ba + kk * 32), idesc_mx(BM, BN, (uint32_t)kk),
+                        sfa, sfa + 4, (kb | a | kk) != 0 ? 1u : 0u);
+            }
           } else {
 #pragma unroll
             for (int kk = 0; kk < BK / UMMA_K; ++kk) {
@@ -835,6 +869,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       const unsigned long long t0 = globaltimer();
       while (!mbar_try_wait<true>(&done_bar, 0u) && globaltimer() - t0 < kTimeoutNs) {
       }
+    }
+  } else if (kScaleWarp && warp == 2) {
+    // ---------------- scale copies (MXFP8 decode tiles) ----------------
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int it = 0, tile, half; ok && walk.item(it, tile, half); ++it) {
+      const TileInfo ti = decode_tile<false, kTR>(tile, s_start, G, G0, s_fam, off, 0);
+      const Family& F = s_fam[ti.fam];
+      for (int kb = 0; kb < F.k_blocks; ++kb) {
+        int w_ok = 1;
+        if (lane == 0) w_ok = mbar_wait<false>(&empty_bar[stage], phase ^ 1u, abort_flag, P.wait_ns) ? 1 : 0;
+        if (!__shfl_sync(kFull, w_ok, 0)) {
+          ok = false;
+          break;
+        }
+        mx_scale_copies(ti, F, kb, stage);
+        if (++stage == kStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    if (!ok && lane == 0) {
+      record_error(P.status, kErrTimeout, 205, (int32_t)blockIdx.x, 0);
+      s_abort = 1;
     }
   } else {
     // ---------------- epilogue warps ----------------
@@ -1317,7 +1378,7 @@ cudaError_t launch_ffn_mx(const Plan& p, const void* xp, const int32_t* expert_o
     f.groups = (int32_t)p.E;
     f.m_from_off = 1;
     f.n_tiles = (int32_t)(p.F / brows);
-    f.k_blocks = f.kseg_blocks = (int32_t)(p.d / 128);
+    f.k_blocks = f.kseg_blocks = (int32_t)(p.d / (128 * mx_atoms(rows)));
     f.b_rows_group = (int32_t)p.F;
     f.a_map = 0;
     f.b_map = 2;
@@ -1355,7 +1416,7 @@ cudaError_t launch_ffn_mx(const Plan& p, const void* xp, const int32_t* expert_o
     f.groups = (int32_t)p.E;
     f.m_from_off = 1;
     f.n_tiles = (int32_t)(p.d / 128);
-    f.k_blocks = f.kseg_blocks = (int32_t)(p.F / 128);
+    f.k_blocks = f.kseg_blocks = (int32_t)(p.F / (128 * mx_atoms(rows)));
     f.b_rows_group = (int32_t)p.d;
     f.a_map = 0;
     f.b_map = 2;
