@@ -298,7 +298,11 @@ MOE_API moe_status moe_permute(const moe_config* cfg, const void* x, const int32
  *      sums (f, P, aux, z over n_tokens_total; counts are the batch's); dropped,
  *      rows and kept in stats are this shard's;
  *   4. moe_expert_ffn and moe_combine on the shard's rows, as for a whole batch.
- * The result for each token equals that of the unsharded batch.
+ * Every token's routing, rows and output equal the unsharded batch's bit for bit for any
+ * cut. The statistics' partial sums are fp32 sums over router tiles (8, 16 or 32
+ * tokens, chosen from n_tokens_total) before the exact fixed-point addition, so they
+ * equal the unsharded batch's bit for bit when every shard starts at a multiple of 32
+ * tokens, and otherwise to fp32 rounding.
  *  shard_counts  [n_shards][E] int32 device; shard_rank in [0, n_shards).
  *  Other arguments as moe_permute (tok_rows [N, k], no tok_off). */
 MOE_API moe_status moe_permute_shard(const moe_config* cfg, const void* x, const int32_t* idx, const float* gate,

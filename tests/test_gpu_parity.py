@@ -105,6 +105,12 @@ SMALL = [
        has_bias=True),
     wl("bf16_tail_split_down256", n_tokens=10000, d_model=256, d_ff=64, n_experts=64, top_k=2,
        capacity_factor=0.0, gating="softmax_topk_renorm"),
+    # the tensor-core router (logits GEMM, then the routing kernel) at 16- and 32-token
+    # router tiles: every gate rule, ragged last tiles, k = 1 and k = 8, E = 33 .. 256
+    wl("bf16_tc_router_renorm", n_tokens=4100, d_model=256, d_ff=128, n_experts=48, top_k=5,
+       capacity_factor=1.25, gating="softmax_topk_renorm", act="swiglu", logit_bias_max=2.0),
+    wl("bf16_tc_router_B_k8", n_tokens=4096, d_model=128, d_ff=64, n_experts=256, top_k=8, capacity_factor=1.0,
+       gating="topk_softmax"),
 ]
 
 
@@ -112,6 +118,18 @@ SMALL = [
 def test_small_layers(w):
     layer, t, res = run_gpu(w)
     check(w, t, res)
+
+
+def test_tc_router_32_token_tiles():
+    """The tensor-core router with 32-token router tiles (batches of >= 16384 tokens), k = 1,
+    E = 33, a ragged last tile: routing, gates and statistics on every token, outputs
+    on 512 sampled tokens (k = 1 with the renormalised gate, so every output is one
+    expert's: the unnormalised top-1 gate makes this narrow layer's outputs so heavy
+    tailed that even the exact outputs with bf16 hidden activations miss the bar)."""
+    w = wl("bf16_tc_router_k1_tile32", n_tokens=16400, d_model=128, d_ff=128, n_experts=33, top_k=1,
+           capacity_factor=1.25, gating="softmax_topk_renorm")
+    layer, t, res = run_gpu(w)
+    print(check(w, t, res, n_sample=512))
 
 
 def test_zero_router_ties():

@@ -23,6 +23,9 @@ CASES = [
     # drops cross the shard boundary; tensor-core router (E > 32) with a logit offset
     (Workload("shard_bf16_e40", 1024, 128, 128, 40, 4, 1.0, "softmax_topk", "swiglu", "bf16", logit_bias_max=2.0,
               n_shared=1, d_ff_shared=128), (0, 384, 1024)),
+    # tensor-core router with 16-token router tiles (shards cut at a router tile's start)
+    (Workload("shard_bf16_e64_tile16", 4200, 128, 128, 64, 4, 1.0, "softmax_topk_renorm", "swiglu", "bf16",
+              logit_bias_max=2.0), (0, 1008, 4200)),
     # warp-MMA router, GELU with bias, heavy drops, three shards of unequal size
     (Workload("shard_bf16_e8_drops", 2048, 128, 256, 8, 2, 0.5, "topk_softmax", "gelu", "bf16", has_bias=True,
               logit_bias_max=3.0), (0, 640, 672, 2048)),
