@@ -241,22 +241,27 @@ def run_e2e(moe, layer, x, steps: int, dev) -> float:
 
 
 def algorithmic(w, rows, touched):
-    """Algorithmic FLOPs / bytes per forward (kept rows only, each operand once)."""
+    """Algorithmic FLOPs / bytes per forward (kept rows only, each operand once). The
+    gate-scaled expert rows Yp and the shared experts' sum Ys are fp32 for every layer
+    dtype; MXFP8 experts read and write their activations as codes plus one scale byte
+    per 32."""
     b = 4 if w.dtype == "f32" else 2
-    bw = 1 + 1 / 32 if getattr(w, "expert_weights", "bf16") == "mxfp8" else b  # routed weight bytes per element
+    mx = getattr(w, "expert_weights", "bf16") == "mxfp8"
+    bw = 1 + 1 / 32 if mx else b  # routed weight bytes per element
+    ba = 1 + 1 / 32 if mx else b  # routed experts' activation bytes per element (xp, H)
     m_up = 2 if w.act == "swiglu" else 1
-    N, d, F, E, S, Fs = w.n_tokens, w.d_model, w.d_ff, w.n_experts, w.n_shared, w.d_ff_shared
+    N, d, F, E, S, Fs, k = w.n_tokens, w.d_model, w.d_ff, w.n_experts, w.n_shared, w.d_ff_shared, w.top_k
     up_flops = 2 * rows * d * F * m_up + 2 * N * d * S * Fs * m_up
     down_flops = 2 * rows * F * d + 2 * N * S * Fs * d
     w_up = touched * F * d * m_up * bw + S * Fs * d * m_up * b
     w_down = touched * d * F * bw + S * d * Fs * b
     return dict(
         up_flops=up_flops, down_flops=down_flops,
-        up_bytes=rows * d * b + N * d * b * (S > 0) + w_up + rows * F * b + N * S * Fs * b,
-        down_bytes=rows * F * b + N * S * Fs * b + w_down + rows * d * b + N * d * b * (S > 0),
-        route_bytes=N * d * b + E * d * b + N * w.top_k * 8 + N * E * 4,
-        permute_bytes=N * d * b + rows * d * b + rows * 8 + N * w.top_k * 8,
-        combine_bytes=rows * d * b + N * d * b * (2 if S > 0 else 1) + N * w.top_k * 4,
+        up_bytes=rows * d * ba + N * d * b * (S > 0) + w_up + rows * F * ba + N * S * Fs * b,
+        down_bytes=rows * F * ba + N * S * Fs * b + w_down + rows * d * 4 + N * d * 4 * (S > 0),
+        route_bytes=N * d * b + E * d * b + N * k * 8 + N * E * 4,
+        permute_bytes=N * d * b + rows * d * ba + rows * 8 + N * k * 8,
+        combine_bytes=rows * d * 4 + N * d * 4 * (S > 0) + N * d * b + N * k * 4,
     )
 
 

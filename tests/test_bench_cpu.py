@@ -28,9 +28,24 @@ def test_algorithmic_counts(bench):
     assert a["down_flops"] == a["up_flops"]
     # up reads xp and W1 (+ bias-free byte count) and writes H, each once
     assert a["up_bytes"] == rows * w.d_model * 2 + w.n_experts * w.d_ff * w.d_model * 2 + rows * w.d_ff * 2
+    # down reads H and W2 and writes the fp32 gate-scaled rows Yp; the combine reads Yp
+    # (fp32) and writes the bf16 output
+    assert a["down_bytes"] == rows * w.d_ff * 2 + w.n_experts * w.d_ff * w.d_model * 2 + rows * w.d_model * 4
+    assert a["combine_bytes"] == rows * w.d_model * 4 + w.n_tokens * w.d_model * 2 + w.n_tokens * w.top_k * 4
     sw = WORKLOADS["mixtral_prefill"]
     b = bench.algorithmic(sw, sw.n_tokens * sw.top_k, sw.n_experts)
     assert b["up_flops"] == 2 * 2 * sw.n_tokens * sw.top_k * sw.d_model * sw.d_ff  # SwiGLU: W1 and W3
+    # shared experts: Ys (fp32) written by the down-projection, read by the combine
+    lf = WORKLOADS["large_fine"]
+    c = bench.algorithmic(lf, lf.n_tokens * lf.top_k, lf.n_experts)
+    N, d, R = lf.n_tokens, lf.d_model, lf.n_tokens * lf.top_k
+    assert c["combine_bytes"] == R * d * 4 + N * d * 4 + N * d * 2 + N * lf.top_k * 4
+    # MXFP8 experts: weights and routed activations at 1 + 1/32 bytes per element
+    fq = WORKLOADS["mixtral_decode_fp8"]
+    q = bench.algorithmic(fq, fq.n_tokens * fq.top_k, fq.n_experts)
+    bq = 1 + 1 / 32
+    R = fq.n_tokens * fq.top_k
+    assert q["up_bytes"] == pytest.approx(R * fq.d_model * bq + 8 * 2 * fq.d_ff * fq.d_model * bq + R * fq.d_ff * bq)
 
 
 @pytest.mark.parametrize("name,bound", [("small_bf16", "tensor"), ("mixtral_prefill", "tensor"),
