@@ -546,7 +546,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const __grid_constant__ CUtensorMap m4, const __grid_constant__ CUtensorMap m5,
                         const __grid_constant__ CUtensorMap o0, const __grid_constant__ CUtensorMap o1,
                         const __grid_constant__ Params P) {
-  static_assert(!PAIR || EPI == kLinear, "CTA pairs serve the down-projection (one B map, linear epilogue)");
+  static_assert(!PAIR || EPI == kLinear || EPI == kLogits,
+                "CTA pairs serve the down-projection and the router logits (one B map, row-wise epilogues)");
   using C = Cfg<BN, PAIR, MXR>;
   constexpr bool kMx = C::kMx;
   constexpr int kTR = C::kTileRows;
@@ -1313,9 +1314,12 @@ cudaError_t launch_router_logits_tc(const Plan& p, const void* x, const void* w_
   const int bn = p.E <= 64 ? 64 : (p.E <= 128 ? 128 : 256);
   const int64_t kb = p.d / BK;
   if (splits < 1 || kb % splits) return cudaErrorInvalidValue;
+  // 256-wide tiles run on CTA pairs (each CTA stages half of W_r's tile: shallower
+  // stages, so a deeper ring of x in flight) once the batch has two 128-row tiles
+  const bool pair = bn == 256 && p.N > BM;
   CUtensorMap maps[8];
   if (!make_map(&maps[0], x, p.N, p.d, BM)) return cudaErrorInvalidValue;
-  if (!make_map(&maps[1], w_router, p.E, p.d, bn)) return cudaErrorInvalidValue;
+  if (!make_map(&maps[1], w_router, p.E, p.d, pair ? bn / 2 : bn)) return cudaErrorInvalidValue;
   for (int i = 2; i < 8; ++i) maps[i] = maps[0];
   Params P{};
   Family& f0 = P.fam[0];
@@ -1334,7 +1338,8 @@ cudaError_t launch_router_logits_tc(const Plan& p, const void* x, const void* w_
   f0.n_valid = p.E;
   P.expert_off = nullptr;
   P.status = status;
-  P.wait_ns = wait_limit_ns();
+  P.wait_ns = pair ? kTimeoutNs : wait_limit_ns();  // the pair form keeps the full bound
+  if (pair) return launch_pair_t<256, kLogits>(maps, P, ceil_div(p.N, 2 * BM) * f0.n_tiles * splits, st);
   return launch_bn<kLogits>(bn, maps, P, ceil_div(p.N, BM) * f0.n_tiles * splits, st);
 }
 
