@@ -98,6 +98,13 @@ SMALL = [
        gating="expert_choice", act="swiglu", n_shared=2, d_ff_shared=128),
     wl("bf16_pair_skewed", n_tokens=1200, d_model=256, d_ff=256, n_experts=2, top_k=1, capacity_factor=0.0,
        gating="softmax_topk_renorm", logit_bias_max=3.0),
+    # the up-projection on CTA pairs (256-wide tiles: experts averaging >= 8 row tiles, or
+    # expert choice with C a multiple of 256): SwiGLU with W1 staged by the leader and W3
+    # by the peer, ragged last pair tiles, shared experts; GELU + bias in expert choice
+    wl("bf16_pair_up_swiglu_shared", n_tokens=2100, d_model=256, d_ff=256, n_experts=2, top_k=1,
+       capacity_factor=0.0, act="swiglu", n_shared=1, d_ff_shared=256, logit_bias_max=1.0),
+    wl("bf16_pair_up_gelu_bias_ec", n_tokens=1024, d_model=256, d_ff=256, n_experts=4, top_k=2,
+       capacity_factor=1.0, gating="expert_choice", has_bias=True),
     # more tiles than CTAs with a last wave at most half full: its tiles are cut into
     # two halves of the tile's columns on two CTAs (183 tiles: up 256 -> 128-column and
     # down 64 -> 32-column halves; 192 tiles: up 64 -> 32, down 256 -> 128 on single CTAs)
