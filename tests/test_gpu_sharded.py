@@ -26,6 +26,10 @@ CASES = [
     # tensor-core router with 16-token router tiles (shards cut at a router tile's start)
     (Workload("shard_bf16_e64_tile16", 4200, 128, 128, 64, 4, 1.0, "softmax_topk_renorm", "swiglu", "bf16",
               logit_bias_max=2.0), (0, 1008, 4200)),
+    # MXFP8 experts: each shard quantises its own rows (xp codes + scales) against the
+    # whole batch's capacity
+    (Workload("shard_mxfp8_drops", 1536, 512, 512, 8, 2, 0.8, "softmax_topk", "swiglu", "bf16",
+              logit_bias_max=2.0, expert_weights="mxfp8"), (0, 512, 1536)),
     # warp-MMA router, GELU with bias, heavy drops, three shards of unequal size
     (Workload("shard_bf16_e8_drops", 2048, 128, 256, 8, 2, 0.5, "topk_softmax", "gelu", "bf16", has_bias=True,
               logit_bias_max=3.0), (0, 640, 672, 2048)),
