@@ -378,8 +378,10 @@ MOE_API moe_status moe_forward_traced(const moe_config* cfg, const void* x, cons
  *    launched.
  *  - All calls on a device share that array and it keeps the last call's
  *    contents: calls that overlap on the GPU race, so serialise them.
- *  - The first call on each device looks up the array's address; make it before
- *    any stream capture.
+ *  - The first call on each device looks up the array's address and keeps it for
+ *    the life of the process; make it before any stream capture, and do not use
+ *    the library across a cudaDeviceReset (or any other re-creation of the
+ *    device's primary context), after which that address is stale.
  *  - stats is required. Layers routed on the tensor cores (bf16, E > 32) need
  *    logits, and expert choice needs probs (the buffers moe_route would otherwise
  *    keep in its workspace); missing ones give MOE_ERR_INVALID_ARG.
