@@ -554,13 +554,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int kStages = C::kStages;
   constexpr int kOutCols = EPI == kSwiglu ? BN / 2 : BN;
   constexpr uint32_t kIdesc = idesc_bf16(PAIR ? 2 * BM : BM, BN);
-  // half tiles (N = BN / 2) for the last wave: bf16, one-B-map, whole-width epilogues only
-  constexpr bool kCanSplit = !PAIR && !kMx && (EPI == kGelu || EPI == kLinear);
+  // half tiles for the last wave (bf16 single CTAs): N = BN / 2 against half of the staged B
+  // tile (GELU, linear), or two N = BN / 4 MMAs against a quarter of each of its W1 and W3
+  // halves (SwiGLU)
+  // (SwiGLU halves: output columns [h BN/4, (h + 1) BN/4), from W1 and W3 rows of that range,
+  // whole 32-column chunks, so BN >= 128)
+  constexpr bool kCanSplit = !PAIR && !kMx && (EPI == kGelu || EPI == kLinear || (EPI == kSwiglu && BN >= 128));
   // MXFP8 decode tiles (32 A rows): warp 2, whose TMEM lane quadrant holds no rows of
   // such a tile, copies the scale bytes, so the TMA producer only issues tensor copies
   constexpr bool kScaleWarp = kMx && kTR == 32;
   constexpr int kDrainWarps = kEpiWarps - (kScaleWarp ? 1 : 0);
   constexpr uint32_t kIdescHalf = idesc_bf16(BM, BN / 2);
+  constexpr uint32_t kIdescQuarter = idesc_bf16(BM, BN / 4);
 
   extern __shared__ uint8_t smem_raw[];
   // full_bar: a stage's operands have landed (MXFP8 form: and the 32 producer lanes'
@@ -808,7 +813,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int kblocks = s_fam[ti.fam].k_blocks;
         // a half tile multiplies by B's rows [half * BN/2, (half + 1) * BN/2) into accumulator columns [0, BN/2)
         const uint32_t idesc = half < 0 ? kIdesc : kIdescHalf;
-        const uint32_t b_off = half < 0 ? 0u : (uint32_t)half * (BN / 2) * 128;
+        // (SwiGLU: B rows [h BN/4, (h + 1) BN/4) of W1 and the same of W3, BN/2 rows further, into
+        // accumulator columns [0, BN/4) and [BN/4, BN/2))
+        const uint32_t b_off =
+            half < 0 ? 0u : (uint32_t)half * (EPI == kSwiglu ? BN / 4 : BN / 2) * 128;
         if (!mbar_wait<false>(&tempty_bar[acc], acc_phase ^ 1u, abort_flag, P.wait_ns)) {
           ok = false;
           break;
@@ -843,12 +851,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else {
 #pragma unroll
             for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-              if constexpr (PAIR)
+              if constexpr (PAIR) {
                 umma_bf16_pair(d_tmem, sw128_desc(a_addr + kk * UMMA_K * 2), sw128_desc(b_addr + kk * UMMA_K * 2),
                                kIdesc, (kb | kk) != 0 ? 1u : 0u);
-              else
+              } else if (EPI == kSwiglu && half >= 0) {
+                umma_bf16(d_tmem, sw128_desc(a_addr + kk * UMMA_K * 2), sw128_desc(b_addr + kk * UMMA_K * 2),
+                          kIdescQuarter, (kb | kk) != 0 ? 1u : 0u);
+                umma_bf16(d_tmem + BN / 4, sw128_desc(a_addr + kk * UMMA_K * 2),
+                          sw128_desc(b_addr + (BN / 2) * 128 + kk * UMMA_K * 2), kIdescQuarter, (kb | kk) != 0 ? 1u : 0u);
+              } else {
                 umma_bf16(d_tmem, sw128_desc(a_addr + kk * UMMA_K * 2), sw128_desc(b_addr + kk * UMMA_K * 2),
                           idesc, (kb | kk) != 0 ? 1u : 0u);
+              }
             }
           }
           umma_commit_t<PAIR>(&empty_bar[stage]);
@@ -916,8 +930,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const TileInfo ti = decode_tile<PAIR, kTR>(tile, s_start, G, G0, s_fam, off, (int)rank);
       const Family& F = s_fam[ti.fam];
       // output columns of this CTA's share of the tile: all, or one half (accumulator columns 0..)
-      const int out_cols = half < 0 ? kOutCols : BN / 2;
-      const int col_shift = half < 0 ? 0 : half * (BN / 2);
+      constexpr int kHalfCols = EPI == kSwiglu ? BN / 4 : BN / 2;
+      const int out_cols = half < 0 ? kOutCols : kHalfCols;
+      const int col_shift = half < 0 ? 0 : half * kHalfCols;
+      const int u_cols = half < 0 ? BN / 2 : BN / 4;  // SwiGLU: accumulator column of the W3 half
       int got = 0;
       if (lane == 0) got = mbar_wait<true>(&tfull_bar[acc], acc_phase, abort_flag, P.wait_ns) ? 1 : 0;
       got = __shfl_sync(kFull, got, 0);
@@ -1113,7 +1129,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t va[32], ua[32];
       for (int c = part * 32; q * 32 < kTR && c < out_cols; c += 32 * (kEpiWarps / 4)) {
         tmem_ld32(tbase + (uint32_t)c, va);
-        if (EPI == kSwiglu) tmem_ld32(tbase + (uint32_t)(BN / 2 + c), ua);
+        if (EPI == kSwiglu) tmem_ld32(tbase + (uint32_t)(u_cols + c), ua);
         tmem_ld_wait(va);
         if (EPI == kSwiglu) reg_fence(ua);
         finish_chunk(va, ua, c);

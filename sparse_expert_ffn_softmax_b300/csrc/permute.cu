@@ -298,19 +298,29 @@ __global__ void __launch_bounds__(kWarps * 32) scatter_kernel(
       return;
     }
   }
+  // each lane keeps kCopyUnroll 16-byte loads of the row in flight before the stores
+  constexpr int kCopyUnroll = 4;
   for (int tt = warp; tt < TT; tt += kWarps) {
     const int64_t tok = tile * TT + tt;
     if (tok >= N) break;
     const int32_t my_row = lane < k ? s_rows[tt * k + lane] : -1;
     const uint4* src = reinterpret_cast<const uint4*>(x) + tok * nchunk;
-    for (int64_t c0 = cbeg; c0 < cend; c0 += 32) {
-      const int64_t c = c0 + lane;
-      const bool act = c < cend;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (act) v = __ldg(src + c);
+    for (int64_t c0 = cbeg; c0 < cend; c0 += 32 * kCopyUnroll) {
+      uint4 v[kCopyUnroll];
+#pragma unroll
+      for (int u = 0; u < kCopyUnroll; ++u) {
+        const int64_t c = c0 + 32 * u + lane;
+        v[u] = c < cend ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+      }
       for (int j = 0; j < k; ++j) {
-        const int32_t row = __shfl_sync(kFull, my_row, j);
-        if (act && row >= 0) reinterpret_cast<uint4*>(xp)[(int64_t)row * nchunk + c] = v;
+        const int32_t row = __shfl_sync(kFull, my_row, j);  // the same in every lane
+        if (row < 0) continue;
+        uint4* dst = reinterpret_cast<uint4*>(xp) + (int64_t)row * nchunk;
+#pragma unroll
+        for (int u = 0; u < kCopyUnroll; ++u) {
+          const int64_t c = c0 + 32 * u + lane;
+          if (c < cend) dst[c] = v[u];
+        }
       }
     }
   }

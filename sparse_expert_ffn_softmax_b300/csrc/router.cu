@@ -200,15 +200,18 @@ __global__ void __launch_bounds__(kRouterWarps * 32) router_kernel(RouterArgs a)
     const float lse = m + __logf(s);
     const float inv_s = __fdividef(1.f, s);
     if (lane == 0) {
-      lse_sum += lse;
-      lse_sq += lse * lse;
+      // explicit roundings: the same sums whichever outputs a call stores (a contracted
+      // multiply-add would round once, and the compiler may contract it in one
+      // specialisation of the loop and not in another)
+      lse_sum = __fadd_rn(lse_sum, lse);
+      lse_sq = __fadd_rn(lse_sq, __fmul_rn(lse, lse));
     }
 #pragma unroll
     for (int i = 0; i < EPL; ++i) {
       const int64_t e = lane + 32 * i;
       if (e < E) {
-        const float pe = ex[i] * inv_s;
-        pacc[i] += pe;
+        const float pe = __fmul_rn(ex[i], inv_s);
+        pacc[i] = __fadd_rn(pacc[i], pe);
         if (a.probs) a.probs[t * E + e] = pe;
         if (a.logits) a.logits[t * E + e] = Lr[i];
       }
@@ -422,15 +425,15 @@ __global__ void __launch_bounds__(KS == 16 ? 512 : 256, KS == 16 ? 1 : 2) router
       const float lse = m + __logf(s);
       const float inv_s = __fdividef(1.f, s);
       if (valid && tig == 0) {
-        lse_sum += lse;
-        lse_sq += lse * lse;
+        lse_sum = __fadd_rn(lse_sum, lse);  // explicit roundings, as in router_kernel
+        lse_sq = __fadd_rn(lse_sq, __fmul_rn(lse, lse));
       }
 #pragma unroll
       for (int i = 0; i < NV; ++i) {
         const int64_t e = 8 * (i >> 1) + 2 * tig + (i & 1);
         if (valid && e < E) {
-          const float pe = ex[i] * inv_s;
-          pacc[i] += pe;
+          const float pe = __fmul_rn(ex[i], inv_s);
+          pacc[i] = __fadd_rn(pacc[i], pe);
           if (a.probs) a.probs[t * E + e] = pe;
           if (a.logits) a.logits[t * E + e] = L[i];
         }

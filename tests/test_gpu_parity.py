@@ -112,6 +112,11 @@ SMALL = [
        has_bias=True),
     wl("bf16_tail_split_down256", n_tokens=10000, d_model=256, d_ff=64, n_experts=64, top_k=2,
        capacity_factor=0.0, gating="softmax_topk_renorm"),
+    # SwiGLU halves: expert choice gives every expert C = 640 rows (5 row tiles), so the
+    # up-projection has 8 x 5 x 4 = 160 tiles on 148 SMs and its last 12 become 24 halves
+    # of 64 output columns, each two N = 64 MMAs against a quarter of the W1 and W3 halves
+    wl("bf16_tail_split_swiglu_ec", n_tokens=2560, d_model=64, d_ff=512, n_experts=8, top_k=2, capacity_factor=1.0,
+       gating="expert_choice", act="swiglu"),
     # the tensor-core router (logits GEMM, then the routing kernel) at 16- and 32-token
     # router tiles: every gate rule, ragged last tiles, k = 1 and k = 8, E = 33 .. 256
     wl("bf16_tc_router_renorm", n_tokens=4100, d_model=256, d_ff=128, n_experts=48, top_k=5,
