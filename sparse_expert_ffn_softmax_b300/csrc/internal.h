@@ -31,6 +31,7 @@ struct Plan {
   size_t stat_acc;                    // fixed-point router statistic accumulators (stats.cuh)
   size_t tile_counts, tile_base;      // permute [E][T], [E][T+1]
   size_t ec_bits;                     // [N][words]
+  size_t probs_t;                     // fp32 [E][N] (expert choice): each expert's probabilities in token order
   int64_t rsplit;                     // bf16 router GEMM split along K into this many groups (1: none)
   size_t logits_part;                 // [rsplit][N][E] fp32 partial logits when rsplit > 1
   size_t rank_base;                   // int32 [E]: assignments to each expert in earlier shards
@@ -76,7 +77,9 @@ bool router_uses_tc(const Plan& p);
 //                    permute_fuses_offsets); scatter block 0 finalises the statistics.
 enum PermuteMode { kCountsFromIdx = 0, kCountsFromRouter = 1, kFusedOffsets = 2 };
 bool permute_fuses_offsets(const Plan& p);
-cudaError_t launch_ec_select(const Plan& p, const float* probs, int32_t* idx, float* gate, void* ws,
+// probs_t (nullable): room for an expert-major copy of the probabilities [E][N], read
+// by the selection instead of the strided columns of probs.
+cudaError_t launch_ec_select(const Plan& p, const float* probs, int32_t* idx, float* gate, float* probs_t,
                              cudaStream_t st);
 // xp null: only the row metadata is written (the up-projection gathers the rows from x).
 // shard_counts (token-sharded batch, kCountsFromIdx only): [n_shards][E] assignment

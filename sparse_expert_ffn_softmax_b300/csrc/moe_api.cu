@@ -122,6 +122,7 @@ moe_status make_plan(const moe_config* c, Plan* p) {
   p->tile_counts = take((size_t)(p->E * p->tiles) * 4);
   p->tile_base = take((size_t)(p->E * (p->tiles + 1)) * 4);
   p->ec_bits = take((size_t)(p->N * p->words) * 4);
+  p->probs_t = take(p->ec ? (size_t)(p->N * p->E) * 4 : 0);  // expert-major probabilities
   p->rsplit = p->bf16 ? router_k_splits(p->Ntot, p->d, p->E) : 1;
   p->logits_part = take(p->rsplit > 1 ? (size_t)(p->rsplit * p->N * p->E) * 4 : 0);
   L.total_bytes = o;
@@ -181,7 +182,7 @@ moe_status do_route(const Plan& p, const void* x, const moe_weights* w, int32_t*
                                 tile_counts == nullptr);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   if (p.ec) {
-    e = launch_ec_select(p, pr, idx, gate, ws, st);
+    e = launch_ec_select(p, pr, idx, gate, ws_at<float>(ws, p.probs_t), st);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
   }
   return MOE_OK;

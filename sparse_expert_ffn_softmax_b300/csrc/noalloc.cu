@@ -88,6 +88,6 @@ extern "C" MOE_API moe_status moe_route_noalloc(const moe_config* cfg, const voi
     return MOE_ERR_CUDA;
   if (launch_router(p, x, w, idx, gate, logits, probs, stats, scratch, st, nullptr, true) != cudaSuccess)
     return MOE_ERR_CUDA;
-  if (p.ec && launch_ec_select(p, probs, idx, gate, scratch, st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (p.ec && launch_ec_select(p, probs, idx, gate, nullptr, st) != cudaSuccess) return MOE_ERR_CUDA;
   return MOE_OK;
 }

@@ -328,9 +328,29 @@ __global__ void __launch_bounds__(kWarps * 32) scatter_kernel(
 
 // ---- expert choice -----------------------------------------------------------
 
-__global__ void __launch_bounds__(1024) ec_select_kernel(const float* __restrict__ probs, int64_t N, int64_t E,
-                                                         int64_t cap, int32_t* __restrict__ idx,
-                                                         float* __restrict__ gate) {
+// probs [N, E] -> probs_t [E, N] through 32 x 32 tiles in shared memory (both sides coalesced).
+__global__ void __launch_bounds__(32 * 8) ec_transpose_kernel(const float* __restrict__ probs, int64_t N, int64_t E,
+                                                              float* __restrict__ probs_t) {
+  __shared__ float tile[32][33];
+  const int64_t t0 = (int64_t)blockIdx.x * 32, e0 = (int64_t)blockIdx.y * 32;
+  const int lx = threadIdx.x & 31, ly = threadIdx.x >> 5;
+  for (int r = ly; r < 32; r += 8) {
+    const int64_t t = t0 + r, e = e0 + lx;
+    tile[r][lx] = t < N && e < E ? probs[t * E + e] : 0.f;
+  }
+  __syncthreads();
+  for (int r = ly; r < 32; r += 8) {
+    const int64_t e = e0 + r, t = t0 + lx;
+    if (e < E && t < N) probs_t[e * N + t] = tile[lx][r];
+  }
+}
+
+// One block per expert over its probabilities, p(e, t) = probs[e * se + t * st] (se = N,
+// st = 1 for the expert-major copy; se = 1, st = E for [N, E]): the C-th largest by four
+// radix passes of 8 bits, then every larger one and the first ties in token order.
+__global__ void __launch_bounds__(1024) ec_select_kernel(const float* __restrict__ probs, int64_t se, int64_t st,
+                                                         int64_t N, int64_t E, int64_t cap,
+                                                         int32_t* __restrict__ idx, float* __restrict__ gate) {
   __shared__ int hist[256];
   __shared__ int s_warp[33];
   __shared__ uint32_t s_prefix;
@@ -342,9 +362,15 @@ __global__ void __launch_bounds__(1024) ec_select_kernel(const float* __restrict
     const int shift = 24 - 8 * pass;
     for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0;
     __syncthreads();
-    for (int64_t t = threadIdx.x; t < N; t += blockDim.x) {
-      const uint32_t u = __float_as_uint(probs[t * E + e]);  // p >= 0: bit order = value order
-      if ((u & pmask) == prefix) atomicAdd(&hist[(u >> shift) & 255u], 1);
+    // (N rounded up to whole blocks so every lane of a warp takes part in the match;
+    // probabilities crowd into a few bins, so lanes with equal bins add once together)
+    const int64_t n_up = (N + blockDim.x - 1) / blockDim.x * blockDim.x;
+    for (int64_t t = threadIdx.x; t < n_up; t += blockDim.x) {
+      const uint32_t u = t < N ? __float_as_uint(probs[e * se + t * st]) : 0u;  // p >= 0: bit order = value order
+      const bool in = t < N && (u & pmask) == prefix;
+      const uint32_t bin = in ? (u >> shift) & 255u : 256u;
+      const uint32_t same = __match_any_sync(kFull, bin);
+      if (in && (__ffs(same) - 1) == (int)(threadIdx.x & 31)) atomicAdd(&hist[bin], __popc(same));
     }
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -365,7 +391,7 @@ __global__ void __launch_bounds__(1024) ec_select_kernel(const float* __restrict
   int carry_eq = 0, carry_sel = 0;
   for (int64_t base = 0; base < N; base += blockDim.x) {
     const int64_t t = base + threadIdx.x;
-    const uint32_t u = t < N ? __float_as_uint(probs[t * E + e]) : 0u;
+    const uint32_t u = t < N ? __float_as_uint(probs[e * se + t * st]) : 0u;
     const int gt = (t < N && u > thr) ? 1 : 0;
     const int eq = (t < N && u == thr) ? 1 : 0;
     int tot_eq = 0, tot_sel = 0;
@@ -384,7 +410,7 @@ __global__ void __launch_bounds__(1024) ec_select_kernel(const float* __restrict
 __global__ void ec_mark_kernel(const int32_t* __restrict__ idx, const float* __restrict__ gate, int64_t N,
                                int64_t E, int64_t cap, int64_t words, uint32_t* __restrict__ bits,
                                int32_t* __restrict__ row_token, float* __restrict__ row_gate,
-                               int32_t* __restrict__ expert_off, int32_t* status) {
+                               int32_t* __restrict__ expert_off, int32_t* __restrict__ tok_off, int32_t* status) {
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i <= E) expert_off[i] = (int32_t)(i * cap);
   if (i >= E * cap) return;
@@ -397,23 +423,25 @@ __global__ void ec_mark_kernel(const int32_t* __restrict__ idx, const float* __r
     return;
   }
   atomicOr(&bits[(int64_t)t * words + (e >> 5)], 1u << (e & 31));
+  atomicAdd(&tok_off[t], 1);  // the token's row count (zeroed before), scanned next
 }
 
-__global__ void __launch_bounds__(1024) ec_tok_scan_kernel(const uint32_t* __restrict__ bits, int64_t N,
-                                                           int64_t E, int64_t words, int64_t cap,
+// tok_off[t] holds token t's row count (ec_mark_kernel); each thread turns a contiguous
+// run of them into exclusive offsets in place.
+__global__ void __launch_bounds__(1024) ec_tok_scan_kernel(int64_t N, int64_t E, int64_t cap,
                                                            int32_t* __restrict__ tok_off, void* stats) {
   __shared__ int s_warp[33];
   const int64_t per = ceil_div(N, (int64_t)blockDim.x);
   const int64_t t0 = (int64_t)threadIdx.x * per;
   const int64_t t1 = t0 + per < N ? t0 + per : N;
   int local = 0;
-  for (int64_t t = t0; t < t1; ++t)
-    for (int64_t w = 0; w < words; ++w) local += __popc(bits[t * words + w]);
+  for (int64_t t = t0; t < t1; ++t) local += tok_off[t];
   int total = 0;
   int run = block_exclusive_scan(local, s_warp, &total);
   for (int64_t t = t0; t < t1; ++t) {
+    const int c = tok_off[t];
     tok_off[t] = run;
-    for (int64_t w = 0; w < words; ++w) run += __popc(bits[t * words + w]);
+    run += c;
   }
   if (threadIdx.x == 0) tok_off[N] = total;
   if (stats && threadIdx.x == 0) {
@@ -606,12 +634,13 @@ cudaError_t launch_permute_t(const Plan& p, const void* x, const int32_t* idx, c
   if (p.ec) {
     uint32_t* bits = ws_at<uint32_t>(ws, p.ec_bits);
     cudaError_t err = cudaMemsetAsync(bits, 0, (size_t)(p.N * p.words) * 4, st);
+    if (err == cudaSuccess) err = cudaMemsetAsync(tok_off, 0, (size_t)(p.N + 1) * 4, st);
     if (err != cudaSuccess) return err;
     const int64_t n = p.E * p.cap;
     const int64_t nb = ceil_div(n > p.E + 1 ? n : p.E + 1, 256);
     ec_mark_kernel<<<(unsigned)nb, 256, 0, st>>>(idx, gate, p.N, p.E, p.cap, p.words, bits, row_token, row_gate,
-                                                 expert_off, status);
-    ec_tok_scan_kernel<<<1, 1024, 0, st>>>(bits, p.N, p.E, p.words, p.cap, tok_off, stats);
+                                                 expert_off, tok_off, status);
+    ec_tok_scan_kernel<<<1, 1024, 0, st>>>(p.N, p.E, p.cap, tok_off, stats);
     ec_fill_kernel<<<(unsigned)ceil_div(p.N, kWarps), kWarps * 32, 0, st>>>(bits, idx, tok_off, p.N, p.words, p.cap,
                                                                             tok_rows);
     if (xp) {
@@ -665,10 +694,15 @@ cudaError_t launch_permute_t(const Plan& p, const void* x, const int32_t* idx, c
 
 }  // namespace
 
-cudaError_t launch_ec_select(const Plan& p, const float* probs, int32_t* idx, float* gate, void* ws,
+cudaError_t launch_ec_select(const Plan& p, const float* probs, int32_t* idx, float* gate, float* probs_t,
                              cudaStream_t st) {
-  (void)ws;
-  ec_select_kernel<<<(unsigned)p.E, 1024, 0, st>>>(probs, p.N, p.E, p.cap, idx, gate);
+  if (probs_t) {  // read each expert's probabilities from an expert-major copy (coalesced)
+    ec_transpose_kernel<<<dim3((unsigned)ceil_div(p.N, 32), (unsigned)ceil_div(p.E, 32)), 32 * 8, 0, st>>>(
+        probs, p.N, p.E, probs_t);
+    ec_select_kernel<<<(unsigned)p.E, 1024, 0, st>>>(probs_t, p.N, 1, p.N, p.E, p.cap, idx, gate);
+  } else {
+    ec_select_kernel<<<(unsigned)p.E, 1024, 0, st>>>(probs, 1, p.E, p.N, p.E, p.cap, idx, gate);
+  }
   return cudaGetLastError();
 }
 

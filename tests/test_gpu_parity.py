@@ -254,13 +254,16 @@ def test_full_size_workloads(name, n_sample):
     torch.cuda.empty_cache()
 
 
-@pytest.mark.parametrize("name,caps", [("overlap_small", (0, 64)), ("fine_skewed", (0, 96))])
+@pytest.mark.parametrize("name,caps", [("overlap_small", (0, 64)), ("overlap_mxfp8", (0, 64)), ("fine_skewed", (0, 96))])
 def test_forward_overlap_matches_forward(name, caps):
     """Shared experts on a second stream (forked at the start of the forward, joined
     before the combine) give the one-stream forward's output bit for bit."""
     if name == "overlap_small":
         w = wl("overlap_small", n_tokens=1500, d_model=256, d_ff=256, n_experts=16, top_k=4, capacity_factor=1.0,
                act="swiglu", n_shared=2, d_ff_shared=256, logit_bias_max=1.0)
+    elif name == "overlap_mxfp8":  # MXFP8 routed experts on the main stream, bf16 shared experts beside them
+        w = wl("overlap_mxfp8", n_tokens=700, d_model=512, d_ff=512, n_experts=8, top_k=2, capacity_factor=1.0,
+               act="swiglu", n_shared=1, d_ff_shared=512, expert_weights="mxfp8")
     else:
         w = WORKLOADS[name]
     t = moe.make_inputs(w, "cuda")
