@@ -288,16 +288,20 @@ def gemm_roofline(flops: float, nbytes: float, seconds: float, pk: dict, traffic
 
 
 def launches_per_step(w):
-    """Kernels the library launches per forward (the expert-choice bitmap memset not counted)."""
+    """Kernels the library launches per forward (the expert-choice memsets not counted)."""
     ec = w.gating == "expert_choice"
     tiles = -(-w.n_tokens // 32)
-    route = 1 + (1 if (w.dtype == "bf16" and w.n_experts > 32) else 0) + (2 if ec else 0)
+    # router (+ logits GEMM for bf16 with E > 32); expert choice: statistics finaliser,
+    # expert-major probability copy, selection
+    route = 1 + (1 if (w.dtype == "bf16" and w.n_experts > 32) else 0) + (3 if ec else 0)
     if ec:
         permute = 4
     else:
         permute = 1 if w.n_experts * tiles <= 8192 else 2
     if w.dtype == "bf16":
-        ffn = 2
+        # MXFP8 routed experts run beside separate bf16 launches of the shared experts
+        mx = getattr(w, "expert_weights", "bf16") == "mxfp8"
+        ffn = 2 * (2 if (mx and w.n_shared > 0) else 1)
     else:
         ffn = 2 * (2 if w.n_shared > 0 else 1)
     return route + permute + ffn + 1

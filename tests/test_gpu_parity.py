@@ -336,3 +336,45 @@ def test_gather_rows_full_size_layer():
     b = moe.Layer(w, t).forward(t["x"])
     torch.cuda.synchronize()
     assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("name", ["bf16_graph_shared", "mixtral_decode_fp8", "bf16_graph_ec"])
+def test_cuda_graph_replay_matches_eager(name):
+    """The forward is stream-ordered with no host synchronisation, so it can be captured
+    into a CUDA graph: replays of the captured forward (new inputs copied into the same
+    buffer in between) give the eager forward's outputs and statistics bit for bit."""
+    if name == "mixtral_decode_fp8":
+        w = WORKLOADS[name]
+    elif name == "bf16_graph_shared":
+        w = wl(name, n_tokens=1100, d_model=256, d_ff=512, n_experts=40, top_k=4, capacity_factor=1.0,
+               act="swiglu", n_shared=1, d_ff_shared=256, logit_bias_max=1.0)
+    else:
+        w = wl(name, n_tokens=600, d_model=128, d_ff=256, n_experts=8, top_k=2, capacity_factor=1.0,
+               gating="expert_choice", has_bias=True)
+    t = moe.make_inputs(w, "cuda")
+    layer = moe.Layer(w, t)
+    x2 = moe.make_inputs(w, "cuda", with_weights=False, x_seed=7)["x"]
+    refs = []
+    for x in (t["x"], x2):
+        refs.append((layer.forward(x).clone(), layer.read_stats()))
+    xbuf = t["x"].clone()
+    out = torch.empty_like(xbuf)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):  # warm-up outside the capture (first launches set kernel attributes)
+        moe.forward(layer.cfg, xbuf, layer.w, out, layer.stats, layer.ws, s)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        moe.forward(layer.cfg, xbuf, layer.w, out, layer.stats, layer.ws, torch.cuda.current_stream())
+    for x, (ref_out, ref_st) in zip((t["x"], x2, t["x"]), refs + refs[:1]):
+        xbuf.copy_(x)
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref_out)
+        st = layer.read_stats()
+        for key in ("aux_loss", "z_loss", "dropped", "rows"):
+            assert st[key] == ref_st[key], key
+        assert torch.equal(st["P"], ref_st["P"]) and torch.equal(st["counts"], ref_st["counts"])
+    assert moe.get_device_status(layer.cfg, layer.ws) == (0, 0)
