@@ -38,11 +38,12 @@ struct Plan {
 };
 
 // K groups of the bf16 logits GEMM (layers with more than 32 experts) for a batch
-// of N tokens, a function of the shapes alone: fewer than 16 128-token tiles with a
-// long K leave most SMs idle, so the K range is split until about one CTA per SM
-// runs (each keeping >= 4 K blocks).
+// of N tokens, a function of the shapes alone: fewer than 75 128-token tiles leave at
+// least half the SMs idle, so the K range is split into floor(148 / tiles) equal
+// groups (each keeping >= 4 K blocks), whose partial sums the routing kernel adds in
+// order (measured on the 8192-token, 160-expert layer: route 69.8 -> 66.7 us with two).
 constexpr int64_t kRouterTcMinE = 33;        // bf16 layers with more experts route from tensor-core logits
-constexpr int64_t kRouterSplitMaxTiles = 16;  // K split only below this many 128-token tiles
+constexpr int64_t kRouterSplitMaxTiles = 75;  // K split only below this many 128-token tiles
 int64_t router_k_splits(int64_t N, int64_t d, int64_t E);
 
 moe_status make_plan(const moe_config* cfg, Plan* p);

@@ -138,7 +138,7 @@ int64_t router_k_splits(int64_t N, int64_t d, int64_t E) {
   int64_t s = kSms / mt;
   if (s > kb / kMinBlocks) s = kb / kMinBlocks;
   while (s > 1 && kb % s) --s;  // equal K ranges
-  return s > 2 ? s : 1;         // two halves do not pay for the extra pass over partial sums
+  return s > 1 ? s : 1;
 }
 
 namespace {
