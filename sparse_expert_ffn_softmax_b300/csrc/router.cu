@@ -118,20 +118,29 @@ __global__ void __launch_bounds__(kRouterWarps * 32) router_kernel(RouterArgs a)
     // ---- logits of token t: lane l holds expert l + 32 i in Lr[i] ----
     float Lr[EPL];
     if (kLogitsIn) {
+      // the lane's experts' logits: one slab, or K-split slabs added in order (slab by
+      // slab, the lane's EPL loads of a slab in flight together)
+      const float* src = a.logits_in + t * E;
 #pragma unroll
       for (int i = 0; i < EPL; ++i) {
         const int64_t e = lane + 32 * i;
-        float acc = 0.f;
-        if (e < E) {
-          const float* src = a.logits_in + t * E + e;
-          if (a.splits == 1) {
-            acc = src[0];  // bias included
-          } else {
-            for (int64_t sp = 0; sp < a.splits; ++sp) acc += src[sp * a.part_stride];  // slabs in order
-            if (a.logit_bias) acc += a.logit_bias[e];
-          }
+        Lr[i] = e < E ? src[e] : 0.f;  // (one slab: bias included)
+      }
+      for (int64_t sp = 1; sp < a.splits; ++sp) {
+        float v[EPL];
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) {
+          const int64_t e = lane + 32 * i;
+          v[i] = e < E ? src[sp * a.part_stride + e] : 0.f;
         }
-        Lr[i] = e < E ? acc : -FLT_MAX;
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) Lr[i] += v[i];
+      }
+#pragma unroll
+      for (int i = 0; i < EPL; ++i) {
+        const int64_t e = lane + 32 * i;
+        if (a.splits > 1 && a.logit_bias && e < E) Lr[i] += a.logit_bias[e];
+        if (e >= E) Lr[i] = -FLT_MAX;
       }
     } else {
       const uint4* xrow = static_cast<const uint4*>(a.x) + t * nchunk;
