@@ -168,19 +168,39 @@ __global__ void __launch_bounds__(kWarps * 32) scatter_kernel(
     return;
   }
   if (kFused) {
-    // one thread per expert runs along the expert's T tile counts (E * T <= 8192): the
-    // loads of a row are independent, so they are in flight together
-    for (int64_t e = threadIdx.x; e < E; e += blockDim.x) {
-      const int32_t* cnt = counts_or_base + e * T;
-      int pre = 0, tot = 0;
+    // each expert's counts in earlier tiles and in all tiles (E * T <= 8192): few tiles
+    // (decode batches), one thread per expert along its T counts, loads in flight
+    // together; many tiles, one warp per expert with its lanes striding over them
+    if (T <= 64) {
+      for (int64_t e = threadIdx.x; e < E; e += blockDim.x) {
+        const int32_t* cnt = counts_or_base + e * T;
+        int pre = 0, tot = 0;
 #pragma unroll 8
-      for (int64_t t = 0; t < T; ++t) {
-        const int c = cnt[t];
-        tot += c;
-        pre += t < tile ? c : 0;
+        for (int64_t t = 0; t < T; ++t) {
+          const int c = cnt[t];
+          tot += c;
+          pre += t < tile ? c : 0;
+        }
+        s_pre[e] = pre;
+        s_off[e] = tot;  // totals for now, offsets below
       }
-      s_pre[e] = pre;
-      s_off[e] = tot;  // totals for now, offsets below
+    } else {
+      for (int64_t e = warp; e < E; e += kWarps) {
+        const int32_t* cnt = counts_or_base + e * T;
+        int pre = 0, tot = 0;
+#pragma unroll 4
+        for (int64_t t = lane; t < T; t += 32) {
+          const int c = cnt[t];
+          tot += c;
+          pre += t < tile ? c : 0;
+        }
+        pre = warp_sum_int(pre);
+        tot = warp_sum_int(tot);
+        if (lane == 0) {
+          s_pre[e] = pre;
+          s_off[e] = tot;
+        }
+      }
     }
     __syncthreads();
     const int per = (int)ceil_div(E, (int64_t)blockDim.x);  // <= 2
