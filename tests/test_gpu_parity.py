@@ -294,6 +294,8 @@ FP8W = [
        act="swiglu", logit_bias_max=1.0, expert_weights="mxfp8"),
     wl("fp8w_drops_passthrough", n_tokens=900, d_model=512, d_ff=512, n_experts=8, top_k=2, capacity_factor=0.6,
        act="swiglu", logit_bias_max=2.0, expert_weights="mxfp8", drop_passthrough=True),
+    wl("fp8w_one_token", n_tokens=1, d_model=512, d_ff=512, n_experts=8, top_k=2, capacity_factor=0.0,
+       act="swiglu", n_shared=1, d_ff_shared=512, expert_weights="mxfp8"),
     wl("fp8w_ragged_32row_tiles", n_tokens=70, d_model=1536, d_ff=1024, n_experts=12, top_k=3,
        capacity_factor=0.0, gating="topk_softmax", act="gelu", has_bias=True, n_shared=1, d_ff_shared=512,
        expert_weights="mxfp8"),
