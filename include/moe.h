@@ -385,10 +385,18 @@ MOE_API moe_status moe_forward_traced(const moe_config* cfg, const void* x, cons
  *  - stats is required. Layers routed on the tensor cores (bf16, E > 32) need
  *    logits, and expert choice needs probs (the buffers moe_route would otherwise
  *    keep in its workspace); missing ones give MOE_ERR_INVALID_ARG.
- *  - Device-side conditions are not reported back (there is no workspace error
- *    word to read); arguments are checked on the host as for moe_route. */
+ *  - Arguments are checked on the host as for moe_route. Device-side conditions
+ *    go to an error word in the same array, cleared at the start of every call:
+ *    read it with moe_get_noalloc_status before the next call on the device. */
 MOE_API moe_status moe_route_noalloc(const moe_config* cfg, const void* x, const moe_weights* w, int32_t* idx,
                                      float* gate, float* logits, float* probs, void* stats, void* stream);
+
+/* moe_get_device_status for moe_route_noalloc: synchronises `stream`, reads and
+ * clears the error word of the current device's no-alloc scratch array (the
+ * last moe_route_noalloc call's). *device_error (may be NULL) receives the raw
+ * word (0 = none). Returns MOE_OK, or MOE_ERR_DEVICE_CHECK / MOE_ERR_TIMEOUT when
+ * a kernel recorded one; MOE_ERR_CUDA if the stream reports an error. */
+MOE_API moe_status moe_get_noalloc_status(void* stream, int32_t* device_error);
 
 /* Synchronises `stream`, reads and clears the workspace's device error word.
  * *device_error receives the raw word (0 = none). Returns MOE_OK, or

@@ -89,6 +89,7 @@ def _load():
         "moe_forward_overlap": ([P, P, P, P, P, P, S, P, P, P, P, c], c),
         "moe_get_device_status": ([P, P, S, P, P], c),
         "moe_route_noalloc": ([P, P, P, P, P, P, P, P, P], c),
+        "moe_get_noalloc_status": ([P, P], c),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -232,6 +233,14 @@ def route_noalloc(cfg, x, w: moe_weights, idx, gate, logits=None, probs=None, st
     (for callers that cannot allocate; calls must not overlap on the GPU)."""
     _check(_lib.moe_route_noalloc(ctypes.byref(cfg), _ptr(x), ctypes.byref(w), _ptr(idx), _ptr(gate),
                                   _ptr(logits), _ptr(probs), _ptr(stats), _stream(stream)), "moe_route_noalloc")
+
+
+def get_noalloc_status(stream=None):
+    """(status code, raw error word) of the last route_noalloc call on the current device;
+    synchronises the stream and clears the word."""
+    word = ctypes.c_int32()
+    code = _lib.moe_get_noalloc_status(_stream(stream), ctypes.byref(word))
+    return int(code), int(word.value)
 
 
 def permute(cfg, x, idx, gate, xp, tok_rows, tok_off, expert_off, row_token, row_gate, stats=None, ws=None,

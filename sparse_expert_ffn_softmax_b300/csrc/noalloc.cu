@@ -91,3 +91,20 @@ extern "C" MOE_API moe_status moe_route_noalloc(const moe_config* cfg, const voi
   if (p.ec && launch_ec_select(p, probs, idx, gate, nullptr, st) != cudaSuccess) return MOE_ERR_CUDA;
   return MOE_OK;
 }
+
+// The error word sits at the start of the scratch array (offset 0 in the layout above).
+extern "C" MOE_API moe_status moe_get_noalloc_status(void* stream, int32_t* device_error) {
+  void* scratch = nullptr;
+  moe_status s = scratch_address(&scratch);
+  if (s != MOE_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int32_t word[4] = {0, 0, 0, 0};
+  cudaGetLastError();
+  if (cudaMemcpyAsync(word, scratch, sizeof word, cudaMemcpyDeviceToHost, st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemsetAsync(scratch, 0, sizeof word, st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (device_error) *device_error = word[0];
+  if (word[0] & kErrTimeout) return MOE_ERR_TIMEOUT;
+  if (word[0] & kErrIndex) return MOE_ERR_DEVICE_CHECK;
+  return MOE_OK;
+}

@@ -31,6 +31,7 @@ def _route(w, t, noalloc):
     W = moe.weights(t)
     if noalloc:
         moe.route_noalloc(cfg, t["x"], W, idx, gate, logits, probs, stats)
+        assert moe.get_noalloc_status() == (0, 0)  # no device-side condition recorded
     else:
         ws = moe.alloc_workspace(cfg)
         moe.route(cfg, t["x"], W, idx, gate, logits, probs, stats, ws)
