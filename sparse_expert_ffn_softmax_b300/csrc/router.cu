@@ -118,15 +118,30 @@ __global__ void __launch_bounds__(kRouterWarps * 32) router_kernel(RouterArgs a)
     // ---- logits of token t: lane l holds expert l + 32 i in Lr[i] ----
     float Lr[EPL];
     if (kLogitsIn) {
-      // the lane's experts' logits: one slab, or K-split slabs added in order (slab by
-      // slab, the lane's EPL loads of a slab in flight together)
+      // the lane's experts' logits: one slab, or K-split slabs added in slab order (the
+      // loads of two slabs in flight together, then their two additions in order)
       const float* src = a.logits_in + t * E;
 #pragma unroll
       for (int i = 0; i < EPL; ++i) {
         const int64_t e = lane + 32 * i;
         Lr[i] = e < E ? src[e] : 0.f;  // (one slab: bias included)
       }
-      for (int64_t sp = 1; sp < a.splits; ++sp) {
+      int64_t sp = 1;
+      for (; sp + 1 < a.splits; sp += 2) {
+        float v[2][EPL];
+#pragma unroll
+        for (int u = 0; u < 2; ++u)
+#pragma unroll
+          for (int i = 0; i < EPL; ++i) {
+            const int64_t e = lane + 32 * i;
+            v[u][i] = e < E ? src[(sp + u) * a.part_stride + e] : 0.f;
+          }
+#pragma unroll
+        for (int u = 0; u < 2; ++u)
+#pragma unroll
+          for (int i = 0; i < EPL; ++i) Lr[i] += v[u][i];
+      }
+      for (; sp < a.splits; ++sp) {
         float v[EPL];
 #pragma unroll
         for (int i = 0; i < EPL; ++i) {
