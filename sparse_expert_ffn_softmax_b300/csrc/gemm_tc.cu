@@ -441,7 +441,10 @@ __device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
 // after an atom's start, whose extra rows are never stored.
 constexpr int mx_atoms(int mxr) { return mxr == 32 ? 2 : 1; }
 
-template <int BN, bool PAIR = false, int MXR = 0>
+// kStaging: the epilogue stores through TMA and needs its per-warp staging blocks (every
+// form but the MXFP8 up-projection, whose epilogue writes codes and scales with plain
+// stores and gives that shared memory to the operand ring instead).
+template <int BN, bool PAIR = false, int MXR = 0, bool kStaging = true>
 struct Cfg {
   static constexpr bool kMx = MXR != 0;
   static constexpr int kTileRows = kMx ? MXR : BM;  // A rows of a tile
@@ -456,12 +459,14 @@ struct Cfg {
   static constexpr int kSFBytes = kAtoms * kSFAtomBytes;
   static constexpr int kTxBytes = kABytes + kBBytes;  // TMA bytes per stage
   static constexpr int kStageBytes = kTxBytes + kSFBytes;
-  static constexpr int kStages = (192 * 1024) / kStageBytes > 8 ? 8 : (192 * 1024) / kStageBytes;
+  static constexpr int kStagingTotal = kStaging ? kEpiWarps * kStagingBytes : 0;
+  static constexpr int kRingBudget = 192 * 1024 + (kEpiWarps * kStagingBytes - kStagingTotal);
+  static constexpr int kStages = kRingBudget / kStageBytes > 8 ? 8 : kRingBudget / kStageBytes;
   static constexpr int kRingBytes = kStages * kStageBytes;  // A slots, B slots, scale atoms
   static constexpr int kSFAtomCols = 4 + 4 * (BN / 128);     // tensor-memory columns of one K atom's scales
   static constexpr int kSFCols = kAtoms * kSFAtomCols;
   static constexpr int kTmemCols = kMx ? 512 : 2 * BN;  // two accumulators (+ the scale ring)
-  static constexpr size_t kSmem = (size_t)kRingBytes + (size_t)kEpiWarps * kStagingBytes + 1024;
+  static constexpr size_t kSmem = (size_t)kRingBytes + (size_t)kStagingTotal + 1024;
   static_assert(!kMx || (!PAIR && BN == 128), "MXFP8 tiles: single CTAs, 128 columns");
   static_assert(!kMx || 2 * BN + kStages * kSFCols <= 512, "accumulators and scales fit tensor memory");
   static_assert(kStages >= 3, "pipeline depth");
@@ -547,7 +552,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const __grid_constant__ CUtensorMap o0, const __grid_constant__ CUtensorMap o1,
                         const __grid_constant__ Params P) {
 
-  using C = Cfg<BN, PAIR, MXR>;
+  using C = Cfg<BN, PAIR, MXR, !(MXR != 0 && EPI != kLinear)>;
   constexpr bool kMx = C::kMx;
   constexpr int kTR = C::kTileRows;
   constexpr int kKE = C::kStageK;
@@ -922,7 +927,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;       // TMEM lane quadrant this warp may read
     const int part = ew >> 2;     // which interleaved share of the 32-column chunks
     const int r = q * 32 + lane;  // row inside the tile
-    uint8_t* staging = smem + C::kRingBytes + ew * C::kStagingBytes;
+    uint8_t* staging = smem + C::kRingBytes + (C::kStagingTotal ? ew * C::kStagingBytes : 0);  // (TMA stores only)
     bool store_pending = false;
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -1231,7 +1236,7 @@ int num_sms() {
 template <int BN, int EPI, int MXR = 0>
 cudaError_t launch_t(const CUtensorMap (&maps)[8], const Params& P, int64_t max_tiles, cudaStream_t st,
                      int64_t grid_cap = 0) {
-  using C = Cfg<BN, false, MXR>;
+  using C = Cfg<BN, false, MXR, !(MXR != 0 && EPI != kLinear)>;
   auto kern = grouped_gemm_kernel<BN, EPI, false, MXR>;
   static cudaError_t attr = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
   if (attr != cudaSuccess) return attr;
