@@ -70,3 +70,31 @@ def test_noalloc_rejects_layers_beyond_its_scratch():
     code = lib.moe_route_noalloc(ctypes.byref(cfg), p, ctypes.byref(W), p, p, p, None, p, None)
     assert code == 2  # MOE_ERR_UNSUPPORTED
     del fake
+
+
+@pytest.mark.gpu
+def test_noalloc_reports_device_timeout_and_recovers(monkeypatch):
+    """A device-side condition during moe_route_noalloc lands in the scratch error word.
+    With the single-CTA GEMM's pipeline-wait limit at 1 ns (MOE_GEMM_WAIT_LIMIT_NS), the
+    tensor-core logits GEMM of the 64-expert layer (64-wide single-CTA tiles) gives up on its
+    first unsatisfied wait and records MOE_ERR_TIMEOUT; moe_get_noalloc_status must report
+    it and clear it, and the next call with the normal limit must match moe_route."""
+    w = CASES[1]  # na_bf16_e64_tc
+    t = moe.make_inputs(w, "cuda")
+    ref = _route(w, t, noalloc=False)
+    cfg = moe.config(w)
+    N, E = w.n_tokens, w.n_experts
+    idx = torch.empty((N, w.top_k), dtype=torch.int32, device="cuda")
+    gate = torch.empty((N, w.top_k), dtype=torch.float32, device="cuda")
+    logits = torch.empty((N, E), dtype=torch.float32, device="cuda")
+    stats = torch.zeros((moe.stats_bytes(E),), dtype=torch.uint8, device="cuda")
+    monkeypatch.setenv("MOE_GEMM_WAIT_LIMIT_NS", "1")
+    moe.route_noalloc(cfg, t["x"], moe.weights(t), idx, gate, logits, None, stats)
+    code, word = moe.get_noalloc_status()
+    assert code == 6 and (word & 2), (code, word)  # MOE_ERR_TIMEOUT
+    assert moe.get_noalloc_status() == (0, 0)  # read once, cleared
+    monkeypatch.delenv("MOE_GEMM_WAIT_LIMIT_NS")
+    got = _route(w, t, noalloc=True)  # asserts a clean status itself
+    assert torch.equal(got[0], ref[0])
+    torch.testing.assert_close(got[1], ref[1], rtol=1e-5, atol=0)
+    torch.testing.assert_close(got[2], ref[2], rtol=1e-5, atol=0)
